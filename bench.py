@@ -1,0 +1,442 @@
+"""Benchmark: MFD drafting rounds per second on one GB300.
+
+Workload (default): K=8 modes, L=15 drafted positions, H=2560, V=151936,
+top-k 16, tree budget B=256, sampled verification at T=1, batch 1 -- one
+round = mfd_lmhead_topk + mfd_build_tree + mfd_verify on fresh seeded inputs
+(W fixed).  Inputs are synthetic (tree_verified_speculative_gb300.synth).
+
+Timing: CUDA events on the launching stream around the three calls of every
+round; the target logits' plant (+10 on the chosen mode's future, input
+generation that needs the round's tree) is applied between the tree and the
+verification call and is not timed.  W (778 MB) is larger than L2, so every
+round streams it from HBM.
+
+``--impl reference`` times the CPU oracle (the only reference on this
+workload) on a bounded sample per step and prints the same JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    "k8_l15_h2560_v151936_b256_t1": dict(K=8, L=15, H=2560, V=151936, n_shared=11, topk=16, B=256, T=1.0),
+    "k8_l15_h2560_v151936_b64_greedy": dict(K=8, L=15, H=2560, V=151936, n_shared=11, topk=16, B=64, T=0.0),
+    "k8_l15_h5120_v248320_b256_greedy": dict(K=8, L=15, H=5120, V=248320, n_shared=13, topk=32, B=256, T=0.0),
+}
+DEFAULT = "k8_l15_h2560_v151936_b256_t1"
+METRIC = "draft-tree rounds/s at K=8,V=151936,B=256; LM-head HBM GB/s vs GB300 peak"
+W_SEED = 2024
+N_NOISE = 4
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """dram bytes per launch of the LM-head kernel from the committed ncu summary."""
+    p = os.path.join(ROOT, "profiles", "lmhead_topk_kernel_k8_l15_h2560_v151936.md")
+    if not os.path.exists(p):
+        return None
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", open(p).read())
+    return float(m.group(1)) if m else None
+
+
+class Clocks:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if _cuda() else "gloo")
+    return ws, rank, local
+
+
+def _cuda():
+    import torch
+
+    return torch.cuda.is_available()
+
+
+def reduce_max(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if _cuda() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+def make_inputs(cfg, n_rounds, rank):
+    import concurrent.futures as cf
+
+    from tree_verified_speculative_gb300 import synth
+
+    W = synth.lm_head(cfg["V"], cfg["H"], seed=W_SEED)
+    base = 1_000_000 * (rank + 1)
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        rounds = list(ex.map(lambda r: synth.round_inputs(W, cfg["K"], cfg["L"], cfg["n_shared"], seed=base + r),
+                             range(n_rounds)))
+    rng = np.random.default_rng(base + 999)
+    noise = [synth.target_noise(cfg["B"] + 1, cfg["V"], rng) for _ in range(N_NOISE)]
+    return W, rounds, noise
+
+
+def run_gpu(args, ws, rank, local):
+    import torch
+
+    from tree_verified_speculative_gb300 import mfd, synth
+
+    cfg = WORKLOADS[args.workload]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K, L, H, V, topk, B, T = cfg["K"], cfg["L"], cfg["H"], cfg["V"], cfg["topk"], cfg["B"], cfg["T"]
+    R = K * L
+    n_rounds = args.warmup + args.steps
+    W, rounds, noise = make_inputs(cfg, n_rounds, rank)
+    Wd = W.to(dev)
+    h_all = torch.stack([r.h for r in rounds]).to(dev)
+    t_dev = [torch.from_numpy(x).to(dev) for x in noise]
+    temp = torch.tensor([T], dtype=torch.float32, device=dev)
+    seeds = torch.tensor(np.array([r.seed for r in rounds], np.uint64).view(np.int64), device=dev)
+    rd = mfd.Round(1, K, L, topk, B, V, device=dev)
+    rd.status.zero_()
+    acc_buf = torch.zeros((n_rounds,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_rounds)]
+    sites = []
+
+    def one_round(i):
+        e0, ea, e1, e3 = ev[i]
+        e0.record(stream)
+        rd.lmhead_topk(h_all[i], Wd)
+        ea.record(stream)
+        rd.build_tree()
+        e1.record(stream)
+        # input generation for verification (untimed): plant +10 on the chosen
+        # mode's future along the tree just built
+        par, tok, dep = rd.parent[0].cpu().numpy(), rd.token[0].cpu().numpy(), rd.depth[0].cpu().numpy()
+        nn = int(rd.n_nodes[0].item())
+        rows, cols = synth.plant_sites(par, tok, dep, nn, rounds[i].fut[rounds[i].target_mode])
+        sites.append((rows, cols))
+        tb = t_dev[i % N_NOISE]
+        ri = torch.from_numpy(rows).to(dev)
+        ci = torch.from_numpy(cols).to(dev)
+        planted = torch.from_numpy(noise[i % N_NOISE][rows, cols] + np.float32(10.0)).to(dev)
+        tb[ri, ci] = planted
+        s2 = torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        rd.verify(tb[None], temp, seeds[i:i + 1])
+        e3.record(stream)
+        tb[ri, ci] = torch.from_numpy(noise[i % N_NOISE][rows, cols]).to(dev)
+        acc_buf[i:i + 1].copy_(rd.accept_len)
+        return s2
+
+    v_start = [None] * n_rounds
+    for i in range(args.warmup):
+        v_start[i] = one_round(i)
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    time.sleep(0.2)
+    wall0 = time.perf_counter()
+    for i in range(args.warmup, n_rounds):
+        v_start[i] = one_round(i)
+    torch.cuda.synchronize()
+    wall1 = time.perf_counter()
+    barrier(ws)
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    st = int(rd.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {mfd.status_string(st)}")
+    lm = bd = vf = 0.0
+    for i in range(args.warmup, n_rounds):
+        e0, ea, e1, e3 = ev[i]
+        lm += e0.elapsed_time(ea)
+        bd += ea.elapsed_time(e1)
+        vf += v_start[i].elapsed_time(e3)
+    total_ms = reduce_max(lm + bd + vf, ws)
+    steps = args.steps
+    value = ws * steps / (total_ms / 1e3)
+    acc = acc_buf[args.warmup:].float().cpu().numpy()
+
+    # ------------------------------------------------------------ e2e
+    e2e = run_e2e(args, cfg, rounds, noise, sites, Wd, rd, dev)
+
+    # ------------------------------------------------------------ roofline
+    peak, peak_kind = peaks()
+    lm_us = lm / steps * 1e3
+    algo_bytes = V * H * 2 + R * H * 2
+    achieved = algo_bytes / (lm_us * 1e-6) / 1e9
+    traffic = profiled_traffic()
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "rounds/s", "n_gpus": ws, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "K": K, "L": L, "H": H, "V": V, "topk": topk, "B": B,
+                   "temperature": T, "n_req": 1, "parallelism": f"replicas{ws}" if ws > 1 else "single",
+                   "l2": "inputs larger than L2 (W = %.0f MB streamed every round)" % (V * H * 2 / 1e6),
+                   "timing": "sum of per-round CUDA-event intervals of the three calls; target plant untimed"},
+        "stages_us": {"lmhead_topk": round(lm_us, 2), "build_tree": round(bd / steps * 1e3, 2),
+                      "verify": round(vf / steps * 1e3, 2)},
+        "mean_accept_len": round(float(acc.mean()), 4),
+        "roofline": {"kernel": "mfd_lmhead_topk (lmhead_topk_kernel + merge_topk_kernel)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": algo_bytes, "traffic": traffic},
+        "gpu_launches": 4 * steps,
+        "clocks": ck,
+        "wall_s_timed_loop": round(wall1 - wall0, 3),
+        "e2e": e2e,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg, W, rounds[args.warmup], rd, noise, sites[args.warmup])
+    return out
+
+
+def run_e2e(args, cfg, rounds, noise, sites, Wd, rd, dev):
+    """Same rounds through the public API from pinned host buffers: H2D of the
+    round's hidden states and target logits, the three calls, D2H of the
+    accepted length and tokens, all inside the timed interval."""
+    import torch
+
+    from tree_verified_speculative_gb300 import synth
+
+    n = min(args.e2e_steps, len(rounds) - args.warmup)
+    warm = 2
+    idx = [args.warmup + i for i in range(n)]
+    order = idx[:warm] + idx
+    V, B, T = cfg["V"], cfg["B"], cfg["T"]
+    h_pin = {i: rounds[i].h.pin_memory() for i in set(order)}
+    t_pin = {}
+    for i in set(order):
+        rows, cols = sites[i]
+        t_pin[i] = torch.from_numpy(synth.plant(noise[i % N_NOISE], rows, cols)).pin_memory()
+    h_d = torch.empty_like(h_pin[order[0]], device=dev)
+    t_d = torch.empty((1, B + 1, V), dtype=torch.float32, device=dev)
+    temp = torch.tensor([T], dtype=torch.float32, device=dev)
+    out_pin = torch.empty((2 + rd.L + 1,), dtype=torch.int32).pin_memory()
+    seeds = torch.tensor(np.array([r.seed for r in rounds], np.uint64).view(np.int64), device=dev)
+    stream = torch.cuda.current_stream()
+    times = []
+    for j, i in enumerate(order):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        h_d.copy_(h_pin[i], non_blocking=True)
+        t_d[0].copy_(t_pin[i], non_blocking=True)
+        rd.lmhead_topk(h_d, Wd)
+        rd.build_tree()
+        rd.verify(t_d, temp, seeds[i:i + 1])
+        out_pin[0:1].copy_(rd.accept_len, non_blocking=True)
+        out_pin[1:1 + rd.L + 1].copy_(rd.out_tokens[0], non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if j >= warm:
+            times.append(e0.elapsed_time(e1))
+    ms = sum(times) / len(times)
+    return {"value": round(1e3 / ms, 2), "unit": "rounds/s", "steps": len(times),
+            "h2d_bytes_per_step": int(h_pin[order[0]].numel() * 2 + (B + 1) * V * 4),
+            "d2h_bytes_per_step": int((1 + rd.L + 1) * 4)}
+
+
+def cpu_baseline(cfg, W, r, rd, noise, site):
+    """The oracle as it stands, on this machine's host cores, on one full
+    round of the workload (LM head + log-softmax + top-k for all rows, the
+    tree from the GPU's tables, the verification walk)."""
+    import torch
+
+    import oracle
+    from tree_verified_speculative_gb300 import synth
+
+    bits = lambda x: x.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    K, L, topk, B, V, T = cfg["K"], cfg["L"], cfg["topk"], cfg["B"], cfg["V"], cfg["T"]
+    R = K * L
+    rows = R
+    hb, wb = bits(r.h[:rows]), bits(W)
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.lmhead_topk(hb, wb, topk)
+    t_lm = (time.perf_counter() - t0) * (R / rows)
+    lp = rd.tk_logp.cpu().numpy().reshape(K, L, topk)
+    tk = rd.tk_tok.cpu().numpy().reshape(K, L, topk)
+    t0 = time.perf_counter()
+    tr = oracle.build_tree(lp, tk, B)
+    t_tree = time.perf_counter() - t0
+    rows_, cols_ = synth.plant_sites(tr["parent"], tr["token"], tr["depth"], int(tr["n_nodes"]),
+                                     r.fut[r.target_mode])
+    tl = synth.plant(noise[0], rows_, cols_)
+    t0 = time.perf_counter()
+    oracle.verify(tl, tr["parent"], tr["token"], int(tr["n_nodes"]), L, T, r.seed)
+    t_ver = time.perf_counter() - t0
+    total = t_lm + t_tree + t_ver
+    return {"value": round(1.0 / total, 4), "unit": "rounds/s", "cores": oracle.default_threads(), "kind": "oracle",
+            "sample": f"one full round: LM head+log-softmax+top-k on all {R} rows, tree build and "
+                      "verification walk",
+            "stage_s": {"lmhead_topk": round(t_lm, 3), "build_tree": round(t_tree, 4), "verify": round(t_ver, 4)}}
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, ws, rank):
+    """The CPU oracle on the same workload, a bounded sample per step."""
+    import torch
+
+    import oracle
+    from tree_verified_speculative_gb300 import synth
+
+    cfg = WORKLOADS[args.workload]
+    K, L, H, V, topk, B, T = cfg["K"], cfg["L"], cfg["H"], cfg["V"], cfg["topk"], cfg["B"], cfg["T"]
+    R = K * L
+    oracle.build()
+    bits = lambda x: x.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    W = synth.lm_head(V, H, seed=W_SEED)
+    wb = bits(W)
+    n_steps = args.warmup + args.steps
+    budget_s = 150.0 / max(1, n_steps)  # whole run within a few minutes
+    # the vocabulary slice the LM-head sample covers, sized from one calibration
+    r0 = synth.round_inputs(W, K, L, cfg["n_shared"], seed=7)
+    t0 = time.perf_counter()
+    oracle.lmhead_logits(bits(r0.h), wb, 0, 4096)
+    per_vocab = (time.perf_counter() - t0) / 4096
+    n_v = int(max(256, min(V, 0.5 * budget_s / max(per_vocab, 1e-9))))
+    z_row = np.random.default_rng(3).standard_normal((1, V)).astype(np.float32)
+    noise = synth.target_noise(B + 1, V, np.random.default_rng(11))
+    times = []
+    for s in range(n_steps):
+        r = synth.round_inputs(W, K, L, cfg["n_shared"], seed=2_000_000 + s)
+        hb = bits(r.h)
+        v0 = (s * 9973) % max(1, V - n_v)
+        t0 = time.perf_counter()
+        oracle.lmhead_logits(hb, wb, v0, v0 + n_v)
+        t_lm = (time.perf_counter() - t0) * V / n_v
+        t0 = time.perf_counter()
+        oracle.logits_topk(z_row, topk)
+        t_sort = (time.perf_counter() - t0) * R
+        lp = np.sort(-np.abs(np.random.default_rng(s).normal(8, 1, size=(K, L, topk))).astype(np.float32),
+                     axis=2)[..., ::-1].copy()
+        tk = np.random.default_rng(s + 1).integers(0, V, size=(K, L, topk)).astype(np.int32)
+        for k in range(K):
+            for i in range(L):
+                tk[k, i] = np.random.default_rng(s * 1000 + k * 16 + i).choice(V, size=topk, replace=False)
+        t0 = time.perf_counter()
+        tr = oracle.build_tree(lp, tk, B)
+        t_tree = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        oracle.verify(noise, tr["parent"], tr["token"], int(tr["n_nodes"]), L, T, r.seed)
+        t_ver = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(t_lm + t_sort + t_tree + t_ver)
+    per_round = sum(times) / len(times)
+    value = 1.0 / per_round
+    cores = oracle.default_threads()
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "rounds/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_round * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "K": K, "L": L, "H": H, "V": V, "topk": topk, "B": B,
+                       "temperature": T, "n_req": 1},
+            "cpu_baseline": {"value": round(value, 4), "unit": "rounds/s", "cores": cores, "kind": "oracle",
+                             "sample": f"per step: LM head on {n_v} of {V} vocabulary rows for all {R} rows "
+                                       f"(scaled), one full-row log-softmax+top-k (scaled x{R}), full tree and "
+                                       "verification walk"},
+            "e2e": {"value": round(value, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, ws, rank)))
+        return
+    out = run_gpu(args, ws, rank, local)
+    if rank == 0:
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+/*
+ * mfd.h -- C ABI of libmfd: the per-round drafting-and-verification hot path
+ * of Multi-Future Drafting (MFD) on one GB300 (sm_103a).
+ *
+ * A round (project page "Multi-Future Drafting", How it works, steps 2-3, and
+ * Figure 2; model card "MFD drafter for Qwen3.5-4B", Model table and first
+ * paragraph) is three calls on one CUDA stream:
+ *
+ *   mfd_lmhead_topk  the K modes' drafter hidden states for the L drafted
+ *                    positions go through the target's LM head; per row an
+ *                    online log-softmax over the vocabulary and the top-k.
+ *   mfd_build_tree   the mixture DDTree: the B prefixes with the highest
+ *                    best-mode log-probability, shared prefixes built once;
+ *                    parent/token/depth arrays and the tree-attention mask.
+ *   mfd_verify       the standard tree verification walk against the
+ *                    target's per-node logits: greedy, or lossless sampled
+ *                    with a counter-based Gumbel-max.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is DEVICE memory owned by the caller, contiguous
+ *     row-major, unless marked "host".  The library allocates nothing and
+ *     keeps no per-call state; it only caches TMA descriptors (see
+ *     mfd_lmhead_topk) and per-device attributes.
+ *   - Work is enqueued on `stream` and never synchronises the host.
+ *   - The return value reports argument and launch errors synchronously.
+ *     Errors found on the device are stored into `*status` (one int32 in
+ *     device memory).  The caller sets *status to MFD_OK before the round;
+ *     a kernel that finds a problem stores its code only if *status is still
+ *     MFD_OK (the first error wins) and no kernel ever clears it.
+ *   - Scratch memory is the caller's: `ws` / `ws_bytes`, at least
+ *     mfd_workspace_size(...) bytes, 256-byte aligned, reused freely
+ *     between calls that do not overlap on the GPU.
+ *   - Rows of the drafted block: r = (q * K + k) * L + i for request q, mode
+ *     k in [0, K) and drafted position i in [0, L) (depth i + 1).
+ *
+ * Limits: 1 <= K <= 16, 1 <= L <= 16, 1 <= topk <= 32, 1 <= B <= 512,
+ * K * B <= 2048, H % 64 == 0, 16 <= V < 2^30 (and V >= topk).
+ */
+#ifndef MFD_H_
+#define MFD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (the same type as cudaStream_t); NULL is the legacy stream. */
+typedef struct CUstream_st *mfd_stream_t;
+
+typedef enum {
+  MFD_OK = 0,
+  MFD_ERR_INVALID_ARG = 1, /* NULL pointer, size out of range, misalignment */
+  MFD_ERR_UNSUPPORTED = 2, /* valid but outside the limits above, or no sm_103a device */
+  MFD_ERR_WORKSPACE = 3,   /* ws NULL or smaller than mfd_workspace_size */
+  MFD_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+  MFD_ERR_TIMEOUT = 5,     /* device: a bounded wait ran out (kernel exited early) */
+  MFD_ERR_INPUT = 6        /* device: input values break the contract (see each call) */
+} mfd_status;
+
+/* Static English text for a status code; never NULL. */
+const char *mfd_status_string(int status);
+
+/* Operation ids for mfd_workspace_size. */
+enum {
+  MFD_OP_LMHEAD_TOPK = 0,
+  MFD_OP_LOGITS_TOPK = 1,
+  MFD_OP_BUILD_TREE = 2,
+  MFD_OP_VERIFY = 3
+};
+
+/* Bytes of scratch that `op` needs for the given sizes on the CURRENT CUDA
+ * device (the LM-head and verify splits follow its SM count).  Arguments an
+ * op does not use are ignored: LMHEAD_TOPK uses (R, V, topk); LOGITS_TOPK
+ * uses (R, V, topk); BUILD_TREE uses (n_req); VERIFY uses (n_req).
+ * Returns 0 for an unknown op or sizes outside the limits. */
+size_t mfd_workspace_size(int op, int n_req, int K, int L, int topk, int B, int R, int V);
+
+/* LM head, log-softmax and top-k.
+ * Model card "MFD drafter for Qwen3.5-4B", Model table: the drafter uses the
+ * target's LM head at run time; project page, How it works, step 2: each
+ * (mode, position) gives one distribution over the vocabulary.
+ *
+ *   z[r][v]     = sum_h h[r][h] * W[v][h]        (bf16 x bf16, fp32 accumulate)
+ *   lse[r]      = log sum_v exp(z[r][v])          (natural log)
+ *   tk_tok[r][] = the topk token ids of largest z[r][.], ties to the smaller id
+ *   tk_logp[r][j] = z[r][tk_tok[r][j]] - lse[r]   (fp32)
+ * Each output row is sorted by (tk_logp descending, token id ascending).
+ * The logits never reach global memory.
+ *
+ *   h        bf16 [R][H], 16-byte aligned (TMA source)
+ *   W        bf16 [V][H], 16-byte aligned (TMA source); streamed once
+ *   tk_logp  fp32 [R][topk]      out
+ *   tk_tok   int32 [R][topk]     out
+ *   lse      fp32 [R]            out, may be NULL
+ *   status   int32 [1]           device status word (MFD_ERR_TIMEOUT on a
+ *                                bounded pipeline wait running out)
+ * Requires an sm_103a device.  TMA descriptors for (h, W, R, H, V) are
+ * encoded on the first call and cached by (pointer, shape); the cache is
+ * thread-safe.  Errors: INVALID_ARG (NULL, R < 1, misaligned h/W),
+ * UNSUPPORTED (limits, device), WORKSPACE, CUDA. */
+int mfd_lmhead_topk(const void *h, int R, int H, const void *W, int V, int topk,
+                    float *tk_logp, int32_t *tk_tok, float *lse, int32_t *status, void *ws,
+                    size_t ws_bytes, mfd_stream_t stream);
+
+/* Log-softmax and top-k of fp32 logits given directly (no LM head): the
+ * same outputs as mfd_lmhead_topk with z = logits [R][V].  Non-finite logits
+ * are the caller's responsibility. */
+int mfd_logits_topk(const float *logits, int R, int V, int topk, float *tk_logp,
+                    int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes,
+                    mfd_stream_t stream);
+
+/* Mixture DDTree (project page, How it works, step 3, and the Figure 1/2
+ * caption): mode k scores a prefix x = (x_1..x_d) by the fp32 left fold,
+ * in depth order, of its per-position table log-probabilities; a token not
+ * in mode k's top-k row at that position makes x unreachable for mode k.
+ * s(x) = max_k score_k(x).  Order: x before y iff s(x) > s(y), or s(x) ==
+ * s(y) and x's token ids are lexicographically smaller (unsigned, a proper
+ * prefix first).  The tree keeps the first B prefixes of depth 1..L with
+ * finite s, which is the union of the per-mode trees at the common cut-off.
+ *
+ *   tk_logp, tk_tok  [n_req][K][L][topk], rows as mfd_lmhead_topk writes
+ *                    them: log-probabilities (<= 0, not NaN) sorted
+ *                    descending with distinct tokens; otherwise *status =
+ *                    MFD_ERR_INPUT.  -inf entries are never used.
+ *   anchor_tok       int32 [n_req]  token of the root (node 0)
+ *   base_pos         int32 [n_req]  position of the root, may be NULL (0)
+ * Outputs, N = B + 1 nodes per request, W32 = ceil(N / 32):
+ *   parent  int32 [n_req][N]       parent node (-1 for the root)
+ *   token   int32 [n_req][N]       node token (anchor for the root)
+ *   depth   int32 [n_req][N]       0 for the root, 1..L otherwise
+ *   score   fp32  [n_req][N]       s(x) (0 for the root)
+ *   mode    int32 [n_req][N]       smallest mode attaining s(x) (-1 root)
+ *   mask    uint32 [n_req][N][W32] bit j of word j/32 of row i set iff node j
+ *                                  is on the root->i path (inclusive)
+ *   pos     int32 [n_req][N]       base_pos + depth
+ *   n_nodes int32 [n_req]          1 + number of kept prefixes (<= N)
+ * Node 0 is the root; nodes 1.. follow the order above (so parent[i] < i).
+ * Rows at and past n_nodes hold -1 (ints), -inf (score) and 0 (mask). */
+int mfd_build_tree(const float *tk_logp, const int32_t *tk_tok, int n_req, int K, int L,
+                   int topk, int B, const int32_t *anchor_tok, const int32_t *base_pos,
+                   int32_t *parent, int32_t *token, int32_t *depth, float *score,
+                   int32_t *mode, uint32_t *mask, int32_t *pos, int32_t *n_nodes,
+                   int32_t *status, void *ws, size_t ws_bytes, mfd_stream_t stream);
+
+/* Tree verification walk (model card, first paragraph; project page,
+ * Figure 2 (c)): from the root, the target picks a token y at the current
+ * node -- greedy (temperature 0): y = argmax_v t[cur][v]; sampled
+ * (temperature T > 0): y = argmax_v (t[cur][v] / T + G(seed, cur, v)), a
+ * Gumbel-max draw from softmax(t / T), where G = -log(-log(u)),
+ * u = (2 * (x >> 9) + 1) * 2^-24 and x is word 0 of Philox4x32-10 (Salmon et
+ * al., SC'11) at counter (v, cur, 0, 0), key (seed low, seed high).  Ties go
+ * to the smaller v.  If a child of cur carries y the walk moves there,
+ * otherwise y is the bonus token and the walk stops.
+ *
+ *   target_logits fp32 [n_req][B + 1][V]; only the rows on the walk are read
+ *   parent, token int32 [n_req][B + 1] and n_nodes int32 [n_req] from
+ *                 mfd_build_tree (or any tree in that format)
+ *   temperature   fp32 [n_req]  0 = greedy; < 0 or NaN -> MFD_ERR_INPUT
+ *   seed          uint64 [n_req]
+ *   accept_len    int32 [n_req]         drafted tokens accepted (0..L)
+ *   path_nodes    int32 [n_req][L + 1]  node read at step j (path_nodes[0] = 0)
+ *   out_tokens    int32 [n_req][L + 1]  y at step j: accepted tokens, bonus last
+ * Entries past accept_len hold -1.  The walk is one cooperative grid with a
+ * bounded grid-wide wait per step (MFD_ERR_TIMEOUT if it runs out). */
+int mfd_verify(const float *target_logits, int n_req, int B, int V, int L,
+               const int32_t *parent, const int32_t *token, const int32_t *n_nodes,
+               const float *temperature, const uint64_t *seed, int32_t *accept_len,
+               int32_t *path_nodes, int32_t *out_tokens, int32_t *status, void *ws,
+               size_t ws_bytes, mfd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MFD_H_ */

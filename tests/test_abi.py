@@ -1,0 +1,65 @@
+"""CPU checks of the C ABI: the library builds, loads and exports every
+function include/mfd.h declares; argument checks that return before any
+CUDA call behave as documented.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tree_verified_speculative_gb300 import build as mfd_build
+from tree_verified_speculative_gb300 import mfd
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+HEADER = os.path.join(HERE, "..", "include", "mfd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mfd_build.build()
+    return mfd.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mfd_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert set(names) >= {"mfd_lmhead_topk", "mfd_build_tree", "mfd_verify"}
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(mfd.EXPORTS)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.mfd_status_string(code)
+    assert b"unknown" in lib.mfd_status_string(99)
+
+
+def test_workspace_size_host_only_ops(lib):
+    assert mfd.mfd_workspace_size(mfd.MFD_OP_BUILD_TREE, n_req=3) == 3 * 16 * 512 * 4
+    assert mfd.mfd_workspace_size(mfd.MFD_OP_LOGITS_TOPK, R=4, V=32, topk=8) > 0
+    assert mfd.mfd_workspace_size(mfd.MFD_OP_LOGITS_TOPK, R=4, V=32, topk=33) == 0
+    assert mfd.mfd_workspace_size(99) == 0
+
+
+def test_argument_errors_before_any_cuda_call(lib):
+    fake = ctypes.c_void_p(0x100000)
+    # NULL inputs
+    rc = lib.mfd_build_tree(None, None, 1, 8, 15, 16, 64, None, None, *([None] * 9), None, 0, None)
+    assert rc == mfd.MFD_ERR_INVALID_ARG
+    args = [fake] * 2 + [1, 17, 15, 16, 64] + [fake, None] + [fake] * 9 + [fake, 1 << 20, None]
+    assert lib.mfd_build_tree(*args) == mfd.MFD_ERR_UNSUPPORTED  # K > 16
+    args = [fake] * 2 + [1, 8, 15, 16, 512] + [fake, None] + [fake] * 9 + [fake, 1 << 20, None]
+    assert lib.mfd_build_tree(*args) == mfd.MFD_ERR_UNSUPPORTED  # K * B > 2048
+    args = [fake] * 2 + [1, 8, 15, 16, 64] + [fake, None] + [fake] * 9 + [fake, 16, None]
+    assert lib.mfd_build_tree(*args) == mfd.MFD_ERR_WORKSPACE
+    rc = lib.mfd_logits_topk(fake, 4, 32, 40, fake, fake, None, fake, fake, 1 << 20, None)
+    assert rc == mfd.MFD_ERR_UNSUPPORTED  # topk > 32
+    rc = lib.mfd_lmhead_topk(ctypes.c_void_p(0x100004), 4, 64, fake, 1000, 8, fake, fake, None, fake, fake,
+                             1 << 20, None)
+    assert rc == mfd.MFD_ERR_INVALID_ARG  # h not 16-byte aligned

@@ -1,0 +1,140 @@
+"""GPU parity of whole rounds on the five workloads (the three calls back to
+back on one stream, as the benchmark runs them), against the oracle.
+
+Stages are checked the way the method statement asks: top-k tables against
+the oracle's LM head (sampled rows at full size); the tree bit-exact against
+the oracle's tree built from the GPU's own tables; the walk against the
+oracle's walk over the same tree and target logits."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tree_verified_speculative_gb300 import mfd, synth
+
+from gpu_helpers import assert_tree_equal, check_topk, check_walk, np_, tree_outputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_tiny_round():
+    c = synth.tiny(seed=1)
+    rd = mfd.Round(1, c.K, c.L, c.topk, c.B, c.V)
+    rd.status.zero_()
+    rd.logits_topk(torch.from_numpy(c.logits).cuda())
+    rd.build_tree()
+    torch.cuda.synchronize()
+    lp, tk = np_(rd.tk_logp), np_(rd.tk_tok)
+    o_lp, o_tk, _ = oracle.logits_topk(c.logits, c.topk)
+    check_topk(lp, tk, o_lp, o_tk)
+    g = tree_outputs(rd)
+    o = oracle.build_tree(lp.reshape(c.K, c.L, c.topk), tk.reshape(c.K, c.L, c.topk), c.B)
+    assert_tree_equal(g, o, 0)
+    rng = np.random.default_rng(5)
+    noise = synth.target_noise(c.B + 1, c.V, rng)
+    rows, cols = synth.plant_sites(o["parent"], o["token"], o["depth"], int(o["n_nodes"]), c.fut[1])
+    t = synth.plant(noise, rows, cols)
+    rd.verify(torch.from_numpy(t[None]).cuda(), torch.zeros(1, device="cuda"),
+              torch.zeros(1, dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    assert int(rd.status.item()) == 0
+    oa = oracle.verify(t, o["parent"], o["token"], int(o["n_nodes"]), c.L)
+    check_walk(int(np_(rd.accept_len)[0]), np_(rd.path_nodes)[0], np_(rd.out_tokens)[0], *oa, sampled=False)
+
+
+@pytest.fixture(scope="module")
+def head():
+    W = synth.lm_head(151936, 2560, seed=2024)
+    return W, W.cuda()
+
+
+def _round(W, Wd, rd, r: synth.Round, temperature: float, rows_checked, check_tables=True):
+    """One round through the three calls; returns the numbers of exact walks."""
+    rd.status.zero_()
+    rd.lmhead_topk(r.h.cuda(), Wd)
+    rd.build_tree()
+    torch.cuda.synchronize()
+    assert int(rd.status.item()) == 0
+    K, L, k, B = rd.K, rd.L, rd.topk, rd.B
+    lp, tk = np_(rd.tk_logp), np_(rd.tk_tok)
+    if check_tables:
+        o_lp, o_tk, _ = oracle.lmhead_topk(_bits(r.h[rows_checked]), _bits(W), k)
+        check_topk(lp[rows_checked], tk[rows_checked], o_lp, o_tk)
+    g = tree_outputs(rd)
+    o = oracle.build_tree(lp.reshape(K, L, k), tk.reshape(K, L, k), B)
+    assert_tree_equal(g, o, 0)
+    rng = np.random.default_rng(r.seed % (2**32))
+    noise = synth.target_noise(B + 1, W.shape[0], rng)
+    rows, cols = synth.plant_sites(o["parent"], o["token"], o["depth"], int(o["n_nodes"]), r.fut[r.target_mode])
+    t = synth.plant(noise, rows, cols)
+    rd.verify(torch.from_numpy(t[None]).cuda(), torch.tensor([temperature], device="cuda"),
+              torch.tensor([r.seed], dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    assert int(rd.status.item()) == 0
+    oa = oracle.verify(t, o["parent"], o["token"], int(o["n_nodes"]), L, temperature, r.seed)
+    return check_walk(int(np_(rd.accept_len)[0]), np_(rd.path_nodes)[0], np_(rd.out_tokens)[0], *oa,
+                      sampled=temperature > 0)
+
+
+def test_pages_shape_greedy_b64(head):
+    W, Wd = head
+    rd = mfd.Round(1, 8, 15, 16, 64, 151936)
+    r = synth.round_inputs(W, 8, 15, 11, seed=11)
+    assert _round(W, Wd, rd, r, 0.0, np.arange(0, 120, 7))
+
+
+def test_pages_shape_sampled_b256(head):
+    """B=256, T=1, a few seeded rounds (W fixed, fresh futures per round)."""
+    W, Wd = head
+    rd = mfd.Round(1, 8, 15, 16, 256, 151936)
+    exact = 0
+    for i in range(4):
+        r = synth.round_inputs(W, 8, 15, 11, seed=1000 + i)
+        exact += _round(W, Wd, rd, r, 1.0, np.arange(i, 120, 15), check_tables=(i < 2))
+    assert exact >= 3
+
+
+def test_batched_32_requests(head):
+    W, Wd = head
+    n = 32
+    rng = np.random.default_rng(77)
+    rounds = [synth.round_inputs(W, 8, 15, int(rng.integers(8, 15)), seed=500 + q) for q in range(n)]
+    h = torch.cat([r.h for r in rounds], 0)
+    rd = mfd.Round(n, 8, 15, 16, 128, 151936)
+    rd.status.zero_()
+    rd.lmhead_topk(h.cuda(), Wd)
+    rd.build_tree()
+    torch.cuda.synchronize()
+    assert int(rd.status.item()) == 0
+    lp, tk = np_(rd.tk_logp), np_(rd.tk_tok)
+    rows = np.array([3, 500, 1800, 3839])
+    o_lp, o_tk, _ = oracle.lmhead_topk(_bits(h[rows]), _bits(W), 16)
+    check_topk(lp[rows], tk[rows], o_lp, o_tk)
+    g = tree_outputs(rd)
+    lp4, tk4 = lp.reshape(n, 8, 15, 16), tk.reshape(n, 8, 15, 16)
+    o = oracle.build_tree(lp4, tk4, 128)
+    for q in range(n):
+        assert_tree_equal(g, {k: v[q] for k, v in o.items()}, q)
+    t = np.empty((n, 129, 151936), np.float32)
+    for q in range(n):
+        noise = synth.target_noise(129, 151936, np.random.default_rng(q))
+        rows_, cols_ = synth.plant_sites(o["parent"][q], o["token"][q], o["depth"][q], int(o["n_nodes"][q]),
+                                         rounds[q].fut[rounds[q].target_mode])
+        t[q] = synth.plant(noise, rows_, cols_)
+    temps = np.array([0.0] * 16 + [1.0] * 16, np.float32)
+    seeds = np.array([r.seed for r in rounds], np.uint64)
+    rd.verify(torch.from_numpy(t).cuda(), torch.from_numpy(temps).cuda(),
+              torch.from_numpy(seeds.view(np.int64)).cuda())
+    torch.cuda.synchronize()
+    assert int(rd.status.item()) == 0
+    exact = 0
+    for q in range(n):
+        oa = oracle.verify(t[q], o["parent"][q], o["token"][q], int(o["n_nodes"][q]), 15, float(temps[q]),
+                           int(seeds[q]))
+        exact += check_walk(int(np_(rd.accept_len)[q]), np_(rd.path_nodes)[q], np_(rd.out_tokens)[q], *oa,
+                            sampled=temps[q] > 0)
+    assert exact >= 30

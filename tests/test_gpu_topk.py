@@ -1,0 +1,133 @@
+"""GPU parity: LM head + log-softmax + top-k, and top-k of given logits,
+against the CPU oracle (log-probs within 1e-4; top-k sets equal except at the
+cut).  Model card "MFD drafter for Qwen3.5-4B", Model table; project page
+"Multi-Future Drafting", How it works, step 2."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tree_verified_speculative_gb300 import mfd, synth
+
+from gpu_helpers import check_topk, np_, status_of
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _gpu_logits_topk(z: np.ndarray, topk: int):
+    R, V = z.shape
+    rd = mfd.Round(1, 1, R, topk, 1, V)
+    rd.status.zero_()
+    rd.logits_topk(torch.from_numpy(z).cuda())
+    torch.cuda.synchronize()
+    assert status_of(rd) == 0
+    return np_(rd.tk_logp), np_(rd.tk_tok), np_(rd.lse)
+
+
+def _gpu_lmhead(h: torch.Tensor, W: torch.Tensor, topk: int, Wd=None):
+    R = h.shape[0]
+    V = W.shape[0]
+    rd = mfd.Round(1, 1, R, topk, 1, V)
+    rd.status.zero_()
+    rd.lmhead_topk(h.cuda(), W.cuda() if Wd is None else Wd)
+    torch.cuda.synchronize()
+    assert status_of(rd) == 0
+    return np_(rd.tk_logp), np_(rd.tk_tok), np_(rd.lse)
+
+
+def test_tiny_case_logits_topk():
+    c = synth.tiny(seed=1)
+    for topk in (8, 32):
+        g = _gpu_logits_topk(c.logits, topk)
+        o = oracle.logits_topk(c.logits, topk)
+        check_topk(g[0], g[1], o[0], o[1])
+        np.testing.assert_allclose(g[2], o[2], atol=1e-5)
+
+
+@pytest.mark.parametrize("R,V,topk", [(1, 16, 1), (3, 1000, 8), (7, 5003, 16), (5, 70001, 32), (130, 2049, 16)])
+def test_logits_topk_random(R, V, topk):
+    rng = np.random.default_rng(R * 1000 + V)
+    z = (2.0 * rng.standard_normal((R, V))).astype(np.float32)
+    g = _gpu_logits_topk(z, topk)
+    o = oracle.logits_topk(z, topk)
+    check_topk(g[0], g[1], o[0], o[1])
+    np.testing.assert_allclose(g[2], o[2], atol=1e-5)
+
+
+def test_logits_topk_ties():
+    rng = np.random.default_rng(4)
+    z = rng.choice(np.array([-1.0, 0.5, 2.0, 2.0, 3.0], np.float32), size=(6, 3000)).astype(np.float32)
+    g = _gpu_logits_topk(z, 16)
+    o = oracle.logits_topk(z, 16)
+    # ties resolve to the smaller token id on both sides
+    np.testing.assert_array_equal(g[1], o[1])
+    np.testing.assert_allclose(g[0], o[0], atol=1e-6)
+
+
+@pytest.mark.parametrize("R,H,V,topk", [
+    (1, 64, 16, 1), (5, 64, 300, 8), (120, 128, 1000, 16), (128, 256, 4099, 32), (130, 64, 2305, 16),
+    (257, 192, 777, 8), (120, 2560, 20000, 16)])
+def test_lmhead_topk_small(R, H, V, topk):
+    rng = np.random.default_rng(R + H + V)
+    h = synth.bf16_round(rng.standard_normal((R, H)).astype(np.float32))
+    W = synth.bf16_round((rng.standard_normal((V, H)) / np.sqrt(H)).astype(np.float32))
+    g = _gpu_lmhead(h, W, topk)
+    o = oracle.lmhead_topk(_bits(h), _bits(W), topk)
+    check_topk(g[0], g[1], o[0], o[1])
+    np.testing.assert_allclose(g[2], o[2], atol=5e-5)
+
+
+@pytest.fixture(scope="module")
+def head_2560():
+    W = synth.lm_head(151936, 2560, seed=2024)
+    return W, W.cuda()
+
+
+def test_lmhead_pages_shape_sampled_rows(head_2560):
+    """K=8, L=15, H=2560, V=151936, top-k 16, planted futures (11 of 15
+    shared): all 120 rows through the kernel, 24 of them checked against the
+    oracle's full-vocabulary row."""
+    W, Wd = head_2560
+    r = synth.round_inputs(W, 8, 15, 11, seed=7)
+    g = _gpu_lmhead(r.h, W, 16, Wd)
+    rows = np.random.default_rng(0).choice(120, size=24, replace=False)
+    o = oracle.lmhead_topk(_bits(r.h[rows]), _bits(W), 16)
+    check_topk(g[0][rows], g[1][rows], o[0], o[1])
+    np.testing.assert_allclose(g[2][rows], o[2], atol=5e-5)
+    # every row is a distribution: the planted token is the usual argmax
+    assert np.mean(g[1][:, 0] == r.fut.reshape(-1)) > 0.5
+
+
+def test_lmhead_batched_3840_rows_sampled(head_2560):
+    """32 requests x 8 modes x 15 positions = 3840 rows (30 M tiles)."""
+    W, Wd = head_2560
+    hs = [synth.round_inputs(W, 8, 15, 8 + (q % 7), seed=100 + q).h for q in range(32)]
+    h = torch.cat(hs, 0)
+    g = _gpu_lmhead(h, W, 16, Wd)
+    rows = np.array([0, 127, 128, 1000, 1919, 2047, 3000, 3839])
+    o = oracle.lmhead_topk(_bits(h[rows]), _bits(W), 16)
+    check_topk(g[0][rows], g[1][rows], o[0], o[1])
+
+
+@pytest.mark.slow
+def test_lmhead_wide_shape_sampled_rows():
+    """H=5120, V=248320, top-k 32 (about 2.5 GB of weights)."""
+    W = synth.lm_head(248320, 5120, seed=4048)
+    r = synth.round_inputs(W, 8, 15, 13, seed=9)
+    g = _gpu_lmhead(r.h, W, 32)
+    rows = np.array([0, 17, 59, 119])
+    o = oracle.lmhead_topk(_bits(r.h[rows]), _bits(W), 32)
+    check_topk(g[0][rows], g[1][rows], o[0], o[1])
+
+
+def test_lmhead_rejects_bad_arguments():
+    h = torch.zeros((4, 100), dtype=torch.bfloat16, device="cuda")  # H not a multiple of 64
+    W = torch.zeros((64, 100), dtype=torch.bfloat16, device="cuda")
+    rd = mfd.Round(1, 1, 4, 8, 1, 64)
+    with pytest.raises(mfd.MfdError) as e:
+        rd.lmhead_topk(h, W)
+    assert e.value.code == mfd.MFD_ERR_UNSUPPORTED

@@ -1,0 +1,129 @@
+"""GPU parity: the tree verification walk against the oracle.  Greedy paths
+are bit-exact; sampled paths are exact except from the first step whose
+top-two perturbed scores (oracle) lie within 1e-5.  Model card "MFD drafter
+for Qwen3.5-4B", first paragraph; project page, Figure 2 (c)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tree_verified_speculative_gb300 import mfd, synth
+
+from gpu_helpers import check_walk, np_, status_of
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_verify(t: np.ndarray, parent, token, n_nodes, L, temps, seeds):
+    """t: [n_req, N, V]; parent/token [n_req, N]; n_nodes [n_req]."""
+    n_req, N, V = t.shape
+    rd = mfd.Round(n_req, 1, L, 1, N - 1, V)
+    rd.parent.copy_(torch.from_numpy(np.asarray(parent, np.int32)))
+    rd.token.copy_(torch.from_numpy(np.asarray(token, np.int32)))
+    rd.n_nodes.copy_(torch.from_numpy(np.asarray(n_nodes, np.int32)))
+    rd.status.zero_()
+    temp = torch.tensor(np.asarray(temps, np.float32), device="cuda")
+    seed = torch.tensor(np.asarray(seeds, np.uint64).view(np.int64), device="cuda")
+    rd.verify(torch.from_numpy(t).cuda(), temp, seed)
+    torch.cuda.synchronize()
+    return np_(rd.accept_len), np_(rd.path_nodes), np_(rd.out_tokens), status_of(rd)
+
+
+def _trees(rng, n_req, K, L, k, V, B):
+    lp = np.empty((n_req, K, L, k), np.float32)
+    tk = np.empty((n_req, K, L, k), np.int32)
+    futs = []
+    for q in range(n_req):
+        fut = synth.futures(K, L, V, 11 if L >= 11 else 1, rng)
+        futs.append(fut)
+        for m in range(K):
+            for i in range(L):
+                others = [t for t in rng.choice(V, size=k + 4, replace=False) if t != fut[m, i]][: k - 1]
+                toks = np.array([fut[m, i], *others])
+                vals = np.concatenate([[-1.0], -3.0 + rng.normal(0, 0.5, size=k - 1)]).astype(np.float32)
+                order = np.lexsort((toks, -vals))
+                lp[q, m, i], tk[q, m, i] = vals[order], toks[order]
+    return oracle.build_tree(lp, tk, B), futs
+
+
+def _targets(rng, tree, futs, V, target_modes):
+    n_req, N = tree["parent"].shape
+    t = np.empty((n_req, N, V), np.float32)
+    for q in range(n_req):
+        noise = synth.target_noise(N, V, rng)
+        rows, cols = synth.plant_sites(tree["parent"][q], tree["token"][q], tree["depth"][q],
+                                       int(tree["n_nodes"][q]), futs[q][target_modes[q]])
+        t[q] = synth.plant(noise, rows, cols)
+    return t
+
+
+def _compare(t, tree, L, temps, seeds):
+    g_acc, g_path, g_out, st = _gpu_verify(t, tree["parent"], tree["token"], tree["n_nodes"], L, temps, seeds)
+    assert st == 0
+    exact = 0
+    for q in range(t.shape[0]):
+        o = oracle.verify(t[q], tree["parent"][q], tree["token"][q], int(tree["n_nodes"][q]), L, temps[q], seeds[q])
+        exact += check_walk(int(g_acc[q]), g_path[q], g_out[q], *o, sampled=temps[q] > 0)
+    return exact, g_acc
+
+
+def test_hand_tree_greedy():
+    parent = np.array([[-1, 0, 0, 1, 1]], np.int32)
+    token = np.array([[0, 5, 7, 2, 8]], np.int32)
+    t = np.zeros((1, 5, 40), np.float32)
+    t[0, 0, 5] = 3.0
+    t[0, 1, 2] = 1.0
+    t[0, 3, 39] = 4.0
+    acc, path, out, st = _gpu_verify(t, parent, token, [5], 3, [0.0], [0])
+    assert st == 0 and acc[0] == 2
+    assert list(path[0]) == [0, 1, 3, -1] and list(out[0]) == [5, 2, 39, -1]
+
+
+@pytest.mark.parametrize("V", [50, 151936])
+def test_greedy_planted(V):
+    rng = np.random.default_rng(V)
+    tree, futs = _trees(rng, 4, 8, 15, 16, 151936 if V > 1000 else V, 64)
+    t = _targets(rng, tree, futs, V, [0, 3, 5, 7])
+    exact, acc = _compare(t, tree, 15, [0.0] * 4, [0] * 4)
+    assert exact == 4
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_sampled(T):
+    rng = np.random.default_rng(int(T * 10))
+    tree, futs = _trees(rng, 6, 8, 15, 16, 151936, 256)
+    t = _targets(rng, tree, futs, 151936, [1, 2, 3, 4, 5, 6])
+    seeds = [int(x) for x in rng.integers(0, 2**63 - 1, size=6)]
+    exact, _ = _compare(t, tree, 15, [T] * 6, seeds)
+    assert exact >= 5
+
+
+def test_sampled_small_vocab_many_seeds():
+    """V = 64: many draws per node; decisions agree with the oracle."""
+    rng = np.random.default_rng(3)
+    tree, futs = _trees(rng, 1, 4, 6, 8, 64, 40)
+    t = _targets(rng, tree, futs, 64, [2])
+    t = np.repeat(t, 64, axis=0)
+    tree64 = {k: np.repeat(v, 64, axis=0) for k, v in tree.items()}
+    seeds = list(range(1000, 1064))
+    exact, _ = _compare(t, tree64, 6, [1.0] * 64, seeds)
+    assert exact >= 60
+
+
+def test_mixed_batch_32():
+    rng = np.random.default_rng(32)
+    tree, futs = _trees(rng, 32, 8, 15, 16, 151936, 128)
+    modes = rng.integers(0, 8, size=32)
+    t = _targets(rng, tree, futs, 151936, modes)
+    temps = [0.0] * 16 + [1.0] * 16
+    seeds = [int(x) for x in rng.integers(0, 2**63 - 1, size=32)]
+    exact, _ = _compare(t, tree, 15, temps, seeds)
+    assert exact >= 30
+
+
+def test_rejects_bad_temperature():
+    parent = np.array([[-1, 0]], np.int32)
+    token = np.array([[0, 1]], np.int32)
+    t = np.zeros((1, 2, 16), np.float32)
+    _, _, _, st = _gpu_verify(t, parent, token, [2], 2, [-1.0], [0])
+    assert st == mfd.MFD_ERR_INPUT

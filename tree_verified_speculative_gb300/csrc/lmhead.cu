@@ -1,0 +1,336 @@
+// lmhead.cu -- the target's LM head on the drafter's hidden states, with the
+// log-softmax and per-row top-k fused into the epilogue (model card "MFD
+// drafter for Qwen3.5-4B", Model table: the target LM head is applied at run
+// time; project page "Multi-Future Drafting", How it works, step 2: one
+// distribution per mode and position).
+//
+// Shape of the work: R hidden rows (K modes x L positions per request) times
+// a V x H bf16 weight.  At R <= 128 the weight stream (V*H*2 bytes) is the
+// whole cost, so the kernel reads W exactly once, with TMA, and keeps the
+// logits in tensor memory: they never reach global memory.
+//
+//   D[128 x 256] (TMEM, fp32) = h_tile[128 x H] . W_tile[256 x H]^T
+//
+// A = 128 hidden rows (one M tile, zero-filled past R), B = 256 vocabulary
+// rows, K streamed in 64-element (128-byte, swizzled) chunks through a
+// 4-stage shared-memory ring.  Each TMEM lane is one hidden row, so the
+// epilogue thread that owns lane r reads its row's logits column by column
+// and keeps the row's running max, running sum of exp and a sorted top-T in
+// registers -- no cross-thread reduction.
+//
+// Grid: persistent, one CTA per SM.  The vocabulary is split into P
+// contiguous ranges of 256-row tiles; work item = (range, M tile).  A CTA
+// writes, per row and range, (max, sum exp) and its T best (logit, id)
+// pairs; merge_topk (topk.cu) combines the P partials of a row.
+//
+// Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer (one
+// thread each), warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4)..).
+// TMEM holds two 256-column fp32 accumulators so that the epilogue of tile
+// n overlaps the MMAs of tile n+1.
+#include "lmhead.h"
+#include "mfd_device.cuh"
+
+namespace mfd {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr float LOG2E = 1.4426950408889634f;
+
+constexpr int smem_bytes() {
+  return 1024 /* alignment slack */ + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5) + 16;
+}
+
+struct Params {
+  int R, H, V;
+  int n_mt;     // M tiles of 128 rows
+  int n_vt;     // vocabulary tiles of 256 rows
+  int P;        // vocabulary ranges
+  int n_items;  // n_mt * P
+  float2 *part_ms;  // [R][P]      (running max, sum exp(z - max))
+  int2 *part_cand;  // [R][P][T]   (logit bits, token id), best first
+  int32_t *status;
+};
+
+__device__ __forceinline__ void item_range(const Params &p, int item, int &mt, int &t0, int &t1, int &range) {
+  range = item / p.n_mt;
+  mt = item - range * p.n_mt;
+  t0 = (int)(((long long)range * p.n_vt) / p.P);
+  t1 = (int)(((long long)(range + 1) * p.n_vt) / p.P);
+}
+
+// Insert (x, v) into the sorted (value desc, id asc) list; the caller has
+// checked that x beats the last entry.
+template <int T>
+__device__ __forceinline__ void topk_insert(float (&tv)[T], int (&ti)[T], float x, int v) {
+  float cv = x;
+  int ci = v;
+#pragma unroll
+  for (int s = 0; s < T; ++s) {
+    const bool sw = vi_before(cv, ci, tv[s], ti[s]);
+    const float ov = tv[s];
+    const int oi = ti[s];
+    tv[s] = sw ? cv : ov;
+    ti[s] = sw ? ci : oi;
+    cv = sw ? ov : cv;
+    ci = sw ? oi : ci;
+  }
+}
+
+template <int T>
+__global__ void __launch_bounds__(THREADS, 1)
+    lmhead_topk_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
+                       const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + STAGES * A_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *never = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    *never = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_h);
+    prefetch_tmap(&tmap_w);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int nk = p.H / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------- producer
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_h = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_par = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+        int mt, t0, t1, range;
+        item_range(p, item, mt, t0, t1, range);
+        for (int t = t0; t < t1 && ok; ++t) {
+          for (int kc = 0; kc < nk; ++kc) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+            tma_load_2d(sA + stage * A_BYTES, &tmap_h, kc * BK, mt * BM, &full[stage], pol_h);
+            tma_load_2d(sB + stage * B_BYTES, &tmap_w, kc * BK, t * BN, &full[stage], pol_w);
+            issued |= 1u << stage;
+            issued_par = phase ? (issued_par | (1u << stage)) : (issued_par & ~(1u << stage));
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        if (!*abort_flag) report(p.status, MFD_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // Every load issued must land before the CTA may exit.
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u) mbar_wait(&full[s], (issued_par >> s) & 1u, never);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+        int mt, t0, t1, range;
+        item_range(p, item, mt, t0, t1, range);
+        for (int t = t0; t < t1 && ok; ++t) {
+          if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+          for (int kc = 0; kc < nk; ++kc) {
+            if (!mbar_wait(&full[stage], phase, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * A_BYTES));
+            const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * B_BYTES));
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              tc_mma_f16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kc | kk) != 0);
+            tc_commit(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          tc_commit(&tfull[acc]);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        if (!*abort_flag) report(p.status, MFD_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // All MMAs must finish before TMEM is released.
+      tc_commit(drain);
+      mbar_wait(drain, 0, never);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+      int mt, t0, t1, range;
+      item_range(p, item, mt, t0, t1, range);
+      float m = -INFINITY, S = 0.f;
+      float tv[T];
+      int ti[T];
+#pragma unroll
+      for (int s = 0; s < T; ++s) {
+        tv[s] = -INFINITY;
+        ti[s] = 0x7FFFFFFF;
+      }
+      for (int t = t0; t < t1; ++t) {
+        if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + lane_addr + (uint32_t)(acc * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float x[32];
+          tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), x);
+          const int v0 = t * BN + c * 32;
+          float cmax = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            x[j] = (v0 + j < p.V) ? x[j] : -INFINITY;
+            cmax = fmaxf(cmax, x[j]);
+          }
+          if (cmax > -INFINITY) {
+            if (cmax > m) {
+              S *= exp2f((m - cmax) * LOG2E);
+              m = cmax;
+            }
+            const float mb = m * LOG2E;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) S += exp2f(fmaf(x[j], LOG2E, -mb));
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (x[j] > tv[T - 1]) topk_insert<T>(tv, ti, x[j], v0 + j);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) break;
+      const int row = mt * BM + row_in_tile;
+      if (row < p.R) {
+        const size_t base = (size_t)row * p.P + range;
+        p.part_ms[base] = make_float2(m, S);
+        int2 *c = p.part_cand + base * T;
+#pragma unroll
+        for (int s = 0; s < T; ++s) c[s] = make_int2(__float_as_int(tv[s]), ti[s]);
+      }
+    }
+    if (!ok) {
+      if (!*abort_flag) report(p.status, MFD_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int T>
+cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
+  static_assert(smem_bytes() <= 232448, "shared memory budget");
+  Params p;
+  p.R = L.R;
+  p.H = L.H;
+  p.V = L.V;
+  p.n_mt = (L.R + BM - 1) / BM;
+  p.n_vt = (L.V + BN - 1) / BN;
+  p.P = L.P;
+  p.n_items = p.n_mt * p.P;
+  p.part_ms = reinterpret_cast<float2 *>(L.part_ms);
+  p.part_cand = reinterpret_cast<int2 *>(L.part_cand);
+  p.status = L.status;
+  cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem_bytes());
+  if (e != cudaSuccess) return e;
+  const int grid = p.n_items < L.n_sm ? p.n_items : L.n_sm;
+  lmhead_topk_kernel<T><<<grid, THREADS, smem_bytes(), stream>>>(*L.tmap_h, *L.tmap_w, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int lmhead_tile_rows() { return BN; }
+int lmhead_m_rows() { return BM; }
+int lmhead_k_chunk() { return BK; }
+
+cudaError_t launch_lmhead_partials(const LmheadLaunch &L, cudaStream_t stream) {
+  switch (L.T) {
+    case 8: return launch_t<8>(L, stream);
+    case 16: return launch_t<16>(L, stream);
+    case 32: return launch_t<32>(L, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mfd

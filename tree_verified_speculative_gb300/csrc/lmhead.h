@@ -1,0 +1,77 @@
+// lmhead.h -- internal launch interface of the fused LM-head kernel.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mfd {
+
+struct LmheadLaunch {
+  const CUtensorMap *tmap_h;  // bf16 [R][H], box 64 x 128, 128-byte swizzle
+  const CUtensorMap *tmap_w;  // bf16 [V][H], box 64 x 256, 128-byte swizzle
+  int R, H, V;
+  int T;     // candidates kept per (row, range): 8, 16 or 32
+  int P;     // vocabulary ranges (<= number of 256-row tiles)
+  int n_sm;  // persistent grid size
+  void *part_ms;    // float2 [R][P]
+  void *part_cand;  // int2 [R][P][T]
+  int32_t *status;
+};
+
+int lmhead_tile_rows();  // vocabulary rows per tile (256)
+int lmhead_m_rows();     // hidden rows per M tile (128)
+int lmhead_k_chunk();    // K elements per pipeline stage (64)
+cudaError_t launch_lmhead_partials(const LmheadLaunch &L, cudaStream_t stream);
+
+// topk.cu
+struct MergeLaunch {
+  const void *part_ms;    // float2 [R][P]
+  const void *part_cand;  // int2 [R][P][T]
+  int R, P, T, topk;
+  float *tk_logp;
+  int32_t *tk_tok;
+  float *lse;  // may be NULL
+  int32_t *status;
+};
+cudaError_t launch_merge_topk(const MergeLaunch &M, cudaStream_t stream);
+
+struct LogitsPartialLaunch {
+  const float *logits;  // [R][V]
+  int R, V, T, P, chunk;
+  void *part_ms;
+  void *part_cand;
+};
+cudaError_t launch_logits_partials(const LogitsPartialLaunch &L, cudaStream_t stream);
+
+// tree.cu
+struct TreeLaunch {
+  const float *tk_logp;
+  const int32_t *tk_tok;
+  int n_req, K, L, topk, B;
+  const int32_t *anchor, *base_pos;
+  int32_t *parent, *token, *depth;
+  float *score;
+  int32_t *mode;
+  uint32_t *mask;
+  int32_t *pos, *n_nodes, *status;
+  int32_t *union_ws;  // [n_req][16][512]
+};
+size_t tree_smem_bytes(int K, int L, int topk, int B, int *cap_out, int *tsize_out);
+cudaError_t launch_build_tree(const TreeLaunch &T, cudaStream_t stream);
+
+// verify.cu
+struct VerifyLaunch {
+  const float *t;
+  int n_req, B, V, L;
+  const int32_t *parent, *token, *n_nodes;
+  const float *temperature;
+  const uint64_t *seed;
+  int32_t *accept_len, *path_nodes, *out_tokens, *status;
+  unsigned *bar;   // [max_groups] zeroed before the launch
+  float2 *part;    // [grid][2]
+  int grid;        // cooperative grid size
+};
+int verify_max_grid(int n_sm);
+cudaError_t launch_verify(const VerifyLaunch &V, cudaStream_t stream);
+
+}  // namespace mfd

@@ -1,0 +1,334 @@
+// mfd_api.cu -- the extern "C" entry points of libmfd (declared and
+// documented in include/mfd.h): argument checks, scratch layout, TMA
+// descriptor encoding, kernel launches.  No allocation, no host sync.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/mfd.h"
+#include "lmhead.h"
+
+namespace {
+
+struct DeviceInfo {
+  int n_sm = 0, major = 0, minor = 0;
+  bool ok = false;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_dev;
+
+int current_device_info(DeviceInfo *out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MFD_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_dev.find(dev);
+  if (it == g_dev.end()) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MFD_ERR_CUDA;
+    d.ok = true;
+    it = g_dev.emplace(dev, d).first;
+  }
+  *out = it->second;
+  return MFD_OK;
+}
+
+bool is_sm103(const DeviceInfo &d) { return d.major == 10 && d.minor == 3; }
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int cand_width(int topk) { return topk <= 8 ? 8 : (topk <= 16 ? 16 : 32); }
+
+// ---------------------------------------------------------------- TMA maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+using MapKey = std::tuple<int, const void *, int, int, int>;  // device, ptr, rows, cols, box rows
+std::map<MapKey, CUtensorMap> g_maps;
+
+// bf16 [rows][cols] row-major, box = 64 columns x box_rows rows, 128B swizzle,
+// out-of-range rows read as zero.
+int tensor_map(const void *ptr, int rows, int cols, int box_rows, const CUtensorMap **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MFD_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  const MapKey key{dev, ptr, rows, cols, box_rows};
+  auto it = g_maps.find(key);
+  if (it == g_maps.end()) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return MFD_ERR_CUDA;
+    CUtensorMap m;
+    std::memset(&m, 0, sizeof m);
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return MFD_ERR_CUDA;
+    if (g_maps.size() > 4096) g_maps.clear();
+    it = g_maps.emplace(key, m).first;
+  }
+  *out = &it->second;  // std::map nodes are stable
+  return MFD_OK;
+}
+
+// ---------------------------------------------------------------- layouts
+struct TopkLayout {
+  int P, T, chunk;
+  size_t ms_bytes, cand_bytes, total;
+};
+
+TopkLayout lmhead_layout(int R, int V, int topk, int n_sm) {
+  TopkLayout y;
+  const int tiles = (V + mfd::lmhead_tile_rows() - 1) / mfd::lmhead_tile_rows();
+  y.P = tiles < n_sm ? tiles : n_sm;
+  if (y.P > 256) y.P = 256;
+  y.T = cand_width(topk);
+  y.chunk = 0;
+  y.ms_bytes = align256((size_t)R * y.P * 8);
+  y.cand_bytes = align256((size_t)R * y.P * y.T * 8);
+  y.total = y.ms_bytes + y.cand_bytes;
+  return y;
+}
+
+TopkLayout logits_layout(int R, int V, int topk) {
+  TopkLayout y;
+  int chunk = (V + 255) / 256;
+  chunk = (chunk + 31) / 32 * 32;
+  if (chunk < 1024) chunk = 1024;
+  y.chunk = chunk;
+  y.P = (V + chunk - 1) / chunk;
+  y.T = cand_width(topk);
+  y.ms_bytes = align256((size_t)R * y.P * 8);
+  y.cand_bytes = align256((size_t)R * y.P * y.T * 8);
+  y.total = y.ms_bytes + y.cand_bytes;
+  return y;
+}
+
+constexpr size_t kVerifyBarBytes = 4096;  // up to 1024 group counters
+size_t verify_bytes(int n_sm) { return kVerifyBarBytes + align256((size_t)mfd::verify_max_grid(n_sm) * 2 * 8); }
+
+size_t tree_bytes(int n_req) { return (size_t)n_req * 16 * 512 * 4; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MFD_OK : MFD_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *mfd_status_string(int status) {
+  switch (status) {
+    case MFD_OK: return "ok";
+    case MFD_ERR_INVALID_ARG: return "invalid argument (NULL pointer, size out of range or misaligned pointer)";
+    case MFD_ERR_UNSUPPORTED: return "unsupported: outside the library limits or not an sm_103a device";
+    case MFD_ERR_WORKSPACE: return "workspace missing or smaller than mfd_workspace_size";
+    case MFD_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case MFD_ERR_TIMEOUT: return "a bounded device wait ran out; the kernel stopped early";
+    case MFD_ERR_INPUT: return "input values break the contract (see mfd.h)";
+    default: return "unknown status";
+  }
+}
+
+size_t mfd_workspace_size(int op, int n_req, int K, int L, int topk, int B, int R, int V) {
+  (void)K;
+  (void)L;
+  (void)B;
+  DeviceInfo d;
+  switch (op) {
+    case MFD_OP_LMHEAD_TOPK:
+      if (R < 1 || V < 16 || topk < 1 || topk > 32 || topk > V) return 0;
+      if (current_device_info(&d) != MFD_OK) return 0;
+      return lmhead_layout(R, V, topk, d.n_sm).total;
+    case MFD_OP_LOGITS_TOPK:
+      if (R < 1 || V < 16 || topk < 1 || topk > 32 || topk > V) return 0;
+      return logits_layout(R, V, topk).total;
+    case MFD_OP_BUILD_TREE:
+      if (n_req < 1) return 0;
+      return tree_bytes(n_req);
+    case MFD_OP_VERIFY:
+      if (n_req < 1) return 0;
+      if (current_device_info(&d) != MFD_OK) return 0;
+      return verify_bytes(d.n_sm);
+    default:
+      return 0;
+  }
+}
+
+int mfd_lmhead_topk(const void *h, int R, int H, const void *W, int V, int topk, float *tk_logp,
+                    int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes,
+                    mfd_stream_t stream) {
+  if (!h || !W || !tk_logp || !tk_tok || !status || R < 1 || H < 1 || V < 1 || topk < 1)
+    return MFD_ERR_INVALID_ARG;
+  if (!aligned(h, 16) || !aligned(W, 16)) return MFD_ERR_INVALID_ARG;
+  if (H % mfd::lmhead_k_chunk() != 0 || topk > 32 || V < 16 || topk > V || V >= (1 << 30))
+    return MFD_ERR_UNSUPPORTED;
+  DeviceInfo d;
+  int rc = current_device_info(&d);
+  if (rc != MFD_OK) return rc;
+  if (!is_sm103(d)) return MFD_ERR_UNSUPPORTED;
+  const TopkLayout y = lmhead_layout(R, V, topk, d.n_sm);
+  if (!ws || ws_bytes < y.total || !aligned(ws, 256)) return MFD_ERR_WORKSPACE;
+  const CUtensorMap *mh = nullptr, *mw = nullptr;
+  if ((rc = tensor_map(h, R, H, mfd::lmhead_m_rows(), &mh)) != MFD_OK) return rc;
+  if ((rc = tensor_map(W, V, H, mfd::lmhead_tile_rows(), &mw)) != MFD_OK) return rc;
+  char *base = static_cast<char *>(ws);
+  mfd::LmheadLaunch L;
+  L.tmap_h = mh;
+  L.tmap_w = mw;
+  L.R = R;
+  L.H = H;
+  L.V = V;
+  L.T = y.T;
+  L.P = y.P;
+  L.n_sm = d.n_sm;
+  L.part_ms = base;
+  L.part_cand = base + y.ms_bytes;
+  L.status = status;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = cuda_status(mfd::launch_lmhead_partials(L, s))) != MFD_OK) return rc;
+  mfd::MergeLaunch M;
+  M.part_ms = L.part_ms;
+  M.part_cand = L.part_cand;
+  M.R = R;
+  M.P = y.P;
+  M.T = y.T;
+  M.topk = topk;
+  M.tk_logp = tk_logp;
+  M.tk_tok = tk_tok;
+  M.lse = lse;
+  M.status = status;
+  return cuda_status(mfd::launch_merge_topk(M, s));
+}
+
+int mfd_logits_topk(const float *logits, int R, int V, int topk, float *tk_logp, int32_t *tk_tok, float *lse,
+                    int32_t *status, void *ws, size_t ws_bytes, mfd_stream_t stream) {
+  if (!logits || !tk_logp || !tk_tok || !status || R < 1 || V < 1 || topk < 1) return MFD_ERR_INVALID_ARG;
+  if (topk > 32 || V < 16 || topk > V || V >= (1 << 30)) return MFD_ERR_UNSUPPORTED;
+  const TopkLayout y = logits_layout(R, V, topk);
+  if (!ws || ws_bytes < y.total || !aligned(ws, 256)) return MFD_ERR_WORKSPACE;
+  char *base = static_cast<char *>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mfd::LogitsPartialLaunch L;
+  L.logits = logits;
+  L.R = R;
+  L.V = V;
+  L.T = y.T;
+  L.P = y.P;
+  L.chunk = y.chunk;
+  L.part_ms = base;
+  L.part_cand = base + y.ms_bytes;
+  int rc = cuda_status(mfd::launch_logits_partials(L, s));
+  if (rc != MFD_OK) return rc;
+  mfd::MergeLaunch M;
+  M.part_ms = L.part_ms;
+  M.part_cand = L.part_cand;
+  M.R = R;
+  M.P = y.P;
+  M.T = y.T;
+  M.topk = topk;
+  M.tk_logp = tk_logp;
+  M.tk_tok = tk_tok;
+  M.lse = lse;
+  M.status = status;
+  return cuda_status(mfd::launch_merge_topk(M, s));
+}
+
+int mfd_build_tree(const float *tk_logp, const int32_t *tk_tok, int n_req, int K, int L, int topk, int B,
+                   const int32_t *anchor_tok, const int32_t *base_pos, int32_t *parent, int32_t *token,
+                   int32_t *depth, float *score, int32_t *mode, uint32_t *mask, int32_t *pos, int32_t *n_nodes,
+                   int32_t *status, void *ws, size_t ws_bytes, mfd_stream_t stream) {
+  if (!tk_logp || !tk_tok || !anchor_tok || !parent || !token || !depth || !score || !mode || !mask || !pos ||
+      !n_nodes || !status)
+    return MFD_ERR_INVALID_ARG;
+  if (n_req < 1 || K < 1 || L < 1 || topk < 1 || B < 1) return MFD_ERR_INVALID_ARG;
+  if (K > 16 || L > 16 || topk > 32 || B > 512 || K * B > 2048) return MFD_ERR_UNSUPPORTED;
+  int cap = 0, tsize = 0;
+  if (mfd::tree_smem_bytes(K, L, topk, B, &cap, &tsize) == 0) return MFD_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < tree_bytes(n_req) || !aligned(ws, 256)) return MFD_ERR_WORKSPACE;
+  mfd::TreeLaunch T;
+  T.tk_logp = tk_logp;
+  T.tk_tok = tk_tok;
+  T.n_req = n_req;
+  T.K = K;
+  T.L = L;
+  T.topk = topk;
+  T.B = B;
+  T.anchor = anchor_tok;
+  T.base_pos = base_pos;
+  T.parent = parent;
+  T.token = token;
+  T.depth = depth;
+  T.score = score;
+  T.mode = mode;
+  T.mask = mask;
+  T.pos = pos;
+  T.n_nodes = n_nodes;
+  T.status = status;
+  T.union_ws = static_cast<int32_t *>(ws);
+  return cuda_status(mfd::launch_build_tree(T, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mfd_verify(const float *target_logits, int n_req, int B, int V, int L, const int32_t *parent,
+               const int32_t *token, const int32_t *n_nodes, const float *temperature, const uint64_t *seed,
+               int32_t *accept_len, int32_t *path_nodes, int32_t *out_tokens, int32_t *status, void *ws,
+               size_t ws_bytes, mfd_stream_t stream) {
+  if (!target_logits || !parent || !token || !n_nodes || !temperature || !seed || !accept_len || !path_nodes ||
+      !out_tokens || !status)
+    return MFD_ERR_INVALID_ARG;
+  if (n_req < 1 || B < 1 || V < 2 || L < 1) return MFD_ERR_INVALID_ARG;
+  if (B > 512 || L > 16 || V >= (1 << 30)) return MFD_ERR_UNSUPPORTED;
+  DeviceInfo d;
+  int rc = current_device_info(&d);
+  if (rc != MFD_OK) return rc;
+  if (!ws || ws_bytes < verify_bytes(d.n_sm) || !aligned(ws, 256)) return MFD_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char *base = static_cast<char *>(ws);
+  if ((rc = cuda_status(cudaMemsetAsync(base, 0, kVerifyBarBytes, s))) != MFD_OK) return rc;
+  mfd::VerifyLaunch Vl;
+  Vl.t = target_logits;
+  Vl.n_req = n_req;
+  Vl.B = B;
+  Vl.V = V;
+  Vl.L = L;
+  Vl.parent = parent;
+  Vl.token = token;
+  Vl.n_nodes = n_nodes;
+  Vl.temperature = temperature;
+  Vl.seed = seed;
+  Vl.accept_len = accept_len;
+  Vl.path_nodes = path_nodes;
+  Vl.out_tokens = out_tokens;
+  Vl.status = status;
+  Vl.bar = reinterpret_cast<unsigned *>(base);
+  Vl.part = reinterpret_cast<float2 *>(base + kVerifyBarBytes);
+  Vl.grid = mfd::verify_max_grid(d.n_sm);
+  return cuda_status(mfd::launch_verify(Vl, s));
+}
+
+}  // extern "C"

@@ -1,0 +1,186 @@
+"""Thin ctypes binding of libmfd (include/mfd.h).
+
+Each ``mfd_*`` function has the C entry point's name and arguments; torch
+tensors stand in for device pointers, and the current torch CUDA stream is
+used unless one is given.  The binding only marshals arguments: every step of
+the round runs in the library's CUDA kernels.  There is no fallback: if the
+library has not been built, or the device is not an sm_103a GPU, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmfd.so")
+
+MFD_OK = 0
+MFD_ERR_INVALID_ARG = 1
+MFD_ERR_UNSUPPORTED = 2
+MFD_ERR_WORKSPACE = 3
+MFD_ERR_CUDA = 4
+MFD_ERR_TIMEOUT = 5
+MFD_ERR_INPUT = 6
+
+MFD_OP_LMHEAD_TOPK = 0
+MFD_OP_LOGITS_TOPK = 1
+MFD_OP_BUILD_TREE = 2
+MFD_OP_VERIFY = 3
+
+EXPORTS = ("mfd_status_string", "mfd_workspace_size", "mfd_lmhead_topk", "mfd_logits_topk",
+           "mfd_build_tree", "mfd_verify")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MfdError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} (code {code})")
+        self.code = code
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libmfd.so; raises if it is missing (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libmfd.so not built ({p}); run `python -m tree_verified_speculative_gb300.build`")
+        lib = ctypes.CDLL(p)
+        P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.mfd_status_string.argtypes = [I]
+        lib.mfd_status_string.restype = ctypes.c_char_p
+        lib.mfd_workspace_size.argtypes = [I] * 8
+        lib.mfd_workspace_size.restype = SZ
+        lib.mfd_lmhead_topk.argtypes = [P, I, I, P, I, I, P, P, P, P, P, SZ, P]
+        lib.mfd_lmhead_topk.restype = I
+        lib.mfd_logits_topk.argtypes = [P, I, I, I, P, P, P, P, P, SZ, P]
+        lib.mfd_logits_topk.restype = I
+        lib.mfd_build_tree.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
+        lib.mfd_build_tree.restype = I
+        lib.mfd_verify.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P]
+        lib.mfd_verify.restype = I
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load().mfd_status_string(int(code)).decode()
+
+
+def _p(t) -> int | None:
+    if t is None:
+        return None
+    assert isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous(), "device tensors, contiguous"
+    return t.data_ptr()
+
+
+def _s(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != MFD_OK:
+        raise MfdError(rc, where)
+
+
+def mfd_workspace_size(op: int, n_req: int = 1, K: int = 1, L: int = 1, topk: int = 1, B: int = 1,
+                       R: int = 1, V: int = 16) -> int:
+    return int(load().mfd_workspace_size(op, n_req, K, L, topk, B, R, V))
+
+
+def mfd_lmhead_topk(h, W, topk, tk_logp, tk_tok, lse, status, ws, stream=None) -> None:
+    R, H = h.shape
+    V = W.shape[0]
+    assert h.dtype == torch.bfloat16 and W.dtype == torch.bfloat16 and W.shape[1] == H
+    rc = load().mfd_lmhead_topk(_p(h), R, H, _p(W), V, topk, _p(tk_logp), _p(tk_tok), _p(lse), _p(status),
+                                _p(ws), ws.numel() * ws.element_size(), _s(stream))
+    _check(rc, "mfd_lmhead_topk")
+
+
+def mfd_logits_topk(logits, topk, tk_logp, tk_tok, lse, status, ws, stream=None) -> None:
+    R, V = logits.shape
+    assert logits.dtype == torch.float32
+    rc = load().mfd_logits_topk(_p(logits), R, V, topk, _p(tk_logp), _p(tk_tok), _p(lse), _p(status), _p(ws),
+                                ws.numel() * ws.element_size(), _s(stream))
+    _check(rc, "mfd_logits_topk")
+
+
+def mfd_build_tree(tk_logp, tk_tok, n_req, K, L, topk, B, anchor_tok, base_pos, parent, token, depth, score,
+                   mode, mask, pos, n_nodes, status, ws, stream=None) -> None:
+    rc = load().mfd_build_tree(_p(tk_logp), _p(tk_tok), n_req, K, L, topk, B, _p(anchor_tok), _p(base_pos),
+                               _p(parent), _p(token), _p(depth), _p(score), _p(mode), _p(mask), _p(pos),
+                               _p(n_nodes), _p(status), _p(ws), ws.numel() * ws.element_size(), _s(stream))
+    _check(rc, "mfd_build_tree")
+
+
+def mfd_verify(target_logits, n_req, B, V, L, parent, token, n_nodes, temperature, seed, accept_len,
+               path_nodes, out_tokens, status, ws, stream=None) -> None:
+    rc = load().mfd_verify(_p(target_logits), n_req, B, V, L, _p(parent), _p(token), _p(n_nodes),
+                           _p(temperature), _p(seed), _p(accept_len), _p(path_nodes), _p(out_tokens),
+                           _p(status), _p(ws), ws.numel() * ws.element_size(), _s(stream))
+    _check(rc, "mfd_verify")
+
+
+# ---------------------------------------------------------------------------
+class Round:
+    """Device buffers for one drafting round of n_req requests, reused from
+    call to call (allocation happens here, once, never inside the calls)."""
+
+    def __init__(self, n_req: int, K: int, L: int, topk: int, B: int, V: int, device="cuda"):
+        self.n_req, self.K, self.L, self.topk, self.B, self.V = n_req, K, L, topk, B, V
+        R = n_req * K * L
+        N = B + 1
+        W32 = (N + 31) // 32
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.R = R
+        self.tk_logp = torch.empty((R, topk), dtype=torch.float32, device=dev)
+        self.tk_tok = torch.empty((R, topk), **i32)
+        self.lse = torch.empty((R,), dtype=torch.float32, device=dev)
+        self.parent = torch.empty((n_req, N), **i32)
+        self.token = torch.empty((n_req, N), **i32)
+        self.depth = torch.empty((n_req, N), **i32)
+        self.score = torch.empty((n_req, N), dtype=torch.float32, device=dev)
+        self.mode = torch.empty((n_req, N), **i32)
+        self.mask = torch.empty((n_req, N, W32), **i32)
+        self.pos = torch.empty((n_req, N), **i32)
+        self.n_nodes = torch.empty((n_req,), **i32)
+        self.accept_len = torch.empty((n_req,), **i32)
+        self.path_nodes = torch.empty((n_req, L + 1), **i32)
+        self.out_tokens = torch.empty((n_req, L + 1), **i32)
+        self.status = torch.zeros((1,), **i32)
+        self.anchor = torch.zeros((n_req,), **i32)
+        self.base_pos = torch.zeros((n_req,), **i32)
+        ws = max(mfd_workspace_size(MFD_OP_LMHEAD_TOPK, n_req, K, L, topk, B, R, V),
+                 mfd_workspace_size(MFD_OP_LOGITS_TOPK, n_req, K, L, topk, B, R, V),
+                 mfd_workspace_size(MFD_OP_BUILD_TREE, n_req, K, L, topk, B, R, V),
+                 mfd_workspace_size(MFD_OP_VERIFY, n_req, K, L, topk, B, R, V))
+        self.ws = torch.empty((ws + 255) // 256 * 256, dtype=torch.uint8, device=dev)
+
+    def lmhead_topk(self, h, W, stream=None):
+        mfd_lmhead_topk(h, W, self.topk, self.tk_logp, self.tk_tok, self.lse, self.status, self.ws, stream)
+
+    def logits_topk(self, logits, stream=None):
+        mfd_logits_topk(logits, self.topk, self.tk_logp, self.tk_tok, self.lse, self.status, self.ws, stream)
+
+    def build_tree(self, stream=None):
+        mfd_build_tree(self.tk_logp, self.tk_tok, self.n_req, self.K, self.L, self.topk, self.B, self.anchor,
+                       self.base_pos, self.parent, self.token, self.depth, self.score, self.mode, self.mask,
+                       self.pos, self.n_nodes, self.status, self.ws, stream)
+
+    def verify(self, target_logits, temperature, seed, stream=None):
+        mfd_verify(target_logits, self.n_req, self.B, self.V, self.L, self.parent, self.token, self.n_nodes,
+                   temperature, seed, self.accept_len, self.path_nodes, self.out_tokens, self.status, self.ws,
+                   stream)
