@@ -12,8 +12,9 @@
 //   D[128 x 256] (TMEM, fp32) = h_tile[128 x H] . W_tile[256 x H]^T
 //
 // A = 128 hidden rows (one M tile, zero-filled past R), B = 256 vocabulary
-// rows, K streamed in 64-element (128-byte, swizzled) chunks through a
-// 4-stage shared-memory ring.  Each TMEM lane is one hidden row, so the
+// rows, K streamed through a 2-stage shared-memory ring; a stage holds two
+// 64-element (128-byte, swizzled) K atoms, so every weight row contributes
+// 256 contiguous bytes per stage (fewer DRAM page openings per byte).  Each TMEM lane is one hidden row, so the
 // epilogue thread that owns lane r reads its row's logits column by column
 // and keeps the row's running max, running sum of exp and a sorted top-T in
 // registers -- no cross-thread reduction.
@@ -35,17 +36,22 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
+constexpr int BK = 64;            // one 128-byte swizzle atom of bf16
+constexpr int KSUB = 2;           // K atoms per pipeline stage: 256 contiguous bytes per weight row
+constexpr int STAGES = 2;
+constexpr int A_SUB = BM * BK * 2;  // one K atom of the hidden tile
+constexpr int B_SUB = BN * BK * 2;  // one K atom of the weight tile
+constexpr int A_BYTES = KSUB * A_SUB;
+constexpr int B_BYTES = KSUB * B_SUB;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr int STAGE_STRIDE = 36;  // floats per staged row (16-byte aligned rows)
+constexpr int STAGE_ROW_BYTES = 32 * STAGE_STRIDE * 4;  // one epilogue warp's 32 rows
 
 constexpr int smem_bytes() {
-  return 1024 /* alignment slack */ + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5) + 16;
+  return 1024 /* alignment slack */ + STAGES * STAGE_BYTES + 4 * STAGE_ROW_BYTES + 8 * (2 * STAGES + 5) + 16;
 }
 
 struct Params {
@@ -93,7 +99,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t *sA = smem;
   uint8_t *sB = smem + STAGES * A_BYTES;
-  uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+  float *stage_all = reinterpret_cast<float *>(sB + STAGES * B_BYTES);
+  uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES + 4 * STAGE_ROW_BYTES);
   uint64_t *empty = full + STAGES;
   uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + 2;
@@ -130,6 +137,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int nk = p.H / BK;
+  // The prologue above may overlap the previous grid; global memory is
+  // touched only after it has finished.
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -143,14 +154,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         int mt, t0, t1, range;
         item_range(p, item, mt, t0, t1, range);
         for (int t = t0; t < t1 && ok; ++t) {
-          for (int kc = 0; kc < nk; ++kc) {
+          for (int kc = 0; kc < nk; kc += KSUB) {
+            const int nsub = nk - kc < KSUB ? nk - kc : KSUB;
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-            tma_load_2d(sA + stage * A_BYTES, &tmap_h, kc * BK, mt * BM, &full[stage], pol_h);
-            tma_load_2d(sB + stage * B_BYTES, &tmap_w, kc * BK, t * BN, &full[stage], pol_w);
+            mbar_arrive_expect_tx(&full[stage], (uint32_t)(nsub * (A_SUB + B_SUB)));
+            for (int sub = 0; sub < nsub; ++sub)
+              tma_load_2d(sB + stage * B_BYTES + sub * B_SUB, &tmap_w, (kc + sub) * BK, t * BN, &full[stage], pol_w);
+            for (int sub = 0; sub < nsub; ++sub)
+              tma_load_2d(sA + stage * A_BYTES + sub * A_SUB, &tmap_h, (kc + sub) * BK, mt * BM, &full[stage], pol_h);
             issued |= 1u << stage;
             issued_par = phase ? (issued_par | (1u << stage)) : (issued_par & ~(1u << stage));
             if (++stage == STAGES) {
@@ -185,17 +199,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-          for (int kc = 0; kc < nk; ++kc) {
+          for (int kc = 0; kc < nk; kc += KSUB) {
+            const int nsub = nk - kc < KSUB ? nk - kc : KSUB;
             if (!mbar_wait(&full[stage], phase, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * A_BYTES));
-            const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * B_BYTES));
+            for (int sub = 0; sub < nsub; ++sub) {
+              const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * A_BYTES + sub * A_SUB));
+              const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * B_BYTES + sub * B_SUB));
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              tc_mma_f16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kc | kk) != 0);
+              for (int kk = 0; kk < BK / 16; ++kk)
+                tc_mma_f16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kc | sub | kk) != 0);
+            }
             tc_commit(&empty[stage]);
             if (++stage == STAGES) {
               stage = 0;
@@ -220,6 +237,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // --------------------------------------------------------- epilogue
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
+    float *stage = stage_all + (warp - 2) * (STAGE_ROW_BYTES / 4);
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -247,12 +265,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           float x[32];
           tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), x);
           const int v0 = t * BN + c * 32;
-          float cmax = -INFINITY;
+          if (v0 + 32 > p.V) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            x[j] = (v0 + j < p.V) ? x[j] : -INFINITY;
-            cmax = fmaxf(cmax, x[j]);
+            for (int j = 0; j < 32; ++j) x[j] = (v0 + j < p.V) ? x[j] : -INFINITY;
           }
+          float cmax = x[0];
+#pragma unroll
+          for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, x[j]);
           if (cmax > -INFINITY) {
             if (cmax > m) {
               S *= exp2f((m - cmax) * LOG2E);
@@ -261,9 +280,27 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float mb = m * LOG2E;
 #pragma unroll
             for (int j = 0; j < 32; ++j) S += exp2f(fmaf(x[j], LOG2E, -mb));
+          }
+          // Top-T: one bit per column that beats this row's current T-th
+          // entry (a later column never ties its way in: its id is larger).
+          // Only the set bits are visited, so the warp pays for the largest
+          // candidate count among its 32 rows, not for every column.
+          const float thr = tv[T - 1];
+          uint32_t cm = 0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (x[j] > tv[T - 1]) topk_insert<T>(tv, ti, x[j], v0 + j);
+          for (int j = 0; j < 32; ++j) cm |= (x[j] > thr ? 1u : 0u) << j;
+          if (__any_sync(0xffffffffu, cm != 0)) {
+            float *st = stage + lane * STAGE_STRIDE;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4 *>(st + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+            while (__any_sync(0xffffffffu, cm != 0)) {
+              if (cm) {
+                const int j = __ffs(cm) - 1;
+                cm &= cm - 1;
+                const float xv = st[j];
+                if (xv > tv[T - 1]) topk_insert<T>(tv, ti, xv, v0 + j);
+              }
+            }
           }
         }
         tc_fence_before();
@@ -314,7 +351,18 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
                                        smem_bytes());
   if (e != cudaSuccess) return e;
   const int grid = p.n_items < L.n_sm ? p.n_items : L.n_sm;
-  lmhead_topk_kernel<T><<<grid, THREADS, smem_bytes(), stream>>>(*L.tmap_h, *L.tmap_w, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem_bytes();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, lmhead_topk_kernel<T>, *L.tmap_h, *L.tmap_w, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

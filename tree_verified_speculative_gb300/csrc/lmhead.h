@@ -54,7 +54,6 @@ struct TreeLaunch {
   int32_t *mode;
   uint32_t *mask;
   int32_t *pos, *n_nodes, *status;
-  int32_t *union_ws;  // [n_req][16][512]
 };
 size_t tree_smem_bytes(int K, int L, int topk, int B, int *cap_out, int *tsize_out);
 cudaError_t launch_build_tree(const TreeLaunch &T, cudaStream_t stream);

@@ -132,7 +132,10 @@ TopkLayout logits_layout(int R, int V, int topk) {
 constexpr size_t kVerifyBarBytes = 4096;  // up to 1024 group counters
 size_t verify_bytes(int n_sm) { return kVerifyBarBytes + align256((size_t)mfd::verify_max_grid(n_sm) * 2 * 8); }
 
-size_t tree_bytes(int n_req) { return (size_t)n_req * 16 * 512 * 4; }
+size_t tree_bytes(int n_req) {
+  (void)n_req;
+  return 256;  // the tree is built in shared memory; the scratch is not used
+}
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -290,7 +293,6 @@ int mfd_build_tree(const float *tk_logp, const int32_t *tk_tok, int n_req, int K
   T.pos = pos;
   T.n_nodes = n_nodes;
   T.status = status;
-  T.union_ws = static_cast<int32_t *>(ws);
   return cuda_status(mfd::launch_build_tree(T, reinterpret_cast<cudaStream_t>(stream)));
 }
 

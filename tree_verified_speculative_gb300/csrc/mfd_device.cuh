@@ -181,6 +181,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- PDL
+// Programmatic dependent launch: wait until the grids this one depends on
+// have finished and their writes are visible (a no-op without PDL), and let
+// the next grid in the stream start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- misc
 // fp32 -> uint32 key whose ascending order is the float's DESCENDING order;
 // -0.0 is folded onto +0.0 so that equal floats get equal keys.

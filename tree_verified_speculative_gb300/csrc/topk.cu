@@ -12,7 +12,7 @@
 namespace mfd {
 namespace {
 
-constexpr int MERGE_WARPS = 4;
+constexpr int MERGE_THREADS = 256;
 constexpr int SURV_CAP = 256;  // survivors a warp gathers before falling back
 constexpr int MAX_LISTS_PER_LANE = 8;  // P <= 256
 
@@ -40,131 +40,126 @@ __device__ __forceinline__ Cand warp_best(Cand c) {
   return c;
 }
 
+// One CTA per row, one thread per list: the row's P lists (T candidates
+// each, best first) and its P (max, sum exp) pairs are staged in shared
+// memory with 16-byte loads, then every step is a parallel count:
+//   LSE   = M + log sum_q S_q exp(m_q - M)
+//   tau   = the topk-th best list head (ties ordered by list): at least topk
+//           candidates are at least as good, so nothing worse can make it
+//   top-k = survivors (the prefix of each list not worse than tau) ranked by
+//           counting how many survivors beat each one
 template <int T>
-__global__ void __launch_bounds__(MERGE_WARPS * 32)
+__global__ void __launch_bounds__(MERGE_THREADS)
     merge_topk_kernel(const float2 *__restrict__ part_ms, const int2 *__restrict__ part_cand, int R, int P,
                       int topk, float *__restrict__ tk_logp, int32_t *__restrict__ tk_tok, float *__restrict__ lse_out) {
-  __shared__ Cand surv[MERGE_WARPS][SURV_CAP];
-  __shared__ Cand park[MERGE_WARPS][32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * MERGE_WARPS + warp;
+  extern __shared__ int4 merge_smem[];
+  __shared__ Cand surv[SURV_CAP];
+  __shared__ Cand top[32];
+  __shared__ float red[MERGE_THREADS / 32];
+  __shared__ Cand tau_s;
+  __shared__ int n_surv_s;
+  __shared__ float lse_s, m_s;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x;
   if (row >= R) return;
-  const float2 *ms = part_ms + (size_t)row * P;
-  const int2 *cand = part_cand + (size_t)row * P * T;
-
-  // ---- log-sum-exp over the ranges
-  float mloc = -INFINITY;
-  for (int q = lane; q < P; q += 32) mloc = fmaxf(mloc, __ldcg(&ms[q]).x);
-  const float M = warp_max(mloc);
-  float sloc = 0.f;
-  for (int q = lane; q < P; q += 32) {
-    const float2 e = __ldcg(&ms[q]);
-    if (e.x > -INFINITY) sloc += e.y * expf(e.x - M);
-  }
-  const float lse = M + logf(warp_sum(sloc));
-
-  // ---- tau = the topk-th best list head: at least topk candidates are
-  // at least as good, so nothing worse than tau can make the top-k.
-  Cand head[MAX_LISTS_PER_LANE];
-#pragma unroll
-  for (int s = 0; s < MAX_LISTS_PER_LANE; ++s) {
-    const int q = lane + 32 * s;
-    head[s] = (q < P) ? load_cand(cand + (size_t)q * T) : Cand{-INFINITY, 0x7FFFFFFF};
-  }
-  Cand tau = Cand{-INFINITY, 0x7FFFFFFF};
+  int2 *cs = reinterpret_cast<int2 *>(merge_smem);
+  float2 *ms = reinterpret_cast<float2 *>(cs + (size_t)P * T);
   {
-    Cand h2[MAX_LISTS_PER_LANE];
-#pragma unroll
-    for (int s = 0; s < MAX_LISTS_PER_LANE; ++s) h2[s] = head[s];
-    const int rounds = topk < P ? topk : P;
-    for (int r = 0; r < rounds; ++r) {
-      Cand b = h2[0];
-      int bs = 0;
-#pragma unroll
-      for (int s = 1; s < MAX_LISTS_PER_LANE; ++s)
-        if (vi_before(h2[s].v, h2[s].i, b.v, b.i)) {
-          b = h2[s];
-          bs = s;
-        }
-      const Cand w = warp_best(b);
-      const unsigned owner = __ballot_sync(0xffffffffu, b.v == w.v && b.i == w.i);
-      if (lane == __ffs(owner) - 1) {
-#pragma unroll
-        for (int s = 0; s < MAX_LISTS_PER_LANE; ++s)
-          if (s == bs) h2[s] = Cand{-INFINITY, 0x7FFFFFFF};
-      }
-      tau = w;
-    }
-    if (rounds < topk) tau = Cand{-INFINITY, 0x7FFFFFFF};  // fewer lists than topk: keep everything
+    const int4 *src = reinterpret_cast<const int4 *>(part_cand + (size_t)row * P * T);
+    const int n4 = P * T / 2;
+    for (int i = tid; i < n4; i += MERGE_THREADS) merge_smem[i] = __ldcg(src + i);
+    for (int i = tid; i < P; i += MERGE_THREADS) ms[i] = __ldcg(part_ms + (size_t)row * P + i);
+  }
+  if (tid == 0) {
+    n_surv_s = 0;
+    tau_s = Cand{-INFINITY, 0x7FFFFFFF};
+  }
+  __syncthreads();
+  auto cand_at = [&](int q, int c) {
+    const int2 e = cs[q * T + c];
+    return Cand{__int_as_float(e.x), e.y};
+  };
+  const int q = tid;  // this thread's list
+  const bool has = q < P;
+
+  // ---- log-sum-exp
+  float x = has ? ms[q].x : -INFINITY;
+  x = warp_max(x);
+  if (lane == 0) red[warp] = x;
+  __syncthreads();
+  if (tid == 0) {
+    float M = red[0];
+    for (int w = 1; w < MERGE_THREADS / 32; ++w) M = fmaxf(M, red[w]);
+    m_s = M;
+  }
+  __syncthreads();
+  const float M = m_s;
+  float sv = (has && ms[q].x > -INFINITY) ? ms[q].y * expf(ms[q].x - M) : 0.f;
+  sv = warp_sum(sv);
+  __syncthreads();
+  if (lane == 0) red[warp] = sv;
+  __syncthreads();
+  if (tid == 0) {
+    float S = 0.f;
+    for (int w = 0; w < MERGE_THREADS / 32; ++w) S += red[w];
+    lse_s = M + logf(S);
   }
 
-  // ---- gather survivors (a prefix of each list)
-  int cnt[MAX_LISTS_PER_LANE];
-  int total = 0;
-#pragma unroll
-  for (int s = 0; s < MAX_LISTS_PER_LANE; ++s) {
-    const int q = lane + 32 * s;
-    int c = 0;
-    if (q < P) {
-      const int2 *L = cand + (size_t)q * T;
-      while (c < T) {
-        const Cand e = load_cand(L + c);
-        if (vi_before(tau.v, tau.i, e.v, e.i)) break;  // e is worse than tau
-        ++c;
-      }
+  // ---- tau: rank of this list's head among all heads
+  const int need = topk < P ? topk : P;
+  if (has) {
+    const Cand h = cand_at(q, 0);
+    int r = 0;
+    for (int o = 0; o < P; ++o) {
+      const Cand g = cand_at(o, 0);
+      r += vi_before(g.v, g.i, h.v, h.i) || (g.v == h.v && g.i == h.i && o < q);
     }
-    cnt[s] = c;
-    total += c;
+    if (r == need - 1 && need == topk) tau_s = h;
   }
-  int incl = total;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  const int n_surv = __shfl_sync(0xffffffffu, incl, 31);
-  Cand mine = Cand{-INFINITY, 0x7FFFFFFF};
-  int rank_mine = 1 << 30;
-  const bool fast = n_surv <= SURV_CAP;
-  if (fast) {
-    int off = incl - total;
-#pragma unroll
-    for (int s = 0; s < MAX_LISTS_PER_LANE; ++s) {
-      const int q = lane + 32 * s;
-      for (int c = 0; c < cnt[s]; ++c) surv[warp][off++] = load_cand(cand + (size_t)q * T + c);
+  __syncthreads();
+  const Cand tau = tau_s;  // (-inf, max) when there are fewer lists than topk: keep all
+
+  // ---- survivors: the prefix of each list not worse than tau
+  int c = 0;
+  if (has)
+    while (c < T) {
+      const Cand e = cand_at(q, c);
+      if (vi_before(tau.v, tau.i, e.v, e.i)) break;
+      ++c;
     }
-    __syncwarp();
-    // rank by counting; equal keys (padding only) are ordered by slot
-    for (int a = lane; a < n_surv; a += 32) {
-      const Cand e = surv[warp][a];
+  const int slot = c ? atomicAdd(&n_surv_s, c) : 0;
+  if (c && slot + c <= SURV_CAP)
+    for (int k = 0; k < c; ++k) surv[slot + k] = cand_at(q, k);
+  __syncthreads();
+  const int n_surv = n_surv_s;
+  if (n_surv <= SURV_CAP) {
+    for (int a = tid; a < n_surv; a += MERGE_THREADS) {
+      const Cand e = surv[a];
       int r = 0;
       for (int b = 0; b < n_surv; ++b) {
-        const Cand f = surv[warp][b];
+        const Cand f = surv[b];
         r += vi_before(f.v, f.i, e.v, e.i) || (f.v == e.v && f.i == e.i && b < a);
       }
-      if (r < topk) park[warp][r] = e;
+      if (r < topk) top[r] = e;
     }
-    __syncwarp();
-    if (lane < topk) {
-      mine = park[warp][lane];
-      rank_mine = lane;
-    }
-  } else {
-    // slow path: topk rounds of "best remaining list head", from memory
+  } else if (warp == 0) {
+    // many exact ties at the cut: topk rounds of "best remaining list head"
     int pos[MAX_LISTS_PER_LANE];
 #pragma unroll
-    for (int s = 0; s < MAX_LISTS_PER_LANE; ++s) pos[s] = 0;
+    for (int s2 = 0; s2 < MAX_LISTS_PER_LANE; ++s2) pos[s2] = 0;
     for (int r = 0; r < topk; ++r) {
       Cand b = Cand{-INFINITY, 0x7FFFFFFF};
       int bs = -1;
 #pragma unroll
-      for (int s = 0; s < MAX_LISTS_PER_LANE; ++s) {
-        const int q = lane + 32 * s;
-        if (q < P && pos[s] < T) {
-          const Cand e = load_cand(cand + (size_t)q * T + pos[s]);
+      for (int s2 = 0; s2 < MAX_LISTS_PER_LANE; ++s2) {
+        const int qq = lane + 32 * s2;
+        if (qq < P && pos[s2] < T) {
+          const Cand e = cand_at(qq, pos[s2]);
           if (bs < 0 || vi_before(e.v, e.i, b.v, b.i)) {
             b = e;
-            bs = s;
+            bs = s2;
           }
         }
       }
@@ -172,30 +167,29 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32)
       const unsigned owner = __ballot_sync(0xffffffffu, bs >= 0 && b.v == w.v && b.i == w.i);
       if (lane == __ffs(owner) - 1) {
 #pragma unroll
-        for (int s = 0; s < MAX_LISTS_PER_LANE; ++s)
-          if (s == bs) ++pos[s];
+        for (int s2 = 0; s2 < MAX_LISTS_PER_LANE; ++s2)
+          if (s2 == bs) ++pos[s2];
       }
-      if (lane == r) {
-        mine = w;
-        rank_mine = r;
-      }
+      if (lane == 0) top[r] = w;
     }
   }
+  __syncthreads();
 
   // ---- log-probabilities, final order (log p desc, id asc)
-  const float lp = mine.v - lse;
-  int r2 = 0;
-  for (int o = 0; o < 32; ++o) {
-    const float olp = __shfl_sync(0xffffffffu, lp, o);
-    const int oi = __shfl_sync(0xffffffffu, mine.i, o);
-    const int orank = __shfl_sync(0xffffffffu, rank_mine, o);
-    if (orank < topk && o != lane) r2 += vi_before(olp, oi, lp, mine.i);
-  }
-  if (rank_mine < topk) {
+  if (tid < topk) {
+    const float lse = lse_s;
+    const Cand e = top[tid];
+    const float lp = e.v - lse;
+    int r2 = 0;
+    for (int o = 0; o < topk; ++o) {
+      if (o == tid) continue;
+      const float olp = top[o].v - lse;
+      r2 += vi_before(olp, top[o].i, lp, e.i);
+    }
     tk_logp[(size_t)row * topk + r2] = lp;
-    tk_tok[(size_t)row * topk + r2] = mine.i;
+    tk_tok[(size_t)row * topk + r2] = e.i;
+    if (tid == 0 && lse_out) lse_out[row] = lse;
   }
-  if (lane == 0 && lse_out) lse_out[row] = lse;
 }
 
 // One warp per (row, vocabulary chunk): lane-local online softmax and top-T,
@@ -270,10 +264,22 @@ __global__ void __launch_bounds__(128)
 
 template <int T>
 cudaError_t merge_t(const MergeLaunch &M, cudaStream_t s) {
-  const int grid = (M.R + MERGE_WARPS - 1) / MERGE_WARPS;
-  merge_topk_kernel<T><<<grid, MERGE_WARPS * 32, 0, s>>>(reinterpret_cast<const float2 *>(M.part_ms),
-                                                        reinterpret_cast<const int2 *>(M.part_cand), M.R, M.P,
-                                                        M.topk, M.tk_logp, M.tk_tok, M.lse);
+  const size_t smem = (size_t)M.P * T * 8 + (size_t)M.P * 8;
+  cudaError_t e = cudaFuncSetAttribute(merge_topk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(M.R);
+  cfg.blockDim = dim3(MERGE_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, merge_topk_kernel<T>, reinterpret_cast<const float2 *>(M.part_ms),
+                         reinterpret_cast<const int2 *>(M.part_cand), M.R, M.P, M.topk, M.tk_logp, M.tk_tok, M.lse);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -4,35 +4,32 @@
 // tree, which is the union of the per-mode trees at the common cut-off;
 // shared prefixes are built once.
 //
-// One CTA (512 threads) builds one request's tree in shared memory.
+// One CTA (512 threads) builds one request's tree in shared memory, in two
+// parts.
 //
-// Keys.  A prefix is ordered by (s desc, token ids lexicographically asc, a
-// proper prefix first).  For the lexicographic part every drafted position i
-// gets the sorted union U_i of all modes' top-k tokens at i (at most 512),
-// and a prefix is encoded as the tuple of its tokens' indices in U_i, 9 bits
-// per position, zero-padded past its depth, followed by its depth: comparing
-// these 149-bit keys as unsigned integers is exactly the lexicographic order
-// of the token sequences, with a proper prefix first.  Equal keys mean equal
-// sequences, so the key also identifies a node.
+// Part 1, per mode (warp k = mode k, warp-synchronous only).  Mode k's B best
+// prefixes under its own key (score_k desc, tokens lexicographically asc, a
+// proper prefix first).  Within one mode a prefix is a tuple of ranks, one
+// per position; replacing each rank by its token's rank inside that row
+// (5 bits, token ids compared unsigned) turns the lexicographic token order
+// into plain unsigned comparison of packed 80-bit keys, depth last.  The
+// search is level by level: level t expands the depth-t entries in rank
+// order (child scores only fall) while the child is not after the mode's
+// current B-th best entry (kappa, from a 4-pass radix select on the score
+// plus exact tie resolution on the key).  kappa only improves, so nothing
+// that belongs to the mode's top-B is ever dropped.  If the pool fills,
+// kappa is tightened, the pool pruned, and expansion resumes where each
+// entry stopped.  The mode's top-B is then sorted (warp bitonic sort).
 //
-// Search.  The pool holds (mode, prefix) entries scored by their own mode.
-// Level t expands the depth-t entries of the pool: the children of a mode-k
-// entry come from mode k's row at depth t+1 in rank order, so their scores
-// only fall.  A cut-off key kappa prunes the search: kappa = the best, over
-// modes, of each mode's B-th best entry.  Each mode's entries are distinct
-// prefixes, and a prefix's mixture score is at least its mode score, so at
-// least B distinct prefixes are at least as good as kappa: the true B-th
-// prefix of the mixture is never worse than kappa, and every entry that can
-// reach the tree is kept.  kappa only improves as entries arrive.  When the
-// pool fills up, kappa is recomputed, the pool pruned, and the expansion
-// resumes where it stopped (each entry remembers its next child rank).
-//
-// Result.  After the last level the pool holds every (mode, prefix) entry
-// that is at least as good as the final kappa, which includes the best-mode
-// entry of every prefix in the tree.  A hash table on the prefix key keeps,
-// per prefix, the entry with the best (score, then smallest mode); the B
-// best of those are the tree.  Node order comes from rank counting, parents
-// from a table lookup of the prefix key with its last position removed.
+// Part 2, merge (all warps).  A prefix of the mixture tree is in the top-B
+// list of every mode that attains its score, so the K sorted lists hold the
+// tree.  Each list entry's token sequence is hashed; a hash table keeps, per
+// sequence, the entry with the best (score, smallest mode) -- equality is
+// checked on the full sequence, and a collision reseeds the table.  These
+// "primary" entries are distinct prefixes keyed by (s, tokens).  A primary's
+// node index is 1 + the number of primaries before it, summed over the K
+// lists by binary search; the first B form the tree.  Parents come from the
+// table (hash of the sequence without its last token).
 #include "lmhead.h"
 #include "mfd_device.cuh"
 
@@ -41,56 +38,46 @@ namespace {
 
 constexpr int THREADS = 512;
 constexpr int NWARPS = THREADS / 32;
-constexpr int TIE_CAP = 1024;
-constexpr int MAX_PASSES = 256;
+constexpr int MAX_PASSES = 1024;
 
-struct Entry {
-  uint64_t g0, g1, g2;  // prefix key: positions 1-7, 8-14, 15-16 + depth
-  float score;          // the entry's own-mode score (fp32 left fold)
-  uint8_t mode, depth, next_j, pad;
+// Pool entry of one mode (16 bytes).  k0: row ranks of positions 1..12,
+// 5 bits each, position 1 highest (bits 59..55).  k1: positions 13..16 at
+// bits 24..5, depth at bits 4..0, next child rank at bits 31..26.
+struct PE {
+  float score;
+  uint32_t k1;
+  uint64_t k0;
 };
-static_assert(sizeof(Entry) == 32, "entry layout");
+static_assert(sizeof(PE) == 16, "pool entry");
 
-struct Key {
-  uint32_t sk;  // desc_key(score)
-  uint64_t g0, g1, g2;
+constexpr uint32_t K1_KEY = 0x01FFFFFFu;
+
+__device__ __forceinline__ void pk_set(uint64_t &k0, uint32_t &k1, int p, uint32_t s) {
+  if (p <= 12) {
+    const int sh = 55 - 5 * (p - 1);
+    k0 = (k0 & ~((uint64_t)31 << sh)) | ((uint64_t)(s & 31u) << sh);
+  } else {
+    const int sh = 20 - 5 * (p - 13);
+    k1 = (k1 & ~(31u << sh)) | ((s & 31u) << sh);
+  }
+}
+__device__ __forceinline__ uint32_t pk_get(uint64_t k0, uint32_t k1, int p) {
+  return p <= 12 ? (uint32_t)(k0 >> (55 - 5 * (p - 1))) & 31u : (k1 >> (20 - 5 * (p - 13))) & 31u;
+}
+__device__ __forceinline__ int pk_depth(uint32_t k1) { return (int)(k1 & 31u); }
+__device__ __forceinline__ int pk_next(uint32_t k1) { return (int)(k1 >> 26); }
+
+struct MK {  // key within one mode
+  uint32_t sk;
+  uint64_t k0;
+  uint32_t k1;
 };
-
-__device__ __forceinline__ Key key_of(const Entry &e) { return Key{desc_key(e.score), e.g0, e.g1, e.g2}; }
-
-__device__ __forceinline__ bool key_before(const Key &a, const Key &b) {
+__device__ __forceinline__ MK mk_of(const PE &e) { return MK{desc_key(e.score), e.k0, e.k1 & K1_KEY}; }
+__device__ __forceinline__ bool mk_before(const MK &a, const MK &b) {
   if (a.sk != b.sk) return a.sk < b.sk;
-  if (a.g0 != b.g0) return a.g0 < b.g0;
-  if (a.g1 != b.g1) return a.g1 < b.g1;
-  return a.g2 < b.g2;
+  if (a.k0 != b.k0) return a.k0 < b.k0;
+  return a.k1 < b.k1;
 }
-
-__device__ __forceinline__ bool gk_less(uint64_t a0, uint64_t a1, uint64_t a2, uint64_t b0, uint64_t b1,
-                                        uint64_t b2) {
-  if (a0 != b0) return a0 < b0;
-  if (a1 != b1) return a1 < b1;
-  return a2 < b2;
-}
-
-// Position pos (1-based) of the key holds the token's index in U_pos.
-__device__ __forceinline__ void gk_set(uint64_t &g0, uint64_t &g1, uint64_t &g2, int pos, uint32_t u) {
-  const int w = (pos - 1) / 7, sl = (pos - 1) % 7;
-  const int sh = 54 - 9 * sl;
-  const uint64_t m = (uint64_t)0x1FF << sh, v = (uint64_t)(u & 0x1FF) << sh;
-  if (w == 0)
-    g0 = (g0 & ~m) | v;
-  else if (w == 1)
-    g1 = (g1 & ~m) | v;
-  else
-    g2 = (g2 & ~m) | v;
-}
-__device__ __forceinline__ uint32_t gk_get(uint64_t g0, uint64_t g1, uint64_t g2, int pos) {
-  const int w = (pos - 1) / 7, sl = (pos - 1) % 7;
-  const int sh = 54 - 9 * sl;
-  const uint64_t g = (w == 0) ? g0 : (w == 1) ? g1 : g2;
-  return (uint32_t)((g >> sh) & 0x1FF);
-}
-__device__ __forceinline__ void gk_set_depth(uint64_t &g2, int d) { g2 = (g2 & ~(uint64_t)31) | (uint64_t)d; }
 
 __device__ __forceinline__ uint64_t mix64(uint64_t x) {
   x ^= x >> 30;
@@ -100,11 +87,11 @@ __device__ __forceinline__ uint64_t mix64(uint64_t x) {
   x ^= x >> 31;
   return x;
 }
-__device__ __forceinline__ uint64_t gk_hash(uint64_t g0, uint64_t g1, uint64_t g2, uint64_t seed) {
-  uint64_t h = mix64(g0 ^ seed);
-  h = mix64(h ^ g1 ^ 0x632BE59BD9B4E019ull);
-  h = mix64(h ^ g2 ^ 0x8CB92BA72F3D8DD7ull);
-  return h | 1ull;  // 0 marks an empty slot
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
 }
 
 __device__ __forceinline__ int warp_excl_scan(int x, int lane) {
@@ -117,6 +104,12 @@ __device__ __forceinline__ int warp_excl_scan(int x, int lane) {
   return incl - x;
 }
 
+// Lanes hitting the same bin are merged first: one atomic per bin per warp.
+__device__ __forceinline__ void warp_hist_add(int *hist, int bin) {
+  const unsigned m = __match_any_sync(0xffffffffu, bin);
+  if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(m) - 1) atomicAdd(&hist[bin], __popc(m));
+}
+
 struct Params {
   const float *tk_logp;
   const int32_t *tk_tok;
@@ -127,500 +120,470 @@ struct Params {
   int32_t *mode;
   uint32_t *mask;
   int32_t *pos, *n_nodes, *status;
-  int32_t *union_ws;
-  int cap, tsize;
+  int pc;     // pool capacity per mode
+  int tsize;  // hash table slots (power of two)
 };
 
 struct Layout {
-  size_t pool, live0, live1, freel, alive, nodeof, hslot, lp, gam, table, hist1, ties, par, nslot, total;
+  size_t lp, tok, sig, inv, pool, hv, hp, hslot, pcnt, nodeid, prim, table, par, nslot, total;
 };
 
-__host__ __device__ inline size_t al(size_t o, size_t a) { return (o + a - 1) / a * a; }
+__host__ __device__ inline size_t al16(size_t o) { return (o + 15) & ~(size_t)15; }
 
-__host__ __device__ inline Layout make_layout(int K, int L, int topk, int B, int cap, int tsize) {
+__host__ __device__ inline Layout make_layout(int K, int L, int topk, int B, int pc, int tsize) {
   Layout y;
   size_t o = 0;
-  const size_t klt = (size_t)K * L * topk;
-  const size_t hist = (size_t)K * 256 * 4, tbl = (size_t)tsize * 16;
+  const size_t klt = (size_t)K * L * topk, ne = (size_t)K * B;
+  const size_t hist = (size_t)NWARPS * 256 * 4, tbl = al16((size_t)tsize * 4) + (size_t)tsize * 8;
   y.pool = o;
-  o += (size_t)cap * 32;
-  y.live0 = o = al(o, 16);
-  o += (size_t)cap * 2;
-  y.live1 = o = al(o, 16);
-  o += (size_t)cap * 2;
-  y.freel = o = al(o, 16);
-  o += (size_t)cap * 2;
-  y.nodeof = o = al(o, 16);
-  o += (size_t)cap * 2;
-  y.hslot = o = al(o, 16);
-  o += (size_t)cap * 2;
-  y.alive = o = al(o, 16);
-  o += (size_t)cap;
-  y.lp = o = al(o, 16);
-  o += klt * 4;
-  y.gam = o = al(o, 16);
-  o += klt * 2;
-  y.table = o = al(o, 16);
+  o += (size_t)K * pc * 16;
+  y.hv = o = al16(o);
+  o += ne * 8;
+  y.hp = o = al16(o);
+  o += ne * 8;
+  y.table = o = al16(o);  // hash tags (u32) then best (u64); the per-warp histograms overlay it
   o += hist > tbl ? hist : tbl;
-  y.hist1 = o = al(o, 16);
-  o += 256 * 4;
-  y.ties = o = al(o, 16);
-  o += TIE_CAP * 2;
-  y.par = o = al(o, 16);
+  y.lp = o = al16(o);
+  o += klt * 4;
+  y.tok = o = al16(o);
+  o += klt * 4;
+  y.hslot = o = al16(o);
+  o += ne * 2;
+  y.pcnt = o = al16(o);
+  o += ne * 2;
+  y.nodeid = o = al16(o);
+  o += ne * 2;
+  y.par = o = al16(o);
   o += (size_t)(B + 1) * 2;
-  y.nslot = o = al(o, 16);
+  y.nslot = o = al16(o);
   o += (size_t)(B + 1) * 2;
-  y.total = al(o, 128);
+  y.sig = o = al16(o);
+  o += klt;
+  y.inv = o = al16(o);
+  o += klt;
+  y.prim = o = al16(o);
+  o += ne;
+  y.total = (o + 127) & ~(size_t)127;
   return y;
 }
 
-// Scalars shared by the whole CTA.
 struct Shared {
-  int n_live, n_new, tail, nfree, free_used, overflow, any_child, bad, has_kappa, nties, tie_over, coll;
-  int n_sel, n_prim;
-  int cur;  // which live buffer is current
-  int cnt[16], active[16], rem[16], ntie[16];
-  uint32_t pre[16];
-  uint64_t kg[16][3];
-  Key kappa;
+  int bad, coll, total_prim;
+  int cnt[16], off[17];
 };
 
-// The B-th best key (score desc, prefix key asc) within each group.  Group
-// of live entry i: grp(i) in [0, G) or -1 (ignored).  Sets sh.active[g] for
-// groups with at least B members and, for those, sh.pre[g] (score key) and
-// sh.kg[g] (prefix key) of their B-th best entry; sh.has_kappa = any active.
-template <typename GroupFn>
-__device__ void select_bth(Shared &sh, const Entry *pool, const uint16_t *live, int n_live, int G, int B,
-                           uint32_t *hist, uint16_t *ties, GroupFn grp) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid < 16) {
-    sh.cnt[tid] = 0;
-    sh.pre[tid] = 0;
-    sh.rem[tid] = B;
-    sh.ntie[tid] = 0;
-  }
-  if (tid == 0) {
-    sh.nties = 0;
-    sh.tie_over = 0;
-  }
-  __syncthreads();
-  for (int i = tid; i < n_live; i += THREADS) {
-    const int g = grp(i);
-    if (g >= 0) atomicAdd(&sh.cnt[g], 1);
-  }
-  __syncthreads();
-  if (tid < 16) sh.active[tid] = (tid < G && sh.cnt[tid] >= B);
-  __syncthreads();
-  if (tid == 0) {
-    int any = 0;
-    for (int g = 0; g < G; ++g) any |= sh.active[g];
-    sh.has_kappa = any;
-  }
-  __syncthreads();
-  if (!sh.has_kappa) return;
+struct Ctx {
+  const float *lp;
+  const int32_t *tok;
+  const uint8_t *sig, *inv;
+  int K, L, topk, B, pc;
+};
 
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < G * 256; i += THREADS) hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < n_live; i += THREADS) {
-      const int g = grp(i);
-      if (g < 0 || !sh.active[g]) continue;
-      const uint32_t sk = desc_key(pool[live[i]].score);
-      if (pass == 0 || (sk >> (shift + 8)) == (sh.pre[g] >> (shift + 8)))
-        atomicAdd(&hist[g * 256 + ((sk >> shift) & 255u)], 1u);
-    }
-    __syncthreads();
-    for (int g = warp; g < G; g += NWARPS) {
-      if (!sh.active[g]) continue;
-      uint32_t c[8];
-      int sum = 0;
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        c[b] = hist[g * 256 + lane * 8 + b];
-        sum += (int)c[b];
-      }
-      const int excl = warp_excl_scan(sum, lane);
-      const int rem = sh.rem[g];
-      int run = excl, fb = -1, fbefore = 0, fcnt = 0;
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        if (fb < 0 && run < rem && rem <= run + (int)c[b]) {
-          fb = lane * 8 + b;
-          fbefore = run;
-          fcnt = (int)c[b];
-        }
-        run += (int)c[b];
-      }
-      if (fb >= 0) {
-        sh.pre[g] |= (uint32_t)fb << shift;
-        sh.rem[g] = rem - fbefore;
-        sh.ntie[g] = fcnt;
-      }
-    }
-    __syncthreads();
-  }
-  // Among the entries of group g whose score key equals pre[g], the B-th is
-  // the rem[g]-th smallest prefix key.
-  for (int i = tid; i < n_live; i += THREADS) {
-    const int g = grp(i);
-    if (g < 0 || !sh.active[g]) continue;
-    const Entry &e = pool[live[i]];
-    if (desc_key(e.score) != sh.pre[g]) continue;
-    if (sh.ntie[g] == 1) {
-      sh.kg[g][0] = e.g0;
-      sh.kg[g][1] = e.g1;
-      sh.kg[g][2] = e.g2;
-    } else {
-      const int k = atomicAdd(&sh.nties, 1);
-      if (k < TIE_CAP)
-        ties[k] = (uint16_t)i;
-      else
-        sh.tie_over = 1;
-    }
-  }
-  __syncthreads();
-  if (sh.nties > 0) {
-    if (!sh.tie_over) {
-      const int nt = sh.nties;
-      for (int a = tid; a < nt; a += THREADS) {
-        const int ia = ties[a];
-        const int g = grp(ia);
-        const Entry &e = pool[live[ia]];
-        int r = 1;
-        for (int b = 0; b < nt; ++b) {
-          const int ib = ties[b];
-          if (grp(ib) != g) continue;
-          const Entry &f = pool[live[ib]];
-          r += gk_less(f.g0, f.g1, f.g2, e.g0, e.g1, e.g2);
-        }
-        if (r == sh.rem[g]) {
-          sh.kg[g][0] = e.g0;
-          sh.kg[g][1] = e.g1;
-          sh.kg[g][2] = e.g2;
-        }
-      }
-    } else {
-      // many exact score ties: rank against the whole live list
-      for (int a = tid; a < n_live; a += THREADS) {
-        const int g = grp(a);
-        if (g < 0 || !sh.active[g] || sh.ntie[g] == 1) continue;
-        const Entry &e = pool[live[a]];
-        if (desc_key(e.score) != sh.pre[g]) continue;
-        int r = 1;
-        for (int b = 0; b < n_live; ++b) {
-          if (grp(b) != g) continue;
-          const Entry &f = pool[live[b]];
-          if (desc_key(f.score) != sh.pre[g]) continue;
-          r += gk_less(f.g0, f.g1, f.g2, e.g0, e.g1, e.g2);
-        }
-        if (r == sh.rem[g]) {
-          sh.kg[g][0] = e.g0;
-          sh.kg[g][1] = e.g1;
-          sh.kg[g][2] = e.g2;
-        }
-      }
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    Key best{0xFFFFFFFFu, ~0ull, ~0ull, ~0ull};
-    bool have = false;
-    for (int g = 0; g < G; ++g) {
-      if (!sh.active[g]) continue;
-      const Key k{sh.pre[g], sh.kg[g][0], sh.kg[g][1], sh.kg[g][2]};
-      if (!have || key_before(k, best)) {
-        best = k;
-        have = true;
-      }
-    }
-    sh.kappa = best;
-  }
-  __syncthreads();
+// token at position p (1-based) of a mode-k key
+__device__ __forceinline__ uint32_t token_at(const Ctx &c, int k, uint64_t k0, uint32_t k1, int p) {
+  const int row = (k * c.L + p - 1) * c.topk;
+  return (uint32_t)c.tok[row + c.inv[row + pk_get(k0, k1, p)]];
 }
 
-__global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params P) {
+// Lexicographic order of two prefixes of possibly different modes, by token
+// ids (unsigned), a proper prefix first: <0, 0, >0.
+__device__ int seq_cmp(const Ctx &c, int ka, const PE &a, int kb, const PE &b) {
+  const int da = pk_depth(a.k1), db = pk_depth(b.k1);
+  const int d = da < db ? da : db;
+  for (int p = 1; p <= d; ++p) {
+    const uint32_t ta = token_at(c, ka, a.k0, a.k1, p), tb = token_at(c, kb, b.k0, b.k1, p);
+    if (ta != tb) return ta < tb ? -1 : 1;
+  }
+  return da - db;
+}
+
+// (s desc, tokens asc) across modes: true iff a is strictly before b.
+__device__ __forceinline__ bool x_before(const Ctx &c, int ka, const PE &a, int kb, const PE &b) {
+  const uint32_t sa = desc_key(a.score), sb = desc_key(b.score);
+  if (sa != sb) return sa < sb;
+  return seq_cmp(c, ka, a, kb, b) < 0;
+}
+
+// ---------------------------------------------------------------- part 1
+// The B-th best entry of P[0, n) (warp-wide).  Returns false when n < B.
+__device__ bool warp_kth(const PE *P, int n, int B, int *hist, MK &kap) {
+  const int lane = threadIdx.x & 31;
+  if (n < B) return false;
+  uint32_t pre = 0;
+  int rem = B, ntie = 0;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int b = lane; b < 256; b += 32) hist[b] = 0;
+    __syncwarp();
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      int bin = -1;
+      if (i < n) {
+        const uint32_t sk = desc_key(P[i].score);
+        if (pass == 0 || (sk >> (shift + 8)) == (pre >> (shift + 8))) bin = (int)((sk >> shift) & 255u);
+      }
+      warp_hist_add(hist, bin);
+    }
+    __syncwarp();
+    int c[8], sum = 0;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      c[b] = hist[lane * 8 + b];
+      sum += c[b];
+    }
+    int run = warp_excl_scan(sum, lane);
+    int fb = -1, fbefore = 0, fcnt = 0;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      if (fb < 0 && run < rem && rem <= run + c[b]) {
+        fb = lane * 8 + b;
+        fbefore = run;
+        fcnt = c[b];
+      }
+      run += c[b];
+    }
+    const unsigned who = __ballot_sync(0xffffffffu, fb >= 0);
+    const int src = __ffs(who) - 1;
+    fb = __shfl_sync(0xffffffffu, fb, src);
+    fbefore = __shfl_sync(0xffffffffu, fbefore, src);
+    fcnt = __shfl_sync(0xffffffffu, fcnt, src);
+    pre |= (uint32_t)fb << shift;
+    rem -= fbefore;
+    ntie = fcnt;
+    __syncwarp();
+  }
+  // the rem-th smallest key among the entries whose score key is pre
+  uint64_t b0 = 0;
+  uint32_t b1 = 0;
+  bool found = false;
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    bool hit = false;
+    if (i < n && desc_key(P[i].score) == pre) {
+      if (ntie == 1) {
+        hit = true;
+      } else {
+        const uint64_t e0 = P[i].k0;
+        const uint32_t e1 = P[i].k1 & K1_KEY;
+        int r = 1;
+        for (int f = 0; f < n; ++f) {
+          if (desc_key(P[f].score) != pre) continue;
+          const uint64_t f0 = P[f].k0;
+          const uint32_t f1 = P[f].k1 & K1_KEY;
+          r += (f0 < e0) || (f0 == e0 && f1 < e1);
+        }
+        hit = (r == rem);
+      }
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, hit);
+    if (m) {
+      const int isrc = base + __ffs(m) - 1;
+      b0 = P[isrc].k0;
+      b1 = P[isrc].k1 & K1_KEY;
+      found = true;
+      break;
+    }
+  }
+  kap = MK{pre, b0, b1};
+  return found;
+}
+
+// Keep the entries not after kap; in place, order preserved.  Returns n.
+__device__ int warp_prune(PE *P, int n, const MK &kap) {
+  const int lane = threadIdx.x & 31;
+  int out = 0;
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    PE e;
+    bool keep = false;
+    if (i < n) {
+      e = P[i];
+      keep = !mk_before(kap, mk_of(e));
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    __syncwarp();
+    if (keep) P[out + __popc(m & lanemask_lt())] = e;
+    out += __popc(m);
+    __syncwarp();
+  }
+  return out;
+}
+
+// Expand the depth-t entries of P[0, n) in rank order (children appended
+// after n).  Returns true when the pool filled before every child that can
+// still make the cut was appended.
+__device__ bool warp_expand(const Ctx &c, int k, int t, PE *P, int &n, bool hk, const MK &kap, bool &any) {
+  const int lane = threadIdx.x & 31;
+  const int n0 = n;
+  const int row = (k * c.L + t) * c.topk;  // depth t+1 uses row index t
+  bool overflow = false;
+  for (int base = 0; base < n0 && !overflow; base += 32) {
+    const int i = base + lane;
+    PE par;
+    bool isp = false, act = false;
+    int j = 0;
+    if (i < n0) {
+      par = P[i];
+      isp = pk_depth(par.k1) == t;
+      j = pk_next(par.k1);
+      act = isp && j < c.topk;
+    }
+    while (__any_sync(0xffffffffu, act)) {
+      bool want = false;
+      PE ch;
+      if (act) {
+        const float lv = c.lp[row + j];
+        if (!(lv > -INFINITY)) {
+          act = false;
+          j = c.topk;
+        } else {
+          ch.score = __fadd_rn(par.score, lv);
+          ch.k0 = par.k0;
+          ch.k1 = par.k1 & ~(31u | (63u << 26));
+          pk_set(ch.k0, ch.k1, t + 1, c.sig[row + j]);
+          ch.k1 |= (uint32_t)(t + 1);
+          if (!hk) {
+            want = true;
+          } else {
+            const MK ck = mk_of(ch);
+            if (ck.sk > kap.sk) {
+              act = false;  // every later rank scores no better
+              j = c.topk;
+            } else if (mk_before(kap, ck)) {
+              ++j;  // same score, after kappa in token order; a later rank may not be
+              if (j >= c.topk) act = false;
+            } else {
+              want = true;
+            }
+          }
+        }
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, want);
+      const int cnt = __popc(m);
+      const int room = c.pc - n;
+      const int r = __popc(m & lanemask_lt());
+      if (want) {
+        if (r < room) {
+          P[n + r] = ch;
+          ++j;
+          if (j >= c.topk) act = false;
+        } else {
+          act = false;  // j kept: resumed in the next pass
+          overflow = true;
+        }
+      }
+      n += cnt < room ? cnt : room;
+      if (cnt) any = true;
+      overflow = __any_sync(0xffffffffu, overflow);
+      if (overflow) act = false;
+    }
+    if (isp) P[i].k1 = (P[i].k1 & ~(63u << 26)) | ((uint32_t)j << 26);
+    __syncwarp();
+  }
+  return overflow;
+}
+
+// Sort P[0, n) ascending by key (warp bitonic sort; P has room for the next
+// power of two of n).  The padding sorts last.
+__device__ void warp_sort(PE *P, int n) {
+  const int lane = threadIdx.x & 31;
+  int np2 = 1;
+  while (np2 < n) np2 <<= 1;
+  for (int i = n + lane; i < np2; i += 32) {
+    P[i].score = -INFINITY;
+    P[i].k0 = ~0ull;
+    P[i].k1 = K1_KEY;
+  }
+  __syncwarp();
+  for (int size = 2; size <= np2; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int ls = __ffs(stride) - 1;
+      for (int e = lane; e < np2 / 2; e += 32) {
+        const int lo = ((e >> ls) << (ls + 1)) | (e & (stride - 1)), hi = lo + stride;
+        const bool asc = (lo & size) == 0;
+        const PE a = P[lo], b = P[hi];
+        if (mk_before(mk_of(b), mk_of(a)) == asc) {
+          P[lo] = b;
+          P[hi] = a;
+        }
+      }
+      __syncwarp();
+    }
+}
+
+__global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ Shared sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = blockIdx.x;
-  const int K = P.K, L = P.L, topk = P.topk, B = P.B;
-  const int KT = K * topk;
+  const int K = prm.K, L = prm.L, topk = prm.topk, B = prm.B, PC = prm.pc, tsize = prm.tsize;
   const int KLT = K * L * topk;
-  const int cap = P.cap, tsize = P.tsize;
-  const Layout lay = make_layout(K, L, topk, B, cap, tsize);
-  Entry *pool = reinterpret_cast<Entry *>(smem + lay.pool);
-  uint16_t *livebuf[2] = {reinterpret_cast<uint16_t *>(smem + lay.live0),
-                          reinterpret_cast<uint16_t *>(smem + lay.live1)};
-  uint16_t *freel = reinterpret_cast<uint16_t *>(smem + lay.freel);
-  int16_t *nodeof = reinterpret_cast<int16_t *>(smem + lay.nodeof);
-  uint16_t *hslot = reinterpret_cast<uint16_t *>(smem + lay.hslot);
-  uint8_t *alive = smem + lay.alive;
+  const Layout lay = make_layout(K, L, topk, B, PC, tsize);
   float *lp_s = reinterpret_cast<float *>(smem + lay.lp);
-  uint16_t *gam_s = reinterpret_cast<uint16_t *>(smem + lay.gam);
-  uint32_t *hist = reinterpret_cast<uint32_t *>(smem + lay.table);
-  uint64_t *tag = reinterpret_cast<uint64_t *>(smem + lay.table);
-  uint64_t *best = tag + tsize;
-  uint32_t *hist1 = reinterpret_cast<uint32_t *>(smem + lay.hist1);
-  uint16_t *ties = reinterpret_cast<uint16_t *>(smem + lay.ties);
+  int32_t *tok_s = reinterpret_cast<int32_t *>(smem + lay.tok);
+  uint8_t *sig_s = smem + lay.sig;
+  uint8_t *inv_s = smem + lay.inv;
+  PE *pools = reinterpret_cast<PE *>(smem + lay.pool);
+  uint64_t *hv = reinterpret_cast<uint64_t *>(smem + lay.hv);
+  uint64_t *hp = reinterpret_cast<uint64_t *>(smem + lay.hp);
+  uint32_t *tag = reinterpret_cast<uint32_t *>(smem + lay.table);
+  uint64_t *best = reinterpret_cast<uint64_t *>(smem + lay.table + al16((size_t)tsize * 4));
+  int *hists = reinterpret_cast<int *>(smem + lay.table);
+  uint16_t *hslot = reinterpret_cast<uint16_t *>(smem + lay.hslot);
+  uint16_t *pcnt = reinterpret_cast<uint16_t *>(smem + lay.pcnt);
+  int16_t *nodeid = reinterpret_cast<int16_t *>(smem + lay.nodeid);
+  uint8_t *prim = smem + lay.prim;
   int16_t *par_s = reinterpret_cast<int16_t *>(smem + lay.par);
   uint16_t *nslot = reinterpret_cast<uint16_t *>(smem + lay.nslot);
 
-  const float *glp = P.tk_logp + (size_t)q * KLT;
-  const int32_t *gtk = P.tk_tok + (size_t)q * KLT;
-  int32_t *U = P.union_ws + (size_t)q * 16 * 512;
+  const float *glp = prm.tk_logp + (size_t)q * KLT;
+  const int32_t *gtk = prm.tk_tok + (size_t)q * KLT;
 
-  // ---------------------------------------------------- 0: tables, checks
+  // ---------------------------------------------------- tables and checks
   if (tid == 0) sh.bad = 0;
   __syncthreads();
   for (int e = tid; e < KLT; e += THREADS) {
     const float v = glp[e];
     lp_s[e] = v;
+    tok_s[e] = gtk[e];
     const int j = e % topk;
     if (isnan(v) || v > 0.f || (j > 0 && !(glp[e - 1] >= v))) sh.bad = 1;
   }
   __syncthreads();
-
-  // ---------------------------------------------------- 1: token unions
-  {
-    int up2 = 32;
-    while (up2 < KT) up2 <<= 1;
-    uint64_t *scratch = reinterpret_cast<uint64_t *>(smem + lay.pool);
-    for (int i = warp; i < L; i += NWARPS) {
-      uint64_t *arr = scratch + (size_t)warp * up2;
-      for (int e = lane; e < up2; e += 32) {
-        if (e < KT) {
-          const int k = e / topk, j = e % topk;
-          const uint32_t tk = (uint32_t)gtk[((size_t)k * L + i) * topk + j];
-          arr[e] = ((uint64_t)tk << 32) | ((uint64_t)k << 16) | (uint64_t)j;
-        } else {
-          arr[e] = ~0ull;
-        }
-      }
-      __syncwarp();
-      for (int size = 2; size <= up2; size <<= 1)
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          for (int e = lane; e < up2 / 2; e += 32) {
-            const int lo = 2 * stride * (e / stride) + (e % stride), hi = lo + stride;
-            const bool asc = (lo & size) == 0;
-            const uint64_t a = arr[lo], b = arr[hi];
-            if ((a > b) == asc) {
-              arr[lo] = b;
-              arr[hi] = a;
-            }
-          }
-          __syncwarp();
-        }
-      const int seg = up2 / 32, beg = lane * seg;
-      int cnt = 0;
-      for (int e = beg; e < beg + seg; ++e)
-        if (e < KT && (e == 0 || (arr[e] >> 32) != (arr[e - 1] >> 32))) ++cnt;
-      int g = warp_excl_scan(cnt, lane) - 1;
-      for (int e = beg; e < beg + seg && e < KT; ++e) {
-        const uint64_t x = arr[e];
-        const bool isnew = (e == 0) || ((x >> 32) != (arr[e - 1] >> 32));
-        if (isnew) {
-          ++g;
-          U[i * 512 + g] = (int32_t)(uint32_t)(x >> 32);
-        } else if (((arr[e - 1] >> 16) & 0xFFFF) == ((x >> 16) & 0xFFFF)) {
-          sh.bad = 1;  // a token twice in one row
-        }
-        const int k = (int)((x >> 16) & 0xFFFF), j = (int)(x & 0xFFFF);
-        gam_s[((size_t)k * L + i) * topk + j] = (uint16_t)g;
-      }
-      __syncwarp();
+  for (int e = tid; e < KLT; e += THREADS) {
+    const int j = e % topk, row = e - j;
+    const uint32_t me = (uint32_t)tok_s[e];
+    int s = 0, dup = 0;
+    for (int f = 0; f < topk; ++f) {
+      const uint32_t o = (uint32_t)tok_s[row + f];
+      s += o < me;
+      dup += (o == me) && f != j;
     }
+    if (dup) sh.bad = 1;
+    sig_s[e] = (uint8_t)s;
+    inv_s[row + s] = (uint8_t)j;
   }
   __syncthreads();
   if (sh.bad) {
-    if (tid == 0) report(P.status, MFD_ERR_INPUT);
+    if (tid == 0) report(prm.status, MFD_ERR_INPUT);
     return;
   }
 
-  // ---------------------------------------------------- 2: depth-1 entries
+  // ---------------------------------------------------- part 1: per mode
+  const Ctx c{lp_s, tok_s, sig_s, inv_s, K, L, topk, B, PC};
+  if (warp < K) {
+    const int k = warp;
+    PE *P = pools + (size_t)k * PC;
+    int *hist = hists + warp * 256;
+    int n = 0;
+    for (int base = 0; base < topk; base += 32) {  // depth-1 entries
+      const int j = base + lane;
+      const int e = (k * L) * topk + j;
+      const bool ok = j < topk && lp_s[e] > -INFINITY;
+      const unsigned m = __ballot_sync(0xffffffffu, ok);
+      if (ok) {
+        PE en;
+        en.score = lp_s[e];
+        en.k0 = 0;
+        en.k1 = 1u;
+        pk_set(en.k0, en.k1, 1, sig_s[e]);
+        P[n + __popc(m & lanemask_lt())] = en;
+      }
+      n += __popc(m);
+    }
+    __syncwarp();
+    bool failed = false;
+    for (int t = 1; t < L && !failed; ++t) {
+      bool any = false;
+      int pass = 0;
+      for (; pass < MAX_PASSES; ++pass) {
+        MK kap{0, 0, 0};
+        const bool hk = warp_kth(P, n, B, hist, kap);
+        if (hk) n = warp_prune(P, n, kap);
+        if (!warp_expand(c, k, t, P, n, hk, kap, any)) break;
+      }
+      if (pass == MAX_PASSES) failed = true;
+      if (!any) break;
+    }
+    if (!failed) {
+      MK kap{0, 0, 0};
+      if (warp_kth(P, n, B, hist, kap)) n = warp_prune(P, n, kap);
+      if (n > B) failed = true;  // the B-th entry was not found: impossible for valid tables
+    }
+    if (failed) {
+      if (lane == 0) report(prm.status, MFD_ERR_UNSUPPORTED);
+      n = 0;
+    }
+    warp_sort(P, n);
+    if (lane == 0) sh.cnt[k] = n;
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------- part 2: merge
   if (tid == 0) {
-    sh.n_live = 0;
-    sh.tail = 0;
-    sh.nfree = 0;
-    sh.free_used = 0;
-    sh.cur = 0;
+    int o = 0;
+    for (int k = 0; k < K; ++k) {
+      sh.off[k] = o;
+      o += sh.cnt[k];
+    }
+    sh.off[K] = o;
   }
   __syncthreads();
-  for (int e = tid; e < KT; e += THREADS) {
-    const int k = e / topk, j = e % topk;
-    const float v = lp_s[((size_t)k * L) * topk + j];
-    if (v == -INFINITY) continue;
-    Entry en;
-    en.g0 = (uint64_t)gam_s[((size_t)k * L) * topk + j] << 54;
-    en.g1 = 0;
-    en.g2 = 1;
-    en.score = v;
-    en.mode = (uint8_t)k;
-    en.depth = 1;
-    en.next_j = 0;
-    en.pad = 0;
-    const int slot = atomicAdd(&sh.tail, 1);
-    pool[slot] = en;
-    livebuf[0][atomicAdd(&sh.n_live, 1)] = (uint16_t)slot;
-  }
-  __syncthreads();
-
-  // prune to the current kappa and rebuild the free list
-  auto prune = [&]() {
-    uint16_t *live = livebuf[sh.cur];
-    uint16_t *nlive = livebuf[sh.cur ^ 1];
-    const int n_live = sh.n_live, tail = sh.tail;
-    const bool hk = sh.has_kappa;
-    const Key kap = sh.kappa;
-    for (int i = tid; i < tail; i += THREADS) alive[i] = 0;
-    if (tid == 0) {
-      sh.n_new = 0;
-      sh.nfree = 0;
-      sh.free_used = 0;
-    }
-    __syncthreads();
-    for (int i = tid; i < n_live; i += THREADS) {
-      const int slot = live[i];
-      if (!hk || !key_before(kap, key_of(pool[slot]))) {
-        alive[slot] = 1;
-        nlive[atomicAdd(&sh.n_new, 1)] = (uint16_t)slot;
-      }
-    }
-    __syncthreads();
-    for (int i = tid; i < tail; i += THREADS)
-      if (!alive[i]) freel[atomicAdd(&sh.nfree, 1)] = (uint16_t)i;
-    __syncthreads();
-    if (tid == 0) {
-      sh.cur ^= 1;
-      sh.n_live = sh.n_new;
-    }
-    __syncthreads();
+  const int NE = sh.off[K];
+  auto entry_of = [&](int id, int &k, int &i) {
+    k = 0;
+    while (id >= sh.off[k + 1]) ++k;
+    i = id - sh.off[k];
   };
-
-  auto kappa_by_mode = [&]() {
-    const uint16_t *live = livebuf[sh.cur];
-    select_bth(sh, pool, live, sh.n_live, K, B, hist, ties, [&](int i) { return (int)pool[live[i]].mode; });
-  };
-
-  // ---------------------------------------------------- 3: level expansion
-  for (int t = 1; t < L; ++t) {
-    if (tid == 0) sh.any_child = 0;
-    int pass = 0;
-    for (; pass < MAX_PASSES; ++pass) {
-      kappa_by_mode();
-      prune();
-      if (tid == 0) sh.overflow = 0;
-      __syncthreads();
-      uint16_t *live = livebuf[sh.cur];
-      const int n0 = sh.n_live;
-      const bool hk = sh.has_kappa;
-      const Key kap = sh.kappa;
-      for (int i = tid; i < n0; i += THREADS) {
-        const int slot = live[i];
-        const Entry e = pool[slot];
-        if (e.depth != t || e.next_j >= topk) continue;
-        const int k = e.mode;
-        const float *lprow = lp_s + ((size_t)k * L + t) * topk;
-        const uint16_t *grow = gam_s + ((size_t)k * L + t) * topk;
-        int j = e.next_j;
-        while (j < topk) {
-          const float lv = lprow[j];
-          if (lv == -INFINITY) {
-            j = topk;
-            break;
-          }
-          const float cs = __fadd_rn(e.score, lv);
-          uint64_t c0 = e.g0, c1 = e.g1, c2 = e.g2;
-          gk_set(c0, c1, c2, t + 1, grow[j]);
-          gk_set_depth(c2, t + 1);
-          if (hk) {
-            const uint32_t csk = desc_key(cs);
-            if (csk > kap.sk) {
-              j = topk;  // every later rank scores no better
-              break;
-            }
-            if (csk == kap.sk && gk_less(kap.g0, kap.g1, kap.g2, c0, c1, c2)) {
-              ++j;
-              continue;
-            }
-          }
-          int s2 = -1;
-          const int f = atomicAdd(&sh.free_used, 1);
-          if (f < sh.nfree) {
-            s2 = freel[f];
-          } else {
-            const int tl = atomicAdd(&sh.tail, 1);
-            if (tl < cap) s2 = tl;
-          }
-          if (s2 < 0) {
-            sh.overflow = 1;
-            break;
-          }
-          Entry c;
-          c.g0 = c0;
-          c.g1 = c1;
-          c.g2 = c2;
-          c.score = cs;
-          c.mode = (uint8_t)k;
-          c.depth = (uint8_t)(t + 1);
-          c.next_j = 0;
-          c.pad = 0;
-          pool[s2] = c;
-          live[atomicAdd(&sh.n_live, 1)] = (uint16_t)s2;
-          sh.any_child = 1;
-          ++j;
-        }
-        pool[slot].next_j = (uint8_t)j;
-      }
-      __syncthreads();
-      if (tid == 0 && sh.tail > cap) sh.tail = cap;
-      __syncthreads();
-      if (!sh.overflow) break;
+  // hashes of each entry's token sequence and of its parent prefix
+  for (int id = tid; id < NE; id += THREADS) {
+    int k, i;
+    entry_of(id, k, i);
+    const PE e = pools[(size_t)k * PC + i];
+    const int d = pk_depth(e.k1);
+    uint64_t h = 0x2545F4914F6CDD1Dull, hpar = h;
+    for (int p = 1; p <= d; ++p) {
+      hpar = h;
+      h = mix64(h ^ ((uint64_t)token_at(c, k, e.k0, e.k1, p) + ((uint64_t)p << 40)));
     }
-    if (pass == MAX_PASSES) {
-      if (tid == 0) report(P.status, MFD_ERR_TIMEOUT);
-      return;
-    }
-    __syncthreads();
-    if (!sh.any_child) break;
+    hv[id] = h;
+    hp[id] = hpar;
   }
-  kappa_by_mode();
-  prune();
-
-  // ---------------------------------------------------- 4: one entry per prefix
-  const uint16_t *live = livebuf[sh.cur];
-  const int n_live = sh.n_live;
-  uint64_t seed = 0x2545F4914F6CDD1Dull;
+  uint64_t seed = 0;
   for (int attempt = 0; attempt < 4; ++attempt) {
-    for (int i = tid; i < tsize; i += THREADS) {
-      tag[i] = 0;
-      best[i] = ~0ull;
+    for (int s = tid; s < tsize; s += THREADS) {
+      tag[s] = 0;
+      best[s] = ~0ull;
     }
     if (tid == 0) sh.coll = 0;
     __syncthreads();
-    for (int i = tid; i < n_live; i += THREADS) {
-      const Entry &e = pool[live[i]];
-      const uint64_t h = gk_hash(e.g0, e.g1, e.g2, seed);
+    for (int id = tid; id < NE; id += THREADS) {
+      const uint64_t h = mix64(hv[id] ^ seed);
+      const uint32_t tg = (uint32_t)(h >> 32) | 1u;
       uint32_t s = (uint32_t)h & (uint32_t)(tsize - 1);
       for (int probe = 0; probe < tsize; ++probe) {
-        const unsigned long long prev =
-            atomicCAS(reinterpret_cast<unsigned long long *>(&tag[s]), 0ull, (unsigned long long)h);
-        if (prev == 0ull || prev == h) break;
+        const uint32_t prev = atomicCAS(&tag[s], 0u, tg);
+        if (prev == 0u || prev == tg) break;
         s = (s + 1) & (uint32_t)(tsize - 1);
       }
-      hslot[i] = (uint16_t)s;
+      hslot[id] = (uint16_t)s;
     }
     __syncthreads();
-    for (int i = tid; i < n_live; i += THREADS) {
-      const Entry &e = pool[live[i]];
-      const uint64_t packed = ((uint64_t)desc_key(e.score) << 32) | ((uint64_t)e.mode << 16) | (uint64_t)i;
-      atomicMin(reinterpret_cast<unsigned long long *>(&best[hslot[i]]), (unsigned long long)packed);
+    for (int id = tid; id < NE; id += THREADS) {
+      int k, i;
+      entry_of(id, k, i);
+      const PE e = pools[(size_t)k * PC + i];
+      const uint64_t packed = ((uint64_t)desc_key(e.score) << 32) | ((uint64_t)k << 16) | (uint64_t)id;
+      atomicMin(reinterpret_cast<unsigned long long *>(&best[hslot[id]]), (unsigned long long)packed);
     }
     __syncthreads();
-    for (int i = tid; i < n_live; i += THREADS) {
-      const Entry &e = pool[live[i]];
-      const Entry &r = pool[live[best[hslot[i]] & 0xFFFF]];
-      if (r.g0 != e.g0 || r.g1 != e.g1 || r.g2 != e.g2) sh.coll = 1;
+    for (int id = tid; id < NE; id += THREADS) {
+      const int rid = (int)(best[hslot[id]] & 0xFFFF);
+      if (rid == id) continue;
+      int k, i, rk, ri;
+      entry_of(id, k, i);
+      entry_of(rid, rk, ri);
+      if (seq_cmp(c, k, pools[(size_t)k * PC + i], rk, pools[(size_t)rk * PC + ri]) != 0) sh.coll = 1;
     }
     __syncthreads();
     if (!sh.coll) break;
@@ -628,61 +591,90 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params P) 
     __syncthreads();
   }
   if (sh.coll) {
-    if (tid == 0) report(P.status, MFD_ERR_UNSUPPORTED);
+    if (tid == 0) report(prm.status, MFD_ERR_UNSUPPORTED);
     return;
   }
-
-  // ---------------------------------------------------- 5: the B best prefixes
-  uint8_t *prim = alive;  // reused: prim[i] = live entry i is its prefix's best entry
-  for (int i = tid; i < n_live; i += THREADS) prim[i] = (int)(best[hslot[i]] & 0xFFFF) == i;
-  for (int i = tid; i < sh.tail; i += THREADS) nodeof[i] = -1;
-  __syncthreads();
-  select_bth(sh, pool, live, n_live, 1, B, hist1, ties, [&](int i) { return prim[i] ? 0 : -1; });
-  uint16_t *sel = livebuf[sh.cur ^ 1];
-  {
-    const bool hk = sh.has_kappa;
-    const Key kap = sh.kappa;
-    if (tid == 0) sh.n_sel = 0;
-    __syncthreads();
-    for (int i = tid; i < n_live; i += THREADS)
-      if (prim[i] && (!hk || !key_before(kap, key_of(pool[live[i]])))) sel[atomicAdd(&sh.n_sel, 1)] = live[i];
-    __syncthreads();
+  // primaries (one per distinct prefix) and their running counts per list
+  for (int id = tid; id < NE; id += THREADS) {
+    prim[id] = (int)(best[hslot[id]] & 0xFFFF) == id;
+    nodeid[id] = -1;
   }
-  const int n = sh.n_sel;  // min(B, number of distinct prefixes in the pool)
-  for (int a = tid; a < n; a += THREADS) {
-    const Key ka = key_of(pool[sel[a]]);
-    int r = 0;
-    for (int b = 0; b < n; ++b) r += key_before(key_of(pool[sel[b]]), ka);
-    nslot[r + 1] = sel[a];
-    nodeof[sel[a]] = (int16_t)(r + 1);
+  __syncthreads();
+  if (warp < K) {
+    const int k = warp, o = sh.off[k], n = sh.cnt[k];
+    int run = 0;
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      const int f = i < n ? prim[o + i] : 0;
+      const int incl = warp_excl_scan(f, lane) + f;
+      if (i < n) pcnt[o + i] = (uint16_t)(run + incl);
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int tot = 0;
+    for (int k = 0; k < K; ++k)
+      if (sh.cnt[k]) tot += pcnt[sh.off[k] + sh.cnt[k] - 1];
+    sh.total_prim = tot;
+  }
+  // node index of a primary: 1 + the primaries before it, over every list
+  for (int id = tid; id < NE; id += THREADS) {
+    if (!prim[id]) continue;
+    int k, i;
+    entry_of(id, k, i);
+    const PE e = pools[(size_t)k * PC + i];
+    int before = pcnt[id] - 1;
+    for (int k2 = 0; k2 < K && before < B; ++k2) {
+      if (k2 == k) continue;
+      const PE *P2 = pools + (size_t)k2 * PC;
+      int lo = 0, hi = sh.cnt[k2];  // first entry of list k2 not before e
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (x_before(c, k2, P2[mid], k, e))
+          lo = mid + 1;
+        else
+          hi = mid;
+      }
+      if (lo > 0) before += pcnt[sh.off[k2] + lo - 1];
+    }
+    if (before < B) {
+      nodeid[id] = (int16_t)(before + 1);
+      nslot[before + 1] = (uint16_t)id;
+    }
   }
   if (tid == 0) {
     par_s[0] = -1;
     sh.bad = 0;
   }
   __syncthreads();
-
-  // ---------------------------------------------------- 6: parents
-  for (int nd = 1 + tid; nd <= n; nd += THREADS) {
-    const Entry &e = pool[nslot[nd]];
-    const int d = e.depth;
+  const int nn = sh.total_prim < B ? sh.total_prim : B;
+  // parents: the table entry of the sequence without its last token
+  for (int nd = 1 + tid; nd <= nn; nd += THREADS) {
+    const int id = nslot[nd];
+    int k, i;
+    entry_of(id, k, i);
+    const PE e = pools[(size_t)k * PC + i];
+    const int d = pk_depth(e.k1);
     int par = 0;
     if (d > 1) {
-      uint64_t p0 = e.g0, p1 = e.g1, p2 = e.g2;
-      gk_set(p0, p1, p2, d, 0);
-      gk_set_depth(p2, d - 1);
-      const uint64_t h = gk_hash(p0, p1, p2, seed);
-      uint32_t s = (uint32_t)h & (uint32_t)(tsize - 1);
       par = -1;
-      for (int probe = 0; probe < tsize; ++probe) {
-        const uint64_t tg = tag[s];
-        if (tg == 0) break;
-        if (tg == h) {
-          const int ps = live[best[s] & 0xFFFF];
-          const Entry &r = pool[ps];
-          if (r.g0 == p0 && r.g1 == p1 && r.g2 == p2) {
-            par = nodeof[ps];
-            break;
+      const uint64_t h = mix64(hp[id] ^ seed);
+      const uint32_t tg = (uint32_t)(h >> 32) | 1u;
+      uint32_t s = (uint32_t)h & (uint32_t)(tsize - 1);
+      for (int probe = 0; probe < tsize && par < 0; ++probe) {
+        const uint32_t t0 = tag[s];
+        if (t0 == 0u) break;
+        if (t0 == tg) {
+          const int rid = (int)(best[s] & 0xFFFF);
+          int rk, ri;
+          entry_of(rid, rk, ri);
+          const PE r = pools[(size_t)rk * PC + ri];
+          if (pk_depth(r.k1) == d - 1) {
+            bool same = true;
+            for (int p = 1; p < d && same; ++p)
+              same = token_at(c, rk, r.k0, r.k1, p) == token_at(c, k, e.k0, e.k1, p);
+            if (same) par = nodeid[rid];
           }
         }
         s = (s + 1) & (uint32_t)(tsize - 1);
@@ -693,50 +685,51 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params P) 
   }
   __syncthreads();
   if (sh.bad) {
-    if (tid == 0) report(P.status, MFD_ERR_INPUT);
+    if (tid == 0) report(prm.status, MFD_ERR_INPUT);
     return;
   }
 
-  // ---------------------------------------------------- 7: outputs
+  // ---------------------------------------------------- outputs
   const int N = B + 1, W32 = (N + 31) / 32;
   const size_t ob = (size_t)q * N;
-  const int anchor = P.anchor[q];
-  const int bp = P.base_pos ? P.base_pos[q] : 0;
-  for (int i = tid; i < N; i += THREADS) {
+  const int anchor = prm.anchor[q];
+  const int bp = prm.base_pos ? prm.base_pos[q] : 0;
+  for (int nd = tid; nd < N; nd += THREADS) {
     int pa = -1, tk = -1, dp = -1, md = -1, ps = -1;
     float sc = -INFINITY;
-    if (i == 0) {
+    if (nd == 0) {
       tk = anchor;
       dp = 0;
       sc = 0.f;
       ps = bp;
-    } else if (i <= n) {
-      const Entry &e = pool[nslot[i]];
-      dp = e.depth;
-      pa = par_s[i];
-      tk = U[(dp - 1) * 512 + (int)gk_get(e.g0, e.g1, e.g2, dp)];
+    } else if (nd <= nn) {
+      int k, i;
+      entry_of(nslot[nd], k, i);
+      const PE e = pools[(size_t)k * PC + i];
+      dp = pk_depth(e.k1);
+      pa = par_s[nd];
+      tk = (int)token_at(c, k, e.k0, e.k1, dp);
       sc = e.score;
-      md = e.mode;
+      md = k;
       ps = bp + dp;
     }
-    P.parent[ob + i] = pa;
-    P.token[ob + i] = tk;
-    P.depth[ob + i] = dp;
-    P.score[ob + i] = sc;
-    P.mode[ob + i] = md;
-    P.pos[ob + i] = ps;
+    prm.parent[ob + nd] = pa;
+    prm.token[ob + nd] = tk;
+    prm.depth[ob + nd] = dp;
+    prm.score[ob + nd] = sc;
+    prm.mode[ob + nd] = md;
+    prm.pos[ob + nd] = ps;
   }
   for (int x = tid; x < N * W32; x += THREADS) {
     const int i = x / W32, w = x - (x / W32) * W32;
     uint32_t word = 0;
-    if (i <= n)
+    if (i <= nn)
       for (int a = i; a >= 0; a = (a == 0) ? -1 : par_s[a])
         if ((a >> 5) == w) word |= 1u << (a & 31);
-    P.mask[(size_t)q * N * W32 + x] = word;
+    prm.mask[(size_t)q * N * W32 + x] = word;
   }
-  if (tid == 0) P.n_nodes[q] = n + 1;
+  if (tid == 0) prm.n_nodes[q] = nn + 1;
 }
-
 
 int next_pow2(int x) {
   int p = 1;
@@ -748,16 +741,12 @@ int next_pow2(int x) {
 
 size_t tree_smem_bytes(int K, int L, int topk, int B, int *cap_out, int *tsize_out) {
   const int tsize = next_pow2(2 * K * B > 64 ? 2 * K * B : 64);
-  const size_t budget = 232448 - sizeof(Shared) - 2048;
-  int up2 = 32;
-  while (up2 < K * topk) up2 <<= 1;
-  const int warps_used = L < NWARPS ? L : NWARPS;
-  for (int cap = 4096; cap >= 256; cap -= 128) {
-    const Layout y = make_layout(K, L, topk, B, cap, tsize);
+  const size_t budget = 232448 - sizeof(Shared) - 1024;
+  const int need = next_pow2(B) > B + 2 * topk ? next_pow2(B) : B + 2 * topk;
+  for (int pc = 4096; pc >= need; pc -= 32) {
+    const Layout y = make_layout(K, L, topk, B, pc, tsize);
     if (y.total > budget) continue;
-    if (cap < K * B + K * topk) return 0;
-    if ((size_t)warps_used * up2 * 8 > (size_t)cap * 32) return 0;
-    *cap_out = cap;
+    *cap_out = pc;
     *tsize_out = tsize;
     return y.total;
   }
@@ -765,8 +754,8 @@ size_t tree_smem_bytes(int K, int L, int topk, int B, int *cap_out, int *tsize_o
 }
 
 cudaError_t launch_build_tree(const TreeLaunch &T, cudaStream_t stream) {
-  int cap = 0, tsize = 0;
-  const size_t bytes = tree_smem_bytes(T.K, T.L, T.topk, T.B, &cap, &tsize);
+  int pc = 0, tsize = 0;
+  const size_t bytes = tree_smem_bytes(T.K, T.L, T.topk, T.B, &pc, &tsize);
   if (bytes == 0) return cudaErrorInvalidValue;
   Params p;
   p.tk_logp = T.tk_logp;
@@ -786,8 +775,7 @@ cudaError_t launch_build_tree(const TreeLaunch &T, cudaStream_t stream) {
   p.pos = T.pos;
   p.n_nodes = T.n_nodes;
   p.status = T.status;
-  p.union_ws = T.union_ws;
-  p.cap = cap;
+  p.pc = pc;
   p.tsize = tsize;
   cudaError_t e = cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
