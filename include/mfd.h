@@ -111,6 +111,28 @@ int mfd_logits_topk(const float *logits, int R, int V, int topk, float *tk_logp,
                     int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes,
                     mfd_stream_t stream);
 
+/* Log-softmax and top-k of given fp32 logits, like mfd_logits_topk, for
+ * callers that cannot allocate device memory at the point where they call
+ * (for instance code that runs after its memory budget is fixed, or that
+ * must not pay the implicit synchronisation of cudaMalloc): it takes no
+ * workspace.  The paper has no counterpart to this entry point; it is a
+ * library convenience.
+ *
+ * Scratch comes from one array of MFD_NOALLOC_SCRATCH_BYTES bytes that the
+ * library reserves as a static device variable on every GPU that loads it,
+ * for the life of the process.  The scratch needed is
+ * mfd_workspace_size(MFD_OP_LOGITS_TOPK, ...) for the same R, V and topk;
+ * larger problems are rejected with MFD_ERR_WORKSPACE (use mfd_logits_topk).
+ * The first call on a device looks up that array's device address (once per
+ * device); make that first call before any stream capture.  All calls share
+ * the one array and it keeps the last call's contents: calls that may
+ * overlap on the GPU (different streams, or different host threads) race on
+ * it, so serialise them.  Arguments and results are those of
+ * mfd_logits_topk; no allocation is made. */
+#define MFD_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+int mfd_logits_topk_noalloc(const float *logits, int R, int V, int topk, float *tk_logp,
+                            int32_t *tk_tok, float *lse, int32_t *status, mfd_stream_t stream);
+
 /* Mixture DDTree (project page, How it works, step 3, and the Figure 1/2
  * caption): mode k scores a prefix x = (x_1..x_d) by the fp32 left fold,
  * in depth order, of its per-position table log-probabilities; a token not

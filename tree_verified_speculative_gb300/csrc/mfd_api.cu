@@ -141,6 +141,28 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MFD_OK : MFD_ERR_CUDA; }
 
+// Scratch of mfd_logits_topk_noalloc: one static array per device, kept
+// for the life of the process.  Host code cannot use its name as a device
+// address, so its address is looked up once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MFD_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+std::map<int, void *> g_noalloc_ptr;
+
+int noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MFD_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  auto it = g_noalloc_ptr.find(dev);
+  if (it == g_noalloc_ptr.end()) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MFD_ERR_CUDA;
+    it = g_noalloc_ptr.emplace(dev, p).first;
+  }
+  *out = it->second;
+  return MFD_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -247,6 +269,42 @@ int mfd_logits_topk(const float *logits, int R, int V, int topk, float *tk_logp,
   L.part_ms = base;
   L.part_cand = base + y.ms_bytes;
   int rc = cuda_status(mfd::launch_logits_partials(L, s));
+  if (rc != MFD_OK) return rc;
+  mfd::MergeLaunch M;
+  M.part_ms = L.part_ms;
+  M.part_cand = L.part_cand;
+  M.R = R;
+  M.P = y.P;
+  M.T = y.T;
+  M.topk = topk;
+  M.tk_logp = tk_logp;
+  M.tk_tok = tk_tok;
+  M.lse = lse;
+  M.status = status;
+  return cuda_status(mfd::launch_merge_topk(M, s));
+}
+
+int mfd_logits_topk_noalloc(const float *logits, int R, int V, int topk, float *tk_logp, int32_t *tk_tok,
+                            float *lse, int32_t *status, mfd_stream_t stream) {
+  if (!logits || !tk_logp || !tk_tok || !status || R < 1 || V < 1 || topk < 1) return MFD_ERR_INVALID_ARG;
+  if (topk > 32 || V < 16 || topk > V || V >= (1 << 30)) return MFD_ERR_UNSUPPORTED;
+  const TopkLayout y = logits_layout(R, V, topk);
+  if (y.total > MFD_NOALLOC_SCRATCH_BYTES) return MFD_ERR_WORKSPACE;  // too large for the fixed scratch
+  void *scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc != MFD_OK) return rc;
+  char *base = static_cast<char *>(scratch);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mfd::LogitsPartialLaunch L;
+  L.logits = logits;
+  L.R = R;
+  L.V = V;
+  L.T = y.T;
+  L.P = y.P;
+  L.chunk = y.chunk;
+  L.part_ms = base;
+  L.part_cand = base + y.ms_bytes;
+  rc = cuda_status(mfd::launch_logits_partials(L, s));
   if (rc != MFD_OK) return rc;
   mfd::MergeLaunch M;
   M.part_ms = L.part_ms;

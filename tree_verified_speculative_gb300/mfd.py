@@ -31,7 +31,8 @@ MFD_OP_BUILD_TREE = 2
 MFD_OP_VERIFY = 3
 
 EXPORTS = ("mfd_status_string", "mfd_workspace_size", "mfd_lmhead_topk", "mfd_logits_topk",
-           "mfd_build_tree", "mfd_verify")
+           "mfd_logits_topk_noalloc", "mfd_build_tree", "mfd_verify")
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -62,6 +63,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.mfd_lmhead_topk.restype = I
         lib.mfd_logits_topk.argtypes = [P, I, I, I, P, P, P, P, P, SZ, P]
         lib.mfd_logits_topk.restype = I
+        lib.mfd_logits_topk_noalloc.argtypes = [P, I, I, I, P, P, P, P, P]
+        lib.mfd_logits_topk_noalloc.restype = I
         lib.mfd_build_tree.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
         lib.mfd_build_tree.restype = I
         lib.mfd_verify.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P]
@@ -115,6 +118,17 @@ def mfd_logits_topk(logits, topk, tk_logp, tk_tok, lse, status, ws, stream=None)
     rc = load().mfd_logits_topk(_p(logits), R, V, topk, _p(tk_logp), _p(tk_tok), _p(lse), _p(status), _p(ws),
                                 ws.numel() * ws.element_size(), _s(stream))
     _check(rc, "mfd_logits_topk")
+
+
+def mfd_logits_topk_noalloc(logits, topk, tk_logp, tk_tok, lse, status, stream=None) -> None:
+    """mfd_logits_topk without a workspace argument, for callers that cannot
+    allocate device memory where they call it; it uses the library's fixed
+    per-device scratch, so calls must not overlap on the GPU."""
+    R, V = logits.shape
+    assert logits.dtype == torch.float32
+    rc = load().mfd_logits_topk_noalloc(_p(logits), R, V, topk, _p(tk_logp), _p(tk_tok), _p(lse), _p(status),
+                                        _s(stream))
+    _check(rc, "mfd_logits_topk_noalloc")
 
 
 def mfd_build_tree(tk_logp, tk_tok, n_req, K, L, topk, B, anchor_tok, base_pos, parent, token, depth, score,
