@@ -63,3 +63,13 @@ def test_argument_errors_before_any_cuda_call(lib):
     rc = lib.mfd_lmhead_topk(ctypes.c_void_p(0x100004), 4, 64, fake, 1000, 8, fake, fake, None, fake, fake,
                              1 << 20, None)
     assert rc == mfd.MFD_ERR_INVALID_ARG  # h not 16-byte aligned
+
+
+@pytest.mark.parametrize("K,L,topk,B", [(16, 16, 32, 128), (4, 16, 32, 512), (8, 15, 16, 256), (8, 15, 32, 256),
+                                        (1, 16, 32, 512), (16, 1, 1, 1)])
+def test_tree_limits_fit_shared_memory(lib, K, L, topk, B):
+    """Every shape inside the documented limits passes the tree's shared-memory
+    budget check (the call then stops at the deliberately tiny workspace)."""
+    fake = ctypes.c_void_p(0x100000)
+    args = [fake] * 2 + [1, K, L, topk, B] + [fake, None] + [fake] * 9 + [fake, 16, None]
+    assert lib.mfd_build_tree(*args) == mfd.MFD_ERR_WORKSPACE

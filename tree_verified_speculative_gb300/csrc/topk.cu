@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(MERGE_THREADS)
   extern __shared__ int4 merge_smem[];
   __shared__ Cand surv[SURV_CAP];
   __shared__ Cand top[32];
+  __shared__ int2 heads[MERGE_THREADS + 4];
   __shared__ float red[MERGE_THREADS / 32];
   __shared__ Cand tau_s;
   __shared__ int n_surv_s;
@@ -107,15 +108,26 @@ __global__ void __launch_bounds__(MERGE_THREADS)
     lse_s = M + logf(S);
   }
 
-  // ---- tau: rank of this list's head among all heads
+  // ---- tau: rank of this list's head among all heads (heads copied to a
+  // compact array; four independent counters keep the loads in flight)
   const int need = topk < P ? topk : P;
+  if (has) heads[q] = cs[q * T];
+  if (tid < 4) heads[P + tid] = make_int2(__float_as_int(-INFINITY), 0x7FFFFFFF);  // padding: never before
+  __syncthreads();
   if (has) {
     const Cand h = cand_at(q, 0);
-    int r = 0;
-    for (int o = 0; o < P; ++o) {
-      const Cand g = cand_at(o, 0);
-      r += vi_before(g.v, g.i, h.v, h.i) || (g.v == h.v && g.i == h.i && o < q);
+    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+    const int P4 = (P + 3) & ~3;
+    for (int o = 0; o < P4; o += 4) {
+      const int2 g0 = heads[o], g1 = heads[o + 1], g2 = heads[o + 2], g3 = heads[o + 3];
+      r0 += vi_before(__int_as_float(g0.x), g0.y, h.v, h.i) || (__int_as_float(g0.x) == h.v && g0.y == h.i && o < q);
+      r1 += vi_before(__int_as_float(g1.x), g1.y, h.v, h.i) || (__int_as_float(g1.x) == h.v && g1.y == h.i && o + 1 < q);
+      r2 += vi_before(__int_as_float(g2.x), g2.y, h.v, h.i) || (__int_as_float(g2.x) == h.v && g2.y == h.i && o + 2 < q);
+      r3 += vi_before(__int_as_float(g3.x), g3.y, h.v, h.i) || (__int_as_float(g3.x) == h.v && g3.y == h.i && o + 3 < q);
     }
+    // the padding heads equal (-inf, max) and sit after every list, so they
+    // never count for a real head
+    const int r = r0 + r1 + r2 + r3;
     if (r == need - 1 && need == topk) tau_s = h;
   }
   __syncthreads();

@@ -4,32 +4,34 @@
 // tree, which is the union of the per-mode trees at the common cut-off;
 // shared prefixes are built once.
 //
-// One CTA (512 threads) builds one request's tree in shared memory, in two
-// parts.
+// One CTA (512 threads) builds one request's tree in shared memory.
 //
-// Part 1, per mode (warp k = mode k, warp-synchronous only).  Mode k's B best
-// prefixes under its own key (score_k desc, tokens lexicographically asc, a
-// proper prefix first).  Within one mode a prefix is a tuple of ranks, one
-// per position; replacing each rank by its token's rank inside that row
-// (5 bits, token ids compared unsigned) turns the lexicographic token order
-// into plain unsigned comparison of packed 80-bit keys, depth last.  The
-// search is level by level: level t expands the depth-t entries in rank
-// order (child scores only fall) while the child is not after the mode's
-// current B-th best entry (kappa, from a 4-pass radix select on the score
-// plus exact tie resolution on the key).  kappa only improves, so nothing
-// that belongs to the mode's top-B is ever dropped.  If the pool fills,
-// kappa is tightened, the pool pruned, and expansion resumes where each
-// entry stopped.  The mode's top-B is then sorted (warp bitonic sort).
+// Entries.  The pool holds (mode, prefix) entries scored by their own mode.
+// Within one mode a prefix is a tuple of ranks, one per position; replacing
+// each rank by its token's rank inside that row (5 bits, token ids compared
+// unsigned) turns the lexicographic token order into an unsigned compare of
+// packed keys, depth last.  Across modes, prefixes are compared by their
+// token ids (looked up through the rows).
 //
-// Part 2, merge (all warps).  A prefix of the mixture tree is in the top-B
-// list of every mode that attains its score, so the K sorted lists hold the
-// tree.  Each list entry's token sequence is hashed; a hash table keeps, per
-// sequence, the entry with the best (score, smallest mode) -- equality is
-// checked on the full sequence, and a collision reseeds the table.  These
-// "primary" entries are distinct prefixes keyed by (s, tokens).  A primary's
-// node index is 1 + the number of primaries before it, summed over the K
-// lists by binary search; the first B form the tree.  Parents come from the
-// table (hash of the sequence without its last token).
+// Search, level by level.  A per-mode score bound tau_k -- a value with at
+// least B of mode k's entries scoring no worse -- comes from a two-digit
+// radix select on the score key.  Each mode's entries are distinct
+// prefixes and a prefix's mixture score is at least its mode score, so at
+// least B distinct prefixes score no worse than min_k tau_k: the tree's
+// cut-off is never worse, and every entry that can reach the tree, or lead
+// to it, scores within the bound.  Level t expands the depth-t entries in
+// rank order (child scores only fall) while the child is within the bound.
+// When the pool fills, it is pruned to each mode's exact B best (radix
+// select on the full score key, then the token order among equal scores)
+// and expansion resumes where each entry stopped.
+//
+// Result.  The entries within the final bound are hashed by token sequence;
+// a table keeps per sequence the entry with the best (score, smallest mode),
+// equality checked on the full sequence (a collision reseeds the table).
+// These primaries are distinct prefixes.  A radix bound over the primaries
+// leaves about B of them; rank counting among those gives both the B best
+// and their order.  Parents are looked up in the table by the hash of the
+// sequence without its last token.
 #include "lmhead.h"
 #include "mfd_device.cuh"
 
@@ -38,11 +40,13 @@ namespace {
 
 constexpr int THREADS = 512;
 constexpr int NWARPS = THREADS / 32;
-constexpr int MAX_PASSES = 1024;
+constexpr int MAX_PASSES = 64;
+constexpr int PLIST = 1024;     // parents listed for pair-parallel expansion
+constexpr int PAIR_MAX = 4096;  // (parent, rank) pairs expanded at once
 
-// Pool entry of one mode (16 bytes).  k0: row ranks of positions 1..12,
-// 5 bits each, position 1 highest (bits 59..55).  k1: positions 13..16 at
-// bits 24..5, depth at bits 4..0, next child rank at bits 31..26.
+// Pool entry (16 bytes).  k0: row ranks of positions 1..12, 5 bits each,
+// position 1 highest (bits 59..55).  k1: depth at bits 4..0, positions
+// 13..16 at bits 24..5, mode at bits 28..25.
 struct PE {
   float score;
   uint32_t k1;
@@ -50,7 +54,7 @@ struct PE {
 };
 static_assert(sizeof(PE) == 16, "pool entry");
 
-constexpr uint32_t K1_KEY = 0x01FFFFFFu;
+constexpr uint32_t K1_KEY = 0x01FFFFFFu;  // depth and positions 13..16
 
 __device__ __forceinline__ void pk_set(uint64_t &k0, uint32_t &k1, int p, uint32_t s) {
   if (p <= 12) {
@@ -65,19 +69,7 @@ __device__ __forceinline__ uint32_t pk_get(uint64_t k0, uint32_t k1, int p) {
   return p <= 12 ? (uint32_t)(k0 >> (55 - 5 * (p - 1))) & 31u : (k1 >> (20 - 5 * (p - 13))) & 31u;
 }
 __device__ __forceinline__ int pk_depth(uint32_t k1) { return (int)(k1 & 31u); }
-__device__ __forceinline__ int pk_next(uint32_t k1) { return (int)(k1 >> 26); }
-
-struct MK {  // key within one mode
-  uint32_t sk;
-  uint64_t k0;
-  uint32_t k1;
-};
-__device__ __forceinline__ MK mk_of(const PE &e) { return MK{desc_key(e.score), e.k0, e.k1 & K1_KEY}; }
-__device__ __forceinline__ bool mk_before(const MK &a, const MK &b) {
-  if (a.sk != b.sk) return a.sk < b.sk;
-  if (a.k0 != b.k0) return a.k0 < b.k0;
-  return a.k1 < b.k1;
-}
+__device__ __forceinline__ int pk_mode(uint32_t k1) { return (int)((k1 >> 25) & 15u); }
 
 __device__ __forceinline__ uint64_t mix64(uint64_t x) {
   x ^= x >> 30;
@@ -110,6 +102,17 @@ __device__ __forceinline__ void warp_hist_add(int *hist, int bin) {
   if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(m) - 1) atomicAdd(&hist[bin], __popc(m));
 }
 
+// Warp-aggregated append: one atomic per warp; this lane's index or -1.
+__device__ __forceinline__ int warp_append(int *ctr, bool pred) {
+  const unsigned m = __ballot_sync(0xffffffffu, pred);
+  if (m == 0) return -1;
+  const int leader = __ffs(m) - 1;
+  int base = 0;
+  if ((int)(threadIdx.x & 31) == leader) base = atomicAdd(ctr, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return pred ? base + __popc(m & lanemask_lt()) : -1;
+}
+
 struct Params {
   const float *tk_logp;
   const int32_t *tk_tok;
@@ -120,295 +123,196 @@ struct Params {
   int32_t *mode;
   uint32_t *mask;
   int32_t *pos, *n_nodes, *status;
-  int pc;     // pool capacity per mode
+  int cap;    // pool entries
+  int nc;     // candidates hashed at the end
   int tsize;  // hash table slots (power of two)
 };
 
 struct Layout {
-  size_t lp, tok, sig, inv, pool, hv, hp, hslot, pcnt, nodeid, prim, table, par, nslot, total;
+  size_t lp, tok, sig, inv, ent, nxt, flg, table, hist1, skk, sel, prim, hslot, nodeid, par, nslot, plist, total;
 };
 
 __host__ __device__ inline size_t al16(size_t o) { return (o + 15) & ~(size_t)15; }
 
-__host__ __device__ inline Layout make_layout(int K, int L, int topk, int B, int pc, int tsize) {
+__host__ __device__ inline Layout make_layout(int K, int L, int topk, int B, int cap, int nc, int tsize) {
   Layout y;
   size_t o = 0;
-  const size_t klt = (size_t)K * L * topk, ne = (size_t)K * B;
-  const size_t hist = (size_t)NWARPS * 256 * 4, tbl = al16((size_t)tsize * 4) + (size_t)tsize * 8;
-  y.pool = o;
-  o += (size_t)K * pc * 16;
-  y.hv = o = al16(o);
-  o += ne * 8;
-  y.hp = o = al16(o);
-  o += ne * 8;
-  y.table = o = al16(o);  // hash tags (u32) then best (u64); the per-warp histograms overlay it
+  const size_t klt = (size_t)K * L * topk;
+  const size_t hist = (size_t)16 * 256 * 4, tbl = al16((size_t)tsize * 4) + (size_t)tsize * 8;
+  y.ent = o;
+  o += (size_t)cap * 16;
+  y.table = o = al16(o);  // hash tags then best entries; the radix histograms overlay it
   o += hist > tbl ? hist : tbl;
+  y.hist1 = o = al16(o);
+  o += 256 * 4;
   y.lp = o = al16(o);
   o += klt * 4;
   y.tok = o = al16(o);
   o += klt * 4;
+  y.skk = o = al16(o);
+  o += (size_t)(nc + 4) * 4;  // padded to whole 16-byte words
+  y.sel = o = al16(o);
+  o += (size_t)nc * 2;
   y.hslot = o = al16(o);
-  o += ne * 2;
-  y.pcnt = o = al16(o);
-  o += ne * 2;
+  o += (size_t)nc * 2;
   y.nodeid = o = al16(o);
-  o += ne * 2;
+  o += (size_t)nc * 2;
   y.par = o = al16(o);
   o += (size_t)(B + 1) * 2;
+  y.plist = o = al16(o);
+  o += (size_t)PLIST * 2;
   y.nslot = o = al16(o);
   o += (size_t)(B + 1) * 2;
+  y.nxt = o = al16(o);
+  o += (size_t)cap;
+  y.flg = o = al16(o);
+  o += (size_t)cap;
   y.sig = o = al16(o);
   o += klt;
   y.inv = o = al16(o);
   o += klt;
   y.prim = o = al16(o);
-  o += ne;
+  o += (size_t)nc;
   y.total = (o + 127) & ~(size_t)127;
   return y;
 }
 
 struct Shared {
-  int bad, coll, total_prim;
-  int cnt[16], off[17];
+  int n_ent, overflow, any, bad, coll, n_prim, n_sel, has_tau, n_par, wsum[NWARPS];
+  int cnt[16], act[16], rem[16], ntie[16];
+  uint32_t pre[16], tau;
 };
 
 struct Ctx {
   const float *lp;
   const int32_t *tok;
   const uint8_t *sig, *inv;
-  int K, L, topk, B, pc;
+  int K, L, topk;
 };
 
-// token at position p (1-based) of a mode-k key
-__device__ __forceinline__ uint32_t token_at(const Ctx &c, int k, uint64_t k0, uint32_t k1, int p) {
-  const int row = (k * c.L + p - 1) * c.topk;
-  return (uint32_t)c.tok[row + c.inv[row + pk_get(k0, k1, p)]];
+// token at position p (1-based) of an entry
+__device__ __forceinline__ uint32_t token_at(const Ctx &c, const PE &e, int p) {
+  const int row = (pk_mode(e.k1) * c.L + p - 1) * c.topk;
+  return (uint32_t)c.tok[row + c.inv[row + pk_get(e.k0, e.k1, p)]];
 }
 
-// Lexicographic order of two prefixes of possibly different modes, by token
-// ids (unsigned), a proper prefix first: <0, 0, >0.
-__device__ int seq_cmp(const Ctx &c, int ka, const PE &a, int kb, const PE &b) {
+// Token order of two prefixes of any modes (unsigned ids, a proper prefix
+// first): <0, 0, >0.
+__device__ int seq_cmp(const Ctx &c, const PE &a, const PE &b) {
   const int da = pk_depth(a.k1), db = pk_depth(b.k1);
   const int d = da < db ? da : db;
   for (int p = 1; p <= d; ++p) {
-    const uint32_t ta = token_at(c, ka, a.k0, a.k1, p), tb = token_at(c, kb, b.k0, b.k1, p);
+    const uint32_t ta = token_at(c, a, p), tb = token_at(c, b, p);
     if (ta != tb) return ta < tb ? -1 : 1;
   }
   return da - db;
 }
 
-// (s desc, tokens asc) across modes: true iff a is strictly before b.
-__device__ __forceinline__ bool x_before(const Ctx &c, int ka, const PE &a, int kb, const PE &b) {
-  const uint32_t sa = desc_key(a.score), sb = desc_key(b.score);
-  if (sa != sb) return sa < sb;
-  return seq_cmp(c, ka, a, kb, b) < 0;
+__device__ __forceinline__ uint64_t seq_hash(const Ctx &c, const PE &e, int d, uint64_t seed) {
+  uint64_t h = 0x2545F4914F6CDD1Dull ^ seed;
+  for (int p = 1; p <= d; ++p) h = mix64(h ^ ((uint64_t)token_at(c, e, p) + ((uint64_t)p << 40)));
+  return h;
 }
 
-// ---------------------------------------------------------------- part 1
-// The B-th best entry of P[0, n) (warp-wide).  Returns false when n < B.
-__device__ bool warp_kth(const PE *P, int n, int B, int *hist, MK &kap) {
-  const int lane = threadIdx.x & 31;
-  if (n < B) return false;
-  uint32_t pre = 0;
-  int rem = B, ntie = 0;
-  for (int pass = 0; pass < 4; ++pass) {
+// Per group g (grp(i) in [0, G), or -1 to skip), with at least B members
+// among ent[0, n): digits of the B-th best score key, most significant
+// first, over `passes` 8-bit passes.  Leaves sh.act[g], sh.pre[g] (the digits
+// found, low bits zero), sh.rem[g] (rank of the B-th within that prefix) and
+// sh.ntie[g] (members sharing the prefix).
+template <typename GroupFn>
+__device__ void radix_bound(Shared &sh, const PE *ent, int n, int G, int B, int passes, int *hist, GroupFn grp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < 16) {
+    sh.pre[tid] = 0;
+    sh.rem[tid] = B;
+    sh.ntie[tid] = 0;
+    sh.act[tid] = tid < G;  // until the first pass has counted the group
+  }
+  for (int i = tid; i < G * 256; i += THREADS) hist[i] = 0;
+  __syncthreads();
+  for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int b = lane; b < 256; b += 32) hist[b] = 0;
-    __syncwarp();
-    for (int base = 0; base < n; base += 32) {
+    if (pass > 0) {
+      for (int i = tid; i < G * 256; i += THREADS) hist[i] = 0;
+      __syncthreads();
+    }
+    for (int base = warp * 32; base < n; base += THREADS) {
       const int i = base + lane;
       int bin = -1;
       if (i < n) {
-        const uint32_t sk = desc_key(P[i].score);
-        if (pass == 0 || (sk >> (shift + 8)) == (pre >> (shift + 8))) bin = (int)((sk >> shift) & 255u);
+        const int g = grp(i);
+        if (g >= 0 && sh.act[g]) {
+          const uint32_t sk = desc_key(ent[i].score);
+          if (pass == 0 || (sk >> (shift + 8)) == (sh.pre[g] >> (shift + 8))) bin = g * 256 + (int)((sk >> shift) & 255u);
+        }
       }
       warp_hist_add(hist, bin);
     }
-    __syncwarp();
-    int c[8], sum = 0;
+    __syncthreads();
+    for (int g = warp; g < G; g += NWARPS) {
+      if (!sh.act[g]) continue;
+      int c[8], sum = 0;
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      c[b] = hist[lane * 8 + b];
-      sum += c[b];
-    }
-    int run = warp_excl_scan(sum, lane);
-    int fb = -1, fbefore = 0, fcnt = 0;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      if (fb < 0 && run < rem && rem <= run + c[b]) {
-        fb = lane * 8 + b;
-        fbefore = run;
-        fcnt = c[b];
+      for (int b = 0; b < 8; ++b) {
+        c[b] = hist[g * 256 + lane * 8 + b];
+        sum += c[b];
       }
-      run += c[b];
-    }
-    const unsigned who = __ballot_sync(0xffffffffu, fb >= 0);
-    const int src = __ffs(who) - 1;
-    fb = __shfl_sync(0xffffffffu, fb, src);
-    fbefore = __shfl_sync(0xffffffffu, fbefore, src);
-    fcnt = __shfl_sync(0xffffffffu, fcnt, src);
-    pre |= (uint32_t)fb << shift;
-    rem -= fbefore;
-    ntie = fcnt;
-    __syncwarp();
-  }
-  // the rem-th smallest key among the entries whose score key is pre
-  uint64_t b0 = 0;
-  uint32_t b1 = 0;
-  bool found = false;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    bool hit = false;
-    if (i < n && desc_key(P[i].score) == pre) {
-      if (ntie == 1) {
-        hit = true;
-      } else {
-        const uint64_t e0 = P[i].k0;
-        const uint32_t e1 = P[i].k1 & K1_KEY;
-        int r = 1;
-        for (int f = 0; f < n; ++f) {
-          if (desc_key(P[f].score) != pre) continue;
-          const uint64_t f0 = P[f].k0;
-          const uint32_t f1 = P[f].k1 & K1_KEY;
-          r += (f0 < e0) || (f0 == e0 && f1 < e1);
+      int run = warp_excl_scan(sum, lane);
+      if (pass == 0) {
+        const int total = __shfl_sync(0xffffffffu, run + sum, 31);
+        if (total < B) {
+          if (lane == 0) sh.act[g] = 0;
+          continue;
         }
-        hit = (r == rem);
+      }
+      const int rem = sh.rem[g];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        if (run < rem && rem <= run + c[b]) {
+          sh.pre[g] |= (uint32_t)(lane * 8 + b) << shift;
+          sh.rem[g] = rem - run;
+          sh.ntie[g] = c[b];
+        }
+        run += c[b];
       }
     }
-    const unsigned m = __ballot_sync(0xffffffffu, hit);
-    if (m) {
-      const int isrc = base + __ffs(m) - 1;
-      b0 = P[isrc].k0;
-      b1 = P[isrc].k1 & K1_KEY;
-      found = true;
-      break;
-    }
+    __syncthreads();
   }
-  kap = MK{pre, b0, b1};
-  return found;
 }
 
-// Keep the entries not after kap; in place, order preserved.  Returns n.
-__device__ int warp_prune(PE *P, int n, const MK &kap) {
-  const int lane = threadIdx.x & 31;
+// In-place stable compaction of ent/nxt[0, n) to the entries with keep(i).
+template <typename KeepFn>
+__device__ int block_compact(Shared &sh, PE *ent, uint8_t *nxt, int n, KeepFn keep) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int out = 0;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
+  for (int base = 0; base < n; base += THREADS) {
+    const int i = base + tid;
     PE e;
-    bool keep = false;
+    uint8_t nx = 0;
+    bool kp = false;
     if (i < n) {
-      e = P[i];
-      keep = !mk_before(kap, mk_of(e));
+      e = ent[i];
+      nx = nxt[i];
+      kp = keep(i);
     }
-    const unsigned m = __ballot_sync(0xffffffffu, keep);
-    __syncwarp();
-    if (keep) P[out + __popc(m & lanemask_lt())] = e;
-    out += __popc(m);
-    __syncwarp();
+    const unsigned m = __ballot_sync(0xffffffffu, kp);
+    if (lane == 0) sh.wsum[warp] = __popc(m);
+    __syncthreads();
+    int woff = 0, tot = 0;
+    for (int w = 0; w < NWARPS; ++w) {
+      const int v = sh.wsum[w];
+      woff += w < warp ? v : 0;
+      tot += v;
+    }
+    if (kp) {
+      const int d = out + woff + __popc(m & lanemask_lt());
+      ent[d] = e;
+      nxt[d] = nx;
+    }
+    out += tot;
+    __syncthreads();
   }
   return out;
-}
-
-// Expand the depth-t entries of P[0, n) in rank order (children appended
-// after n).  Returns true when the pool filled before every child that can
-// still make the cut was appended.
-__device__ bool warp_expand(const Ctx &c, int k, int t, PE *P, int &n, bool hk, const MK &kap, bool &any) {
-  const int lane = threadIdx.x & 31;
-  const int n0 = n;
-  const int row = (k * c.L + t) * c.topk;  // depth t+1 uses row index t
-  bool overflow = false;
-  for (int base = 0; base < n0 && !overflow; base += 32) {
-    const int i = base + lane;
-    PE par;
-    bool isp = false, act = false;
-    int j = 0;
-    if (i < n0) {
-      par = P[i];
-      isp = pk_depth(par.k1) == t;
-      j = pk_next(par.k1);
-      act = isp && j < c.topk;
-    }
-    while (__any_sync(0xffffffffu, act)) {
-      bool want = false;
-      PE ch;
-      if (act) {
-        const float lv = c.lp[row + j];
-        if (!(lv > -INFINITY)) {
-          act = false;
-          j = c.topk;
-        } else {
-          ch.score = __fadd_rn(par.score, lv);
-          ch.k0 = par.k0;
-          ch.k1 = par.k1 & ~(31u | (63u << 26));
-          pk_set(ch.k0, ch.k1, t + 1, c.sig[row + j]);
-          ch.k1 |= (uint32_t)(t + 1);
-          if (!hk) {
-            want = true;
-          } else {
-            const MK ck = mk_of(ch);
-            if (ck.sk > kap.sk) {
-              act = false;  // every later rank scores no better
-              j = c.topk;
-            } else if (mk_before(kap, ck)) {
-              ++j;  // same score, after kappa in token order; a later rank may not be
-              if (j >= c.topk) act = false;
-            } else {
-              want = true;
-            }
-          }
-        }
-      }
-      const unsigned m = __ballot_sync(0xffffffffu, want);
-      const int cnt = __popc(m);
-      const int room = c.pc - n;
-      const int r = __popc(m & lanemask_lt());
-      if (want) {
-        if (r < room) {
-          P[n + r] = ch;
-          ++j;
-          if (j >= c.topk) act = false;
-        } else {
-          act = false;  // j kept: resumed in the next pass
-          overflow = true;
-        }
-      }
-      n += cnt < room ? cnt : room;
-      if (cnt) any = true;
-      overflow = __any_sync(0xffffffffu, overflow);
-      if (overflow) act = false;
-    }
-    if (isp) P[i].k1 = (P[i].k1 & ~(63u << 26)) | ((uint32_t)j << 26);
-    __syncwarp();
-  }
-  return overflow;
-}
-
-// Sort P[0, n) ascending by key (warp bitonic sort; P has room for the next
-// power of two of n).  The padding sorts last.
-__device__ void warp_sort(PE *P, int n) {
-  const int lane = threadIdx.x & 31;
-  int np2 = 1;
-  while (np2 < n) np2 <<= 1;
-  for (int i = n + lane; i < np2; i += 32) {
-    P[i].score = -INFINITY;
-    P[i].k0 = ~0ull;
-    P[i].k1 = K1_KEY;
-  }
-  __syncwarp();
-  for (int size = 2; size <= np2; size <<= 1)
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const int ls = __ffs(stride) - 1;
-      for (int e = lane; e < np2 / 2; e += 32) {
-        const int lo = ((e >> ls) << (ls + 1)) | (e & (stride - 1)), hi = lo + stride;
-        const bool asc = (lo & size) == 0;
-        const PE a = P[lo], b = P[hi];
-        if (mk_before(mk_of(b), mk_of(a)) == asc) {
-          P[lo] = b;
-          P[hi] = a;
-        }
-      }
-      __syncwarp();
-    }
 }
 
 __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm) {
@@ -416,31 +320,39 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   __shared__ Shared sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = blockIdx.x;
-  const int K = prm.K, L = prm.L, topk = prm.topk, B = prm.B, PC = prm.pc, tsize = prm.tsize;
+  const int K = prm.K, L = prm.L, topk = prm.topk, B = prm.B, CAP = prm.cap, NC = prm.nc, tsize = prm.tsize;
   const int KLT = K * L * topk;
-  const Layout lay = make_layout(K, L, topk, B, PC, tsize);
+  const Layout lay = make_layout(K, L, topk, B, CAP, NC, tsize);
   float *lp_s = reinterpret_cast<float *>(smem + lay.lp);
   int32_t *tok_s = reinterpret_cast<int32_t *>(smem + lay.tok);
   uint8_t *sig_s = smem + lay.sig;
   uint8_t *inv_s = smem + lay.inv;
-  PE *pools = reinterpret_cast<PE *>(smem + lay.pool);
-  uint64_t *hv = reinterpret_cast<uint64_t *>(smem + lay.hv);
-  uint64_t *hp = reinterpret_cast<uint64_t *>(smem + lay.hp);
+  PE *ent = reinterpret_cast<PE *>(smem + lay.ent);
+  uint8_t *nxt = smem + lay.nxt;
+  uint8_t *flg = smem + lay.flg;
+  int *hist1 = reinterpret_cast<int *>(smem + lay.hist1);
   uint32_t *tag = reinterpret_cast<uint32_t *>(smem + lay.table);
   uint64_t *best = reinterpret_cast<uint64_t *>(smem + lay.table + al16((size_t)tsize * 4));
-  int *hists = reinterpret_cast<int *>(smem + lay.table);
+  int *hist = reinterpret_cast<int *>(smem + lay.table);
+  uint32_t *skk = reinterpret_cast<uint32_t *>(smem + lay.skk);
+  uint16_t *sel = reinterpret_cast<uint16_t *>(smem + lay.sel);
   uint16_t *hslot = reinterpret_cast<uint16_t *>(smem + lay.hslot);
-  uint16_t *pcnt = reinterpret_cast<uint16_t *>(smem + lay.pcnt);
   int16_t *nodeid = reinterpret_cast<int16_t *>(smem + lay.nodeid);
   uint8_t *prim = smem + lay.prim;
   int16_t *par_s = reinterpret_cast<int16_t *>(smem + lay.par);
   uint16_t *nslot = reinterpret_cast<uint16_t *>(smem + lay.nslot);
+  uint16_t *plist = reinterpret_cast<uint16_t *>(smem + lay.plist);
 
   const float *glp = prm.tk_logp + (size_t)q * KLT;
   const int32_t *gtk = prm.tk_tok + (size_t)q * KLT;
+  pdl_wait();  // the tables may come from the grid launched just before
+  pdl_launch_dependents();
 
   // ---------------------------------------------------- tables and checks
-  if (tid == 0) sh.bad = 0;
+  if (tid == 0) {
+    sh.bad = 0;
+    sh.n_ent = 0;
+  }
   __syncthreads();
   for (int e = tid; e < KLT; e += THREADS) {
     const float v = glp[e];
@@ -468,87 +380,228 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     if (tid == 0) report(prm.status, MFD_ERR_INPUT);
     return;
   }
+  const Ctx c{lp_s, tok_s, sig_s, inv_s, K, L, topk};
+  auto mode_of = [&](int i) { return pk_mode(ent[i].k1); };
 
-  // ---------------------------------------------------- part 1: per mode
-  const Ctx c{lp_s, tok_s, sig_s, inv_s, K, L, topk, B, PC};
-  if (warp < K) {
-    const int k = warp;
-    PE *P = pools + (size_t)k * PC;
-    int *hist = hists + warp * 256;
-    int n = 0;
-    for (int base = 0; base < topk; base += 32) {  // depth-1 entries
-      const int j = base + lane;
-      const int e = (k * L) * topk + j;
-      const bool ok = j < topk && lp_s[e] > -INFINITY;
-      const unsigned m = __ballot_sync(0xffffffffu, ok);
-      if (ok) {
-        PE en;
-        en.score = lp_s[e];
-        en.k0 = 0;
-        en.k1 = 1u;
-        pk_set(en.k0, en.k1, 1, sig_s[e]);
-        P[n + __popc(m & lanemask_lt())] = en;
-      }
-      n += __popc(m);
+  // ---------------------------------------------------- depth-1 entries
+  for (int base = warp * 32; base < K * topk; base += THREADS) {
+    const int e = base + lane;
+    const int k = e / topk, j = e - (e / topk) * topk;
+    const bool ok = e < K * topk && lp_s[(k * L) * topk + j] > -INFINITY;
+    const int slot = warp_append(&sh.n_ent, ok);
+    if (ok) {
+      PE en;
+      en.score = lp_s[(k * L) * topk + j];
+      en.k0 = 0;
+      en.k1 = 1u | ((uint32_t)k << 25);
+      pk_set(en.k0, en.k1, 1, sig_s[(k * L) * topk + j]);
+      ent[slot] = en;
+      nxt[slot] = 0;
     }
-    __syncwarp();
-    bool failed = false;
-    for (int t = 1; t < L && !failed; ++t) {
-      bool any = false;
-      int pass = 0;
-      for (; pass < MAX_PASSES; ++pass) {
-        MK kap{0, 0, 0};
-        const bool hk = warp_kth(P, n, B, hist, kap);
-        if (hk) n = warp_prune(P, n, kap);
-        if (!warp_expand(c, k, t, P, n, hk, kap, any)) break;
-      }
-      if (pass == MAX_PASSES) failed = true;
-      if (!any) break;
-    }
-    if (!failed) {
-      MK kap{0, 0, 0};
-      if (warp_kth(P, n, B, hist, kap)) n = warp_prune(P, n, kap);
-      if (n > B) failed = true;  // the B-th entry was not found: impossible for valid tables
-    }
-    if (failed) {
-      if (lane == 0) report(prm.status, MFD_ERR_UNSUPPORTED);
-      n = 0;
-    }
-    warp_sort(P, n);
-    if (lane == 0) sh.cnt[k] = n;
   }
   __syncthreads();
 
-  // ---------------------------------------------------- part 2: merge
-  if (tid == 0) {
-    int o = 0;
-    for (int k = 0; k < K; ++k) {
-      sh.off[k] = o;
-      o += sh.cnt[k];
+  // the best (smallest) per-mode bound into sh.tau / sh.has_tau
+  auto set_tau = [&](int passes) {
+    radix_bound(sh, ent, sh.n_ent, K, B, passes, hist, mode_of);
+    if (tid == 0) {
+      uint32_t t = 0xFFFFFFFFu;
+      int h = 0;
+      for (int k = 0; k < K; ++k)
+        if (sh.act[k]) {
+          const uint32_t tk = sh.pre[k] | (passes >= 4 ? 0u : (0xFFFFFFFFu >> (8 * passes)));
+          if (!h || tk < t) t = tk;
+          h = 1;
+        }
+      sh.tau = t;
+      sh.has_tau = h;
     }
-    sh.off[K] = o;
-  }
-  __syncthreads();
-  const int NE = sh.off[K];
-  auto entry_of = [&](int id, int &k, int &i) {
-    k = 0;
-    while (id >= sh.off[k + 1]) ++k;
-    i = id - sh.off[k];
+    __syncthreads();
   };
-  // hashes of each entry's token sequence and of its parent prefix
-  for (int id = tid; id < NE; id += THREADS) {
-    int k, i;
-    entry_of(id, k, i);
-    const PE e = pools[(size_t)k * PC + i];
-    const int d = pk_depth(e.k1);
-    uint64_t h = 0x2545F4914F6CDD1Dull, hpar = h;
-    for (int p = 1; p <= d; ++p) {
-      hpar = h;
-      h = mix64(h ^ ((uint64_t)token_at(c, k, e.k0, e.k1, p) + ((uint64_t)p << 40)));
+
+  // prune to each mode's exact B best (only when the pool is full)
+  auto prune_exact = [&]() {
+    radix_bound(sh, ent, sh.n_ent, K, B, 4, hist, mode_of);
+    const int n = sh.n_ent;
+    // among a mode's entries tied at its B-th score, keep the first rem[k]
+    // in token order; decided for every entry before any entry moves
+    for (int i = tid; i < n; i += THREADS) {
+      const PE e = ent[i];
+      const int k = pk_mode(e.k1);
+      bool kp = true;
+      if (sh.act[k]) {
+        const uint32_t sk = desc_key(e.score);
+        if (sk != sh.pre[k]) {
+          kp = sk < sh.pre[k];
+        } else if (sh.ntie[k] != sh.rem[k]) {
+          int r = 1;
+          for (int f = 0; f < n; ++f) {
+            const PE g = ent[f];
+            if (pk_mode(g.k1) != k || desc_key(g.score) != sh.pre[k]) continue;
+            r += (g.k0 < e.k0) || (g.k0 == e.k0 && (g.k1 & K1_KEY) < (e.k1 & K1_KEY));
+          }
+          kp = r <= sh.rem[k];
+        }
+      }
+      flg[i] = kp;
     }
-    hv[id] = h;
-    hp[id] = hpar;
+    __syncthreads();
+    const int out = block_compact(sh, ent, nxt, n, [&](int i) { return flg[i] != 0; });
+    if (tid == 0) sh.n_ent = out;
+    __syncthreads();
+  };
+
+  // ---------------------------------------------------- level expansion
+  bool failed = false, tau_current = false;
+  for (int t = 1; t < L && !failed; ++t) {
+    if (tid == 0) sh.any = 0;
+    int pass = 0;
+    for (; pass < MAX_PASSES; ++pass) {
+      if (t == 1 && pass == 0 && topk < B) {
+        if (tid == 0) sh.has_tau = 0;  // each mode holds only its topk depth-1 entries
+      } else {
+        set_tau(2);
+      }
+      tau_current = true;
+      if (tid == 0) {
+        sh.overflow = 0;
+        sh.n_par = 0;
+      }
+      __syncthreads();
+      const int n0 = sh.n_ent;
+      const bool ht = sh.has_tau;
+      const uint32_t tau = sh.tau;
+      // the parents of this level that can still reach the bound
+      for (int base = warp * 32; base < n0; base += THREADS) {
+        const int i = base + lane;
+        bool isp = false;
+        if (i < n0) {
+          const PE e = ent[i];
+          isp = pk_depth(e.k1) == t && nxt[i] < topk && (!ht || desc_key(e.score) <= tau);
+        }
+        const int k = warp_append(&sh.n_par, isp);
+        if (isp && k < PLIST) plist[k] = (uint16_t)i;
+      }
+      __syncthreads();
+      const int np = sh.n_par;
+      if (np <= PLIST && np * topk <= PAIR_MAX && n0 + np * topk <= CAP) {
+        // few parents and room for every child: all (parent, rank) pairs at once
+        for (int base = warp * 32; base < np * topk; base += THREADS) {
+          const int x = base + lane;
+          bool want = false;
+          PE ch;
+          if (x < np * topk) {
+            const int i = plist[x / topk], j = x - (x / topk) * topk;
+            const PE par = ent[i];
+            const int row = (pk_mode(par.k1) * L + t) * topk;
+            const float lv = lp_s[row + j];
+            if (j >= nxt[i] && lv > -INFINITY) {
+              ch.score = __fadd_rn(par.score, lv);
+              if (!ht || desc_key(ch.score) <= tau) {
+                ch.k0 = par.k0;
+                ch.k1 = par.k1 & ~31u;
+                pk_set(ch.k0, ch.k1, t + 1, sig_s[row + j]);
+                ch.k1 |= (uint32_t)(t + 1);
+                want = true;
+              }
+            }
+          }
+          const int slot = warp_append(&sh.n_ent, want);
+          if (want) {
+            ent[slot] = ch;
+            nxt[slot] = 0;
+          }
+        }
+        __syncthreads();
+        for (int pi = tid; pi < np; pi += THREADS) nxt[plist[pi]] = (uint8_t)topk;
+      } else {
+        for (int base = warp * 32; base < n0; base += THREADS) {
+          const int i = base + lane;
+          PE par{0.f, 0u, 0ull};
+          bool isp = false, act = false;
+          int j = 0;
+          if (i < n0) {
+            par = ent[i];
+            j = nxt[i];
+            isp = pk_depth(par.k1) == t && j < topk && (!ht || desc_key(par.score) <= tau);
+            act = isp;
+          }
+          const int row = (pk_mode(par.k1) * L + t) * topk;
+          while (__any_sync(0xffffffffu, act)) {
+            bool want = false;
+            PE ch;
+            if (act) {
+              const float lv = lp_s[row + j];
+              if (!(lv > -INFINITY)) {
+                act = false;
+                j = topk;
+              } else {
+                ch.score = __fadd_rn(par.score, lv);
+                if (ht && desc_key(ch.score) > tau) {
+                  act = false;  // every later rank scores no better
+                  j = topk;
+                } else {
+                  ch.k0 = par.k0;
+                  ch.k1 = par.k1 & ~31u;
+                  pk_set(ch.k0, ch.k1, t + 1, sig_s[row + j]);
+                  ch.k1 |= (uint32_t)(t + 1);
+                  want = true;
+                }
+              }
+            }
+            const int slot = warp_append(&sh.n_ent, want);
+            if (want) {
+              if (slot < CAP) {
+                ent[slot] = ch;
+                nxt[slot] = 0;
+                ++j;
+                if (j >= topk) act = false;
+              } else {
+                act = false;  // j kept: resumed after the pool is pruned
+                sh.overflow = 1;
+              }
+            }
+          }
+          if (isp) nxt[i] = (uint8_t)j;
+        }
+      }
+      __syncthreads();
+      if (tid == 0) {
+        if (sh.n_ent > CAP) sh.n_ent = CAP;
+        if (sh.n_ent > n0) sh.any = 1;
+      }
+      __syncthreads();
+      if (sh.any) tau_current = false;
+      if (!sh.overflow) break;
+      prune_exact();
+    }
+    if (pass == MAX_PASSES) failed = true;
+    if (!sh.any) break;
   }
+  if (failed) {
+    if (tid == 0) report(prm.status, MFD_ERR_UNSUPPORTED);
+    return;
+  }
+
+  // ---------------------------------------------------- candidates
+  if (!tau_current) set_tau(2);  // else: nothing was added since the last bound
+  {
+    const bool ht = sh.has_tau;
+    const uint32_t tau = sh.tau;
+    const int n = block_compact(sh, ent, nxt, sh.n_ent, [&](int i) { return !ht || desc_key(ent[i].score) <= tau; });
+    if (tid == 0) sh.n_ent = n;
+    __syncthreads();
+  }
+  if (sh.n_ent > NC) {  // many ties within the bound: keep each mode's exact B best
+    prune_exact();
+    if (sh.n_ent > NC) {
+      if (tid == 0) report(prm.status, MFD_ERR_UNSUPPORTED);
+      return;
+    }
+  }
+  const int n = sh.n_ent;
+
+  // ---------------------------------------------------- one entry per prefix
   uint64_t seed = 0;
   for (int attempt = 0; attempt < 4; ++attempt) {
     for (int s = tid; s < tsize; s += THREADS) {
@@ -557,8 +610,8 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     }
     if (tid == 0) sh.coll = 0;
     __syncthreads();
-    for (int id = tid; id < NE; id += THREADS) {
-      const uint64_t h = mix64(hv[id] ^ seed);
+    for (int i = tid; i < n; i += THREADS) {
+      const uint64_t h = seq_hash(c, ent[i], pk_depth(ent[i].k1), seed);
       const uint32_t tg = (uint32_t)(h >> 32) | 1u;
       uint32_t s = (uint32_t)h & (uint32_t)(tsize - 1);
       for (int probe = 0; probe < tsize; ++probe) {
@@ -566,24 +619,14 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         if (prev == 0u || prev == tg) break;
         s = (s + 1) & (uint32_t)(tsize - 1);
       }
-      hslot[id] = (uint16_t)s;
+      hslot[i] = (uint16_t)s;
+      const uint64_t packed = ((uint64_t)desc_key(ent[i].score) << 32) | ((uint64_t)pk_mode(ent[i].k1) << 16) | i;
+      atomicMin(reinterpret_cast<unsigned long long *>(&best[s]), (unsigned long long)packed);
     }
     __syncthreads();
-    for (int id = tid; id < NE; id += THREADS) {
-      int k, i;
-      entry_of(id, k, i);
-      const PE e = pools[(size_t)k * PC + i];
-      const uint64_t packed = ((uint64_t)desc_key(e.score) << 32) | ((uint64_t)k << 16) | (uint64_t)id;
-      atomicMin(reinterpret_cast<unsigned long long *>(&best[hslot[id]]), (unsigned long long)packed);
-    }
-    __syncthreads();
-    for (int id = tid; id < NE; id += THREADS) {
-      const int rid = (int)(best[hslot[id]] & 0xFFFF);
-      if (rid == id) continue;
-      int k, i, rk, ri;
-      entry_of(id, k, i);
-      entry_of(rid, rk, ri);
-      if (seq_cmp(c, k, pools[(size_t)k * PC + i], rk, pools[(size_t)rk * PC + ri]) != 0) sh.coll = 1;
+    for (int i = tid; i < n; i += THREADS) {
+      const int r = (int)(best[hslot[i]] & 0xFFFF);
+      if (r != i && seq_cmp(c, ent[i], ent[r]) != 0) sh.coll = 1;
     }
     __syncthreads();
     if (!sh.coll) break;
@@ -594,53 +637,66 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     if (tid == 0) report(prm.status, MFD_ERR_UNSUPPORTED);
     return;
   }
-  // primaries (one per distinct prefix) and their running counts per list
-  for (int id = tid; id < NE; id += THREADS) {
-    prim[id] = (int)(best[hslot[id]] & 0xFFFF) == id;
-    nodeid[id] = -1;
+  for (int i = tid; i < n; i += THREADS) {
+    prim[i] = (int)(best[hslot[i]] & 0xFFFF) == i;
+    nodeid[i] = -1;
   }
   __syncthreads();
-  if (warp < K) {
-    const int k = warp, o = sh.off[k], n = sh.cnt[k];
-    int run = 0;
-    for (int base = 0; base < n; base += 32) {
+
+  // ---------------------------------------------------- the B best prefixes
+  radix_bound(sh, ent, n, 1, B, 2, hist1, [&](int i) { return prim[i] ? 0 : -1; });
+  if (tid == 0) sh.n_sel = 0;
+  __syncthreads();
+  {
+    const bool ht = sh.act[0];
+    const uint32_t tau = sh.pre[0] | 0xFFFFu;
+    for (int base = warp * 32; base < n; base += THREADS) {
       const int i = base + lane;
-      const int f = i < n ? prim[o + i] : 0;
-      const int incl = warp_excl_scan(f, lane) + f;
-      if (i < n) pcnt[o + i] = (uint16_t)(run + incl);
-      run += __shfl_sync(0xffffffffu, incl, 31);
+      const bool in = i < n && prim[i] && (!ht || desc_key(ent[i].score) <= tau);
+      const int k = warp_append(&sh.n_sel, in);
+      if (in) {
+        sel[k] = (uint16_t)i;
+        skk[k] = desc_key(ent[i].score);
+      }
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    int tot = 0;
-    for (int k = 0; k < K; ++k)
-      if (sh.cnt[k]) tot += pcnt[sh.off[k] + sh.cnt[k] - 1];
-    sh.total_prim = tot;
-  }
-  // node index of a primary: 1 + the primaries before it, over every list
-  for (int id = tid; id < NE; id += THREADS) {
-    if (!prim[id]) continue;
-    int k, i;
-    entry_of(id, k, i);
-    const PE e = pools[(size_t)k * PC + i];
-    int before = pcnt[id] - 1;
-    for (int k2 = 0; k2 < K && before < B; ++k2) {
-      if (k2 == k) continue;
-      const PE *P2 = pools + (size_t)k2 * PC;
-      int lo = 0, hi = sh.cnt[k2];  // first entry of list k2 not before e
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (x_before(c, k2, P2[mid], k, e))
-          lo = mid + 1;
-        else
-          hi = mid;
+  const int ns = sh.n_sel;
+  const int ns4 = (ns + 3) & ~3;
+  for (int b = ns + tid; b < ns4; b += THREADS) skk[b] = 0xFFFFFFFFu;  // never before a real key
+  __syncthreads();
+  // rank of each selected prefix = how many others come before it: score
+  // keys first (four per load, two threads per prefix, each half of the
+  // keys), then token order for the rare equal scores
+  {
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(skk);
+    const int nw = ns4 >> 2, h4 = nw >> 1;  // words of four keys; the first half
+    for (int base = warp * 32; base < 2 * ns; base += THREADS) {
+      const int a2 = base + lane;
+      const bool valid = a2 < 2 * ns;
+      const int a = valid ? a2 >> 1 : 0, half = a2 & 1;
+      int lt = 0;
+      if (valid) {
+        const uint32_t ka = skk[a];
+        const int w0 = half ? h4 : 0, w1 = half ? nw : h4;
+        int eq = 0;
+        for (int w = w0; w < w1; ++w) {
+          const uint4 v = s4[w];
+          lt += (v.x < ka) + (v.y < ka) + (v.z < ka) + (v.w < ka);
+          eq += (v.x == ka) + (v.y == ka) + (v.z == ka) + (v.w == ka);
+        }
+        const int self = (a >= 4 * w0 && a < 4 * w1) ? 1 : 0;
+        if (eq > self) {  // another prefix has the same score key
+          const PE ea = ent[sel[a]];
+          for (int b = 4 * w0; b < 4 * w1 && b < ns; ++b)
+            if (b != a && skk[b] == ka && seq_cmp(c, ent[sel[b]], ea) < 0) ++lt;
+        }
       }
-      if (lo > 0) before += pcnt[sh.off[k2] + lo - 1];
-    }
-    if (before < B) {
-      nodeid[id] = (int16_t)(before + 1);
-      nslot[before + 1] = (uint16_t)id;
+      lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+      if (valid && half == 0 && lt < B) {
+        nslot[lt + 1] = sel[a];
+        nodeid[sel[a]] = (int16_t)(lt + 1);
+      }
     }
   }
   if (tid == 0) {
@@ -648,33 +704,29 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     sh.bad = 0;
   }
   __syncthreads();
-  const int nn = sh.total_prim < B ? sh.total_prim : B;
-  // parents: the table entry of the sequence without its last token
+  const int nn = ns < B ? ns : B;
+
+  // ---------------------------------------------------- parents
   for (int nd = 1 + tid; nd <= nn; nd += THREADS) {
-    const int id = nslot[nd];
-    int k, i;
-    entry_of(id, k, i);
-    const PE e = pools[(size_t)k * PC + i];
+    const int i = nslot[nd];
+    const PE e = ent[i];
     const int d = pk_depth(e.k1);
     int par = 0;
     if (d > 1) {
       par = -1;
-      const uint64_t h = mix64(hp[id] ^ seed);
+      const uint64_t h = seq_hash(c, e, d - 1, seed);
       const uint32_t tg = (uint32_t)(h >> 32) | 1u;
       uint32_t s = (uint32_t)h & (uint32_t)(tsize - 1);
       for (int probe = 0; probe < tsize && par < 0; ++probe) {
         const uint32_t t0 = tag[s];
         if (t0 == 0u) break;
         if (t0 == tg) {
-          const int rid = (int)(best[s] & 0xFFFF);
-          int rk, ri;
-          entry_of(rid, rk, ri);
-          const PE r = pools[(size_t)rk * PC + ri];
-          if (pk_depth(r.k1) == d - 1) {
+          const int r = (int)(best[s] & 0xFFFF);
+          const PE g = ent[r];
+          if (pk_depth(g.k1) == d - 1) {
             bool same = true;
-            for (int p = 1; p < d && same; ++p)
-              same = token_at(c, rk, r.k0, r.k1, p) == token_at(c, k, e.k0, e.k1, p);
-            if (same) par = nodeid[rid];
+            for (int p = 1; p < d && same; ++p) same = token_at(c, g, p) == token_at(c, e, p);
+            if (same) par = nodeid[r];
           }
         }
         s = (s + 1) & (uint32_t)(tsize - 1);
@@ -703,14 +755,12 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       sc = 0.f;
       ps = bp;
     } else if (nd <= nn) {
-      int k, i;
-      entry_of(nslot[nd], k, i);
-      const PE e = pools[(size_t)k * PC + i];
+      const PE e = ent[nslot[nd]];
       dp = pk_depth(e.k1);
       pa = par_s[nd];
-      tk = (int)token_at(c, k, e.k0, e.k1, dp);
+      tk = (int)token_at(c, e, dp);
       sc = e.score;
-      md = k;
+      md = pk_mode(e.k1);
       ps = bp + dp;
     }
     prm.parent[ob + nd] = pa;
@@ -740,13 +790,14 @@ int next_pow2(int x) {
 }  // namespace
 
 size_t tree_smem_bytes(int K, int L, int topk, int B, int *cap_out, int *tsize_out) {
-  const int tsize = next_pow2(2 * K * B > 64 ? 2 * K * B : 64);
   const size_t budget = 232448 - sizeof(Shared) - 1024;
-  const int need = next_pow2(B) > B + 2 * topk ? next_pow2(B) : B + 2 * topk;
-  for (int pc = 4096; pc >= need; pc -= 32) {
-    const Layout y = make_layout(K, L, topk, B, pc, tsize);
+  const int need = K * B + K * topk + 64;
+  for (int cap = 6144; cap >= need; cap -= 128) {
+    const int nc = cap < K * B + 512 ? cap : K * B + 512;
+    const int tsize = next_pow2(nc + nc / 2);
+    const Layout y = make_layout(K, L, topk, B, cap, nc, tsize);
     if (y.total > budget) continue;
-    *cap_out = pc;
+    *cap_out = cap;
     *tsize_out = tsize;
     return y.total;
   }
@@ -754,8 +805,8 @@ size_t tree_smem_bytes(int K, int L, int topk, int B, int *cap_out, int *tsize_o
 }
 
 cudaError_t launch_build_tree(const TreeLaunch &T, cudaStream_t stream) {
-  int pc = 0, tsize = 0;
-  const size_t bytes = tree_smem_bytes(T.K, T.L, T.topk, T.B, &pc, &tsize);
+  int cap = 0, tsize = 0;
+  const size_t bytes = tree_smem_bytes(T.K, T.L, T.topk, T.B, &cap, &tsize);
   if (bytes == 0) return cudaErrorInvalidValue;
   Params p;
   p.tk_logp = T.tk_logp;
@@ -775,11 +826,23 @@ cudaError_t launch_build_tree(const TreeLaunch &T, cudaStream_t stream) {
   p.pos = T.pos;
   p.n_nodes = T.n_nodes;
   p.status = T.status;
-  p.pc = pc;
+  p.cap = cap;
+  p.nc = cap < T.K * T.B + 512 ? cap : T.K * T.B + 512;
   p.tsize = tsize;
   cudaError_t e = cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  build_tree_kernel<<<T.n_req, THREADS, bytes, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(T.n_req);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, build_tree_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
