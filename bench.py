@@ -34,6 +34,8 @@ WORKLOADS = {
     "k8_l15_h2560_v151936_b256_t1": dict(K=8, L=15, H=2560, V=151936, n_shared=11, topk=16, B=256, T=1.0),
     "k8_l15_h2560_v151936_b64_greedy": dict(K=8, L=15, H=2560, V=151936, n_shared=11, topk=16, B=64, T=0.0),
     "k8_l15_h5120_v248320_b256_greedy": dict(K=8, L=15, H=5120, V=248320, n_shared=13, topk=32, B=256, T=0.0),
+    # a small shape for quick host-side runs (the reference arm in CPU tests)
+    "tiny": dict(K=2, L=4, H=64, V=512, n_shared=2, topk=8, B=16, T=1.0),
 }
 DEFAULT = "k8_l15_h2560_v151936_b256_t1"
 METRIC = "draft-tree rounds/s at K=8,V=151936,B=256; LM-head HBM GB/s vs GB300 peak"
@@ -51,6 +53,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-rounds", type=int, default=0,
+                    help="run this many untimed rounds (LM head, tree, verify) and exit: the ncu capture target")
     return ap.parse_args()
 
 
@@ -121,7 +125,8 @@ def dist_setup():
     if ws > 1:
         import torch.distributed as dist
 
-        dist.init_process_group("nccl" if _cuda() else "gloo")
+        if not dist.is_initialized():
+            dist.init_process_group("nccl" if _cuda() else "gloo")
     return ws, rank, local
 
 
@@ -140,6 +145,12 @@ def reduce_max(x: float, ws: int) -> float:
     t = torch.tensor([x], dtype=torch.float64, device="cuda" if _cuda() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(steps: int, ws: int, max_ms: float) -> float:
+    """Rounds per second of the whole job: every replica runs `steps` rounds,
+    over the slowest rank's timed interval."""
+    return ws * steps / (max_ms / 1e3)
 
 
 def barrier(ws):
@@ -270,7 +281,7 @@ def run_gpu(args, ws, rank, local):
         vf += s2.elapsed_time(e3)
     total_ms = reduce_max(lm + bd + vf, ws)
     steps = args.steps
-    value = ws * steps / (total_ms / 1e3)
+    value = whole_job_rate(steps, ws, total_ms)
     acc = acc_buf[args.warmup:].float().cpu().numpy()
     sites = {**sites_t}
 
@@ -454,9 +465,41 @@ def run_reference(args, ws, rank):
             "e2e": {"value": round(value, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def profile_rounds(args, local):
+    """A few untimed rounds of the three calls on the workload's shapes, so
+    that an ncu capture sees each kernel with few launches before it."""
+    import torch
+
+    from tree_verified_speculative_gb300 import mfd
+
+    cfg = WORKLOADS[args.workload]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    W, rounds, noise = make_inputs(cfg, 1, 0)
+    Wd = W.to(dev)
+    h = rounds[0].h.to(dev)
+    t = torch.from_numpy(noise[0]).to(dev)
+    temp = torch.tensor([cfg["T"]], dtype=torch.float32, device=dev)
+    seed = torch.tensor(np.array([rounds[0].seed], np.uint64).view(np.int64), device=dev)
+    rd = mfd.Round(1, cfg["K"], cfg["L"], cfg["topk"], cfg["B"], cfg["V"], device=dev)
+    rd.status.zero_()
+    for _ in range(args.profile_rounds):
+        rd.lmhead_topk(h, Wd)
+        rd.build_tree()
+        rd.verify(t, temp, seed)
+    torch.cuda.synchronize()
+    st = int(rd.status.item())
+    print(json.dumps({"profile_rounds": args.profile_rounds, "workload": args.workload, "status": st}))
+    if st != mfd.MFD_OK:
+        raise SystemExit(1)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_setup()
+    if args.profile_rounds > 0:
+        profile_rounds(args, local)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, ws, rank)))
