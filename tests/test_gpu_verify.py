@@ -127,3 +127,65 @@ def test_rejects_bad_temperature():
     t = np.zeros((1, 2, 16), np.float32)
     _, _, _, st = _gpu_verify(t, parent, token, [2], 2, [-1.0], [0])
     assert st == mfd.MFD_ERR_INPUT
+
+
+def test_workspace_reuse_and_graph_replay():
+    """The walk's exchange words need no zeroing between calls: the same
+    workspace is reused after other writers (zeros, a byte pattern, random
+    bytes, another call's scratch) and under CUDA-graph replay, with long
+    greedy walks (many steps, so both parities of every word are reused)."""
+    rng = np.random.default_rng(77)
+    V = 151936
+    tree, futs = _trees(rng, 2, 8, 15, 16, V, 128)
+    t = _targets(rng, tree, futs, V, [4, 6])
+    n_req, N = tree["parent"].shape
+    ref = [oracle.verify(t[q], tree["parent"][q], tree["token"][q], int(tree["n_nodes"][q]), 15, 0.0, 0)
+           for q in range(n_req)]
+    assert max(int(r[0]) for r in ref) >= 3  # the walks are long
+    rd = mfd.Round(n_req, 1, 15, 1, N - 1, V)
+    rd.parent.copy_(torch.from_numpy(tree["parent"]))
+    rd.token.copy_(torch.from_numpy(tree["token"]))
+    rd.n_nodes.copy_(torch.from_numpy(tree["n_nodes"].astype(np.int32)))
+    rd.status.zero_()
+    td = torch.from_numpy(t).cuda()
+    temp = torch.zeros(n_req, device="cuda")
+    seed = torch.zeros(n_req, dtype=torch.int64, device="cuda")
+
+    def check():
+        torch.cuda.synchronize()
+        assert status_of(rd) == 0
+        acc, path, out = np_(rd.accept_len), np_(rd.path_nodes), np_(rd.out_tokens)
+        for q in range(n_req):
+            assert check_walk(int(acc[q]), path[q], out[q], *ref[q], sampled=False)
+        rd.accept_len.fill_(-7)
+        rd.path_nodes.fill_(-7)
+        rd.out_tokens.fill_(-7)
+
+    fills = [lambda: None, lambda: rd.ws.zero_(), lambda: rd.ws.fill_(1), lambda: rd.ws.fill_(0xFF),
+             lambda: rd.ws.copy_(torch.randint(0, 256, rd.ws.shape, dtype=torch.uint8, device="cuda"))]
+    for fill in fills:
+        fill()
+        rd.verify(td, temp, seed)
+        check()
+        rd.verify(td, temp, seed)  # right after a call: the previous call's words are in place
+        check()
+    # another op's scratch in between (top-k partials written into the same workspace)
+    logits = torch.randn((4, 4096), device="cuda")
+    tl = torch.empty((4, 8), device="cuda")
+    tt = torch.empty((4, 8), dtype=torch.int32, device="cuda")
+    mfd.mfd_logits_topk(logits, 8, tl, tt, None, rd.status, rd.ws)
+    rd.verify(td, temp, seed)
+    check()
+    # graph capture and replay: identical launch parameters every replay
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        rd.verify(td, temp, seed)
+    torch.cuda.current_stream().wait_stream(s)
+    check()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        rd.verify(td, temp, seed)
+    for _ in range(4):
+        g.replay()
+        check()

@@ -66,9 +66,8 @@ struct VerifyLaunch {
   const float *temperature;
   const uint64_t *seed;
   int32_t *accept_len, *path_nodes, *out_tokens, *status;
-  unsigned *bar;   // [max_groups] zeroed before the launch
-  float2 *part;    // [grid][2]
-  int grid;        // cooperative grid size
+  unsigned long long *ws;  // [grid][8] exchange words (generation-tagged, no zeroing needed)
+  int grid;                   // largest cooperative grid
 };
 int verify_max_grid(int n_sm);
 cudaError_t launch_verify(const VerifyLaunch &V, cudaStream_t stream);

@@ -129,8 +129,7 @@ TopkLayout logits_layout(int R, int V, int topk) {
   return y;
 }
 
-constexpr size_t kVerifyBarBytes = 4096;  // up to 1024 group counters
-size_t verify_bytes(int n_sm) { return kVerifyBarBytes + align256((size_t)mfd::verify_max_grid(n_sm) * 2 * 8); }
+size_t verify_bytes(int n_sm) { return align256((size_t)mfd::verify_max_grid(n_sm) * 8 * 8); }
 
 size_t tree_bytes(int n_req) {
   (void)n_req;
@@ -368,8 +367,6 @@ int mfd_verify(const float *target_logits, int n_req, int B, int V, int L, const
   if (rc != MFD_OK) return rc;
   if (!ws || ws_bytes < verify_bytes(d.n_sm) || !aligned(ws, 256)) return MFD_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  char *base = static_cast<char *>(ws);
-  if ((rc = cuda_status(cudaMemsetAsync(base, 0, kVerifyBarBytes, s))) != MFD_OK) return rc;
   mfd::VerifyLaunch Vl;
   Vl.t = target_logits;
   Vl.n_req = n_req;
@@ -385,8 +382,7 @@ int mfd_verify(const float *target_logits, int n_req, int B, int V, int L, const
   Vl.path_nodes = path_nodes;
   Vl.out_tokens = out_tokens;
   Vl.status = status;
-  Vl.bar = reinterpret_cast<unsigned *>(base);
-  Vl.part = reinterpret_cast<float2 *>(base + kVerifyBarBytes);
+  Vl.ws = static_cast<unsigned long long *>(ws);
   Vl.grid = mfd::verify_max_grid(d.n_sm);
   return cuda_status(mfd::launch_verify(Vl, s));
 }

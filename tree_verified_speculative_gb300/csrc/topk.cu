@@ -12,166 +12,192 @@
 namespace mfd {
 namespace {
 
-constexpr int MERGE_THREADS = 256;
-constexpr int SURV_CAP = 256;  // survivors a warp gathers before falling back
-constexpr int MAX_LISTS_PER_LANE = 8;  // P <= 256
+constexpr int MERGE_THREADS = 128;       // one CTA per row
+constexpr int MERGE_WARPS = MERGE_THREADS / 32;
+constexpr int SURV_CAP = 512;            // survivors ranked before falling back
+constexpr int LISTS_PER_THREAD = 2;      // P <= 256
 
 struct Cand {
   float v;
   int i;
 };
 
-__device__ __forceinline__ Cand load_cand(const int2 *p) {
-  const int2 c = __ldcg(p);
-  return Cand{__int_as_float(c.x), c.y};
+__device__ __forceinline__ Cand cand_of(int x, int y) { return Cand{__int_as_float(x), y}; }
+__device__ __forceinline__ bool before(const Cand &a, const Cand &b) { return vi_before(a.v, a.i, b.v, b.i); }
+__device__ __forceinline__ Cand shfl_cand(const Cand &c, int o) {
+  return Cand{__shfl_xor_sync(0xffffffffu, c.v, o), __shfl_xor_sync(0xffffffffu, c.i, o)};
 }
 
 // Warp-wide best of (v, i) pairs; every lane gets the winner.
 __device__ __forceinline__ Cand warp_best(Cand c) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, c.v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, c.i, o);
-    if (vi_before(ov, oi, c.v, c.i)) {
-      c.v = ov;
-      c.i = oi;
-    }
+    const Cand d = shfl_cand(c, o);
+    if (before(d, c)) c = d;
   }
   return c;
 }
 
-// One CTA per row, one thread per list: the row's P lists (T candidates
-// each, best first) and its P (max, sum exp) pairs are staged in shared
-// memory with 16-byte loads, then every step is a parallel count:
-//   LSE   = M + log sum_q S_q exp(m_q - M)
-//   tau   = the topk-th best list head (ties ordered by list): at least topk
-//           candidates are at least as good, so nothing worse can make it
-//   top-k = survivors (the prefix of each list not worse than tau) ranked by
-//           counting how many survivors beat each one
+// One CTA of 128 threads per row; thread t owns lists t and t + 128 (P <=
+// 256), each a range's T best (value desc, id asc) plus the range's (max,
+// sum exp).  The steps are short and spread over the block so that the
+// row's critical path stays a few hundred cycles past the loads:
+//   LSE  = M + log sum_q S_q exp(m_q - M)
+//   tau  = a candidate with at least topk candidates at or before it: the
+//          threads are cut into G >= topk groups by t mod G (G a power of
+//          two), and tau is the worst of the G group bests -- G distinct
+//          candidates, each at or before tau.  Nothing after tau can be in
+//          the top-k.
+//   top  = the survivors (each list's prefix at or before tau) ranked by
+//          counting how many survivors precede each one.
 template <int T>
 __global__ void __launch_bounds__(MERGE_THREADS)
     merge_topk_kernel(const float2 *__restrict__ part_ms, const int2 *__restrict__ part_cand, int R, int P,
                       int topk, float *__restrict__ tk_logp, int32_t *__restrict__ tk_tok, float *__restrict__ lse_out) {
-  extern __shared__ int4 merge_smem[];
   __shared__ Cand surv[SURV_CAP];
   __shared__ Cand top[32];
-  __shared__ int2 heads[MERGE_THREADS + 4];
-  __shared__ float red[MERGE_THREADS / 32];
-  __shared__ Cand tau_s;
+  __shared__ Cand gbest[MERGE_WARPS][32];
+  __shared__ float red_m[MERGE_WARPS], red_s[MERGE_WARPS];
   __shared__ int n_surv_s;
-  __shared__ float lse_s, m_s;
   pdl_wait();
   pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;
   if (row >= R) return;
-  int2 *cs = reinterpret_cast<int2 *>(merge_smem);
-  float2 *ms = reinterpret_cast<float2 *>(cs + (size_t)P * T);
-  {
-    const int4 *src = reinterpret_cast<const int4 *>(part_cand + (size_t)row * P * T);
-    const int n4 = P * T / 2;
-    for (int i = tid; i < n4; i += MERGE_THREADS) merge_smem[i] = __ldcg(src + i);
-    for (int i = tid; i < P; i += MERGE_THREADS) ms[i] = __ldcg(part_ms + (size_t)row * P + i);
-  }
-  if (tid == 0) {
-    n_surv_s = 0;
-    tau_s = Cand{-INFINITY, 0x7FFFFFFF};
-  }
-  __syncthreads();
-  auto cand_at = [&](int q, int c) {
-    const int2 e = cs[q * T + c];
-    return Cand{__int_as_float(e.x), e.y};
+  const float2 *ms = part_ms + (size_t)row * P;
+  const int2 *cand = part_cand + (size_t)row * P * T;
+  auto list_at = [&](int q, int j) {
+    const int2 e = __ldcg(cand + (size_t)q * T + j);
+    return cand_of(e.x, e.y);
   };
-  const int q = tid;  // this thread's list
-  const bool has = q < P;
+  if (tid == 0) n_surv_s = 0;
 
-  // ---- log-sum-exp
-  float x = has ? ms[q].x : -INFINITY;
-  x = warp_max(x);
-  if (lane == 0) red[warp] = x;
-  __syncthreads();
-  if (tid == 0) {
-    float M = red[0];
-    for (int w = 1; w < MERGE_THREADS / 32; ++w) M = fmaxf(M, red[w]);
-    m_s = M;
-  }
-  __syncthreads();
-  const float M = m_s;
-  float sv = (has && ms[q].x > -INFINITY) ? ms[q].y * expf(ms[q].x - M) : 0.f;
-  sv = warp_sum(sv);
-  __syncthreads();
-  if (lane == 0) red[warp] = sv;
-  __syncthreads();
-  if (tid == 0) {
-    float S = 0.f;
-    for (int w = 0; w < MERGE_THREADS / 32; ++w) S += red[w];
-    lse_s = M + logf(S);
-  }
-
-  // ---- tau: rank of this list's head among all heads (heads copied to a
-  // compact array; four independent counters keep the loads in flight)
-  const int need = topk < P ? topk : P;
-  if (has) heads[q] = cs[q * T];
-  if (tid < 4) heads[P + tid] = make_int2(__float_as_int(-INFINITY), 0x7FFFFFFF);  // padding: never before
-  __syncthreads();
-  if (has) {
-    const Cand h = cand_at(q, 0);
-    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-    const int P4 = (P + 3) & ~3;
-    for (int o = 0; o < P4; o += 4) {
-      const int2 g0 = heads[o], g1 = heads[o + 1], g2 = heads[o + 2], g3 = heads[o + 3];
-      r0 += vi_before(__int_as_float(g0.x), g0.y, h.v, h.i) || (__int_as_float(g0.x) == h.v && g0.y == h.i && o < q);
-      r1 += vi_before(__int_as_float(g1.x), g1.y, h.v, h.i) || (__int_as_float(g1.x) == h.v && g1.y == h.i && o + 1 < q);
-      r2 += vi_before(__int_as_float(g2.x), g2.y, h.v, h.i) || (__int_as_float(g2.x) == h.v && g2.y == h.i && o + 2 < q);
-      r3 += vi_before(__int_as_float(g3.x), g3.y, h.v, h.i) || (__int_as_float(g3.x) == h.v && g3.y == h.i && o + 3 < q);
+  // ---- (max, sum exp) and the first two candidates of each owned list
+  float m[LISTS_PER_THREAD], sx[LISTS_PER_THREAD];
+  Cand h0[LISTS_PER_THREAD], h1[LISTS_PER_THREAD];
+#pragma unroll
+  for (int s = 0; s < LISTS_PER_THREAD; ++s) {
+    const int q = tid + MERGE_THREADS * s;
+    m[s] = -INFINITY;
+    sx[s] = 0.f;
+    h0[s] = h1[s] = Cand{-INFINITY, 0x7FFFFFFF};
+    if (q < P) {
+      const float2 x = __ldcg(ms + q);
+      const int4 c = __ldcg(reinterpret_cast<const int4 *>(cand + (size_t)q * T));
+      m[s] = x.x;
+      sx[s] = x.y;
+      h0[s] = cand_of(c.x, c.y);
+      h1[s] = cand_of(c.z, c.w);
     }
-    // the padding heads equal (-inf, max) and sit after every list, so they
-    // never count for a real head
-    const int r = r0 + r1 + r2 + r3;
-    if (r == need - 1 && need == topk) tau_s = h;
   }
-  __syncthreads();
-  const Cand tau = tau_s;  // (-inf, max) when there are fewer lists than topk: keep all
 
-  // ---- survivors: the prefix of each list not worse than tau
+  // ---- per-warp partials of the LSE and of the group bests
+  const float wm = warp_max(fmaxf(m[0], m[1]));
+  float ls = 0.f;
+#pragma unroll
+  for (int s = 0; s < LISTS_PER_THREAD; ++s)
+    if (m[s] > -INFINITY) ls += sx[s] * expf(m[s] - wm);
+  ls = warp_sum(ls);
+  int G = 1;
+  while (G < topk) G <<= 1;
+  Cand g = before(h0[1], h0[0]) ? h0[1] : h0[0];
+  for (int o = 16; o >= G; o >>= 1) {
+    const Cand d = shfl_cand(g, o);
+    if (before(d, g)) g = d;
+  }
+  if (lane == 0) {
+    red_m[warp] = wm;
+    red_s[warp] = ls;
+  }
+  if (lane < G) gbest[warp][lane] = g;
+  __syncthreads();
+
+  float M = red_m[0];
+#pragma unroll
+  for (int w = 1; w < MERGE_WARPS; ++w) M = fmaxf(M, red_m[w]);
+  float S = 0.f;
+#pragma unroll
+  for (int w = 0; w < MERGE_WARPS; ++w)
+    if (red_m[w] > -INFINITY) S += red_s[w] * expf(red_m[w] - M);
+  const float lse = M + logf(S);
+  // group (lane mod G) best over the warps, then the worst over the groups
+  Cand t = gbest[0][lane & (G - 1)];
+#pragma unroll
+  for (int w = 1; w < MERGE_WARPS; ++w) {
+    const Cand d = gbest[w][lane & (G - 1)];
+    if (before(d, t)) t = d;
+  }
+  for (int o = G >> 1; o > 0; o >>= 1) {
+    const Cand d = shfl_cand(t, o);
+    if (before(t, d)) t = d;
+  }
+  const Cand tau = t;  // (-inf, max) when a group owns no list: everything survives
+
+  // ---- survivors: per owned list, the prefix at or before tau
+  int cnt[LISTS_PER_THREAD];
   int c = 0;
-  if (has)
-    while (c < T) {
-      const Cand e = cand_at(q, c);
-      if (vi_before(tau.v, tau.i, e.v, e.i)) break;
-      ++c;
+#pragma unroll
+  for (int s = 0; s < LISTS_PER_THREAD; ++s) {
+    const int q = tid + MERGE_THREADS * s;
+    int k = 0;
+    if (q < P && !before(tau, h0[s])) {
+      k = 1;
+      if (T > 1 && !before(tau, h1[s])) {
+        k = 2;
+        while (k < T && !before(tau, list_at(q, k))) ++k;
+      }
     }
-  const int slot = c ? atomicAdd(&n_surv_s, c) : 0;
-  if (c && slot + c <= SURV_CAP)
-    for (int k = 0; k < c; ++k) surv[slot + k] = cand_at(q, k);
+    cnt[s] = k;
+    c += k;
+  }
+  int off = c ? atomicAdd(&n_surv_s, c) : 0;
+  if (c && off + c <= SURV_CAP) {
+#pragma unroll
+    for (int s = 0; s < LISTS_PER_THREAD; ++s) {
+      const int q = tid + MERGE_THREADS * s;
+      if (cnt[s] > 0) surv[off++] = h0[s];
+      if (cnt[s] > 1) surv[off++] = h1[s];
+      for (int k = 2; k < cnt[s]; ++k) surv[off++] = list_at(q, k);
+    }
+  }
   __syncthreads();
   const int n_surv = n_surv_s;
+
   if (n_surv <= SURV_CAP) {
+    // rank = survivors before this one (equal pairs, only the padding, are
+    // ordered by slot)
     for (int a = tid; a < n_surv; a += MERGE_THREADS) {
       const Cand e = surv[a];
-      int r = 0;
-      for (int b = 0; b < n_surv; ++b) {
-        const Cand f = surv[b];
-        r += vi_before(f.v, f.i, e.v, e.i) || (f.v == e.v && f.i == e.i && b < a);
+      int r0 = 0, r1 = 0;
+      int b = 0;
+      for (; b + 1 < n_surv; b += 2) {
+        const Cand f0 = surv[b], f1 = surv[b + 1];
+        r0 += before(f0, e) || (f0.v == e.v && f0.i == e.i && b < a);
+        r1 += before(f1, e) || (f1.v == e.v && f1.i == e.i && b + 1 < a);
       }
+      if (b < n_surv) {
+        const Cand f = surv[b];
+        r0 += before(f, e) || (f.v == e.v && f.i == e.i && b < a);
+      }
+      const int r = r0 + r1;
       if (r < topk) top[r] = e;
     }
   } else if (warp == 0) {
     // many exact ties at the cut: topk rounds of "best remaining list head"
-    int pos[MAX_LISTS_PER_LANE];
+    int pos[8];
 #pragma unroll
-    for (int s2 = 0; s2 < MAX_LISTS_PER_LANE; ++s2) pos[s2] = 0;
+    for (int s = 0; s < 8; ++s) pos[s] = 0;
     for (int r = 0; r < topk; ++r) {
       Cand b = Cand{-INFINITY, 0x7FFFFFFF};
       int bs = -1;
 #pragma unroll
-      for (int s2 = 0; s2 < MAX_LISTS_PER_LANE; ++s2) {
-        const int qq = lane + 32 * s2;
-        if (qq < P && pos[s2] < T) {
-          const Cand e = cand_at(qq, pos[s2]);
-          if (bs < 0 || vi_before(e.v, e.i, b.v, b.i)) {
+      for (int s = 0; s < 8; ++s) {
+        const int q = lane + 32 * s;
+        if (q < P && pos[s] < T) {
+          const Cand e = list_at(q, pos[s]);
+          if (bs < 0 || before(e, b)) {
             b = e;
-            bs = s2;
+            bs = s;
           }
         }
       }
@@ -179,8 +205,8 @@ __global__ void __launch_bounds__(MERGE_THREADS)
       const unsigned owner = __ballot_sync(0xffffffffu, bs >= 0 && b.v == w.v && b.i == w.i);
       if (lane == __ffs(owner) - 1) {
 #pragma unroll
-        for (int s2 = 0; s2 < MAX_LISTS_PER_LANE; ++s2)
-          if (s2 == bs) ++pos[s2];
+        for (int s = 0; s < 8; ++s)
+          if (s == bs) ++pos[s];
       }
       if (lane == 0) top[r] = w;
     }
@@ -189,19 +215,17 @@ __global__ void __launch_bounds__(MERGE_THREADS)
 
   // ---- log-probabilities, final order (log p desc, id asc)
   if (tid < topk) {
-    const float lse = lse_s;
     const Cand e = top[tid];
     const float lp = e.v - lse;
     int r2 = 0;
     for (int o = 0; o < topk; ++o) {
       if (o == tid) continue;
-      const float olp = top[o].v - lse;
-      r2 += vi_before(olp, top[o].i, lp, e.i);
+      r2 += vi_before(top[o].v - lse, top[o].i, lp, e.i);
     }
     tk_logp[(size_t)row * topk + r2] = lp;
     tk_tok[(size_t)row * topk + r2] = e.i;
-    if (tid == 0 && lse_out) lse_out[row] = lse;
   }
+  if (tid == 0 && lse_out) lse_out[row] = lse;
 }
 
 // One warp per (row, vocabulary chunk): lane-local online softmax and top-T,
@@ -276,20 +300,17 @@ __global__ void __launch_bounds__(128)
 
 template <int T>
 cudaError_t merge_t(const MergeLaunch &M, cudaStream_t s) {
-  const size_t smem = (size_t)M.P * T * 8 + (size_t)M.P * 8;
-  cudaError_t e = cudaFuncSetAttribute(merge_topk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(M.R);
   cfg.blockDim = dim3(MERGE_THREADS);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, merge_topk_kernel<T>, reinterpret_cast<const float2 *>(M.part_ms),
+  cudaError_t e = cudaLaunchKernelEx(&cfg, merge_topk_kernel<T>, reinterpret_cast<const float2 *>(M.part_ms),
                          reinterpret_cast<const int2 *>(M.part_cand), M.R, M.P, M.topk, M.tk_logp, M.tk_tok, M.lse);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -307,7 +328,7 @@ cudaError_t partial_t(const LogitsPartialLaunch &L, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_merge_topk(const MergeLaunch &M, cudaStream_t s) {
-  if (M.P > 32 * MAX_LISTS_PER_LANE) return cudaErrorInvalidValue;
+  if (M.P > MERGE_THREADS * LISTS_PER_THREAD) return cudaErrorInvalidValue;
   switch (M.T) {
     case 8: return merge_t<8>(M, s);
     case 16: return merge_t<16>(M, s);

@@ -9,9 +9,10 @@
 // Each step reduces one vocabulary row (V up to ~250K fp32) and the next
 // step depends on its result, so the walk is a chain of short, wide
 // reductions.  One cooperative grid covers the GPU; the CTAs of a request's
-// group split the row, publish (best value, index), meet at a bounded
-// grid-group barrier and all read the winner.  Only rows on the walk are read.
-#include <cooperative_groups.h>
+// group split the row and publish (best value, index) in tagged slots; the
+// group's first CTA waits (bounded) for every slot of the step, publishes the
+// winner in one tagged word, and the others wait (bounded) on that word.
+// Only rows on the walk are read.
 
 #include "lmhead.h"
 #include "mfd_device.cuh"
@@ -50,9 +51,43 @@ __device__ __forceinline__ float gumbel(uint64_t seed, int node, int v) {
   return -logf(-logf(u));
 }
 
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// A published step result: one 64-bit word, value in bits 63..32,
+// vocabulary index in bits 31..2 (0x3FFFFFFF = none; V < 2^30), and a 2-bit
+// tag in bits 1..0.  Result words are double-buffered by step parity; step e
+// writes tag 1 + ((e >> 1) & 1), which differs from the tag step e - 2 left
+// in the same word and from zero.
+//
+// No zeroing pass is needed before a call.  The workspace holds, per group, a
+// generation word gen; every CTA reads it at the start (all read the same
+// value, see below), and with G = gen + 1:
+//   - each CTA clears the result words it will write, then stores G into its
+//     ready word with release semantics;
+//   - a reader waits until the writer's ready word holds G and takes it with
+//     acquire semantics before it trusts that writer's result words: what it
+//     then reads is the clear or a value of this call, never an earlier call's;
+//   - the group's first CTA stores G into gen when it leaves, after it has
+//     acquired every ready word of the group, so every CTA of the group read
+//     gen before that store; the next call therefore uses G + 1, and a ready
+//     word left by an earlier call never matches (also under graph replay).
+// Workspace contents left by other calls only matter if a ready word happens
+// to equal its group's gen + 1, which fresh, zeroed or pattern-filled memory
+// does not.
+constexpr uint32_t IDX_NONE = 0x3FFFFFFFu;
+
+__device__ __forceinline__ unsigned long long slot_pack(float v, int i, unsigned tag) {
+  const uint32_t ii = (i >= 0 && (uint32_t)i < IDX_NONE) ? (uint32_t)i : IDX_NONE;
+  return ((unsigned long long)__float_as_uint(v) << 32) | ((unsigned long long)ii << 2) | tag;
+}
+__device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void st_relaxed(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -63,26 +98,90 @@ struct Params {
   const float *temperature;
   const uint64_t *seed;
   int32_t *accept_len, *path_nodes, *out_tokens, *status;
-  unsigned *bar;
-  float2 *part;
-  int cpr;  // CTAs per request group
+  unsigned long long *ws;  // [grid][8] words: see Ws
+  int cpr;                    // CTAs per request group
 };
 
+// Workspace words, 7 per CTA of the grid: per group g its gen, its leader's
+// ready word and its result words; per CTA b its ready word and result words.
+struct Ws {
+  unsigned long long *base;
+  int grid;
+  __device__ unsigned long long *gen(int g) const { return base + g; }
+  __device__ unsigned long long *lready(int g) const { return base + grid + g; }
+  __device__ unsigned long long *res(int g, unsigned par) const { return base + 2 * grid + 2 * g + par; }
+  __device__ unsigned long long *ready(int b) const { return base + 4 * grid + b; }
+  __device__ unsigned long long *slot(int b, unsigned par) const { return base + 5 * grid + 2 * b + par; }
+};
+
+constexpr int NODE_SLOTS = (MAX_NODES + 31) / 32;  // nodes a lane of warp 0 holds
+constexpr int POLL_SLOTS = 8;                       // group slots a lane polls (cpr <= 256)
+constexpr int PRE = 4;                              // root-row entries a thread loads up front
+
+
+// Per step: every thread scans its share of the row (loads first, then the
+// arithmetic), the CTA reduces to one (value, index), warp 0 exchanges it
+// with the group (above), takes the winner y and looks for the child of cur
+// carrying y in the node table it holds in registers (tokens of a node's
+// children are distinct, so at most one matches).  Two block barriers per
+// step.
 __global__ void __launch_bounds__(THREADS) verify_kernel(const Params p) {
-  __shared__ int32_t par_s[MAX_NODES], tok_s[MAX_NODES];
   __shared__ float red_v[THREADS / 32];
   __shared__ int red_i[THREADS / 32];
   __shared__ int s_next, s_ok;
-  __shared__ float s_bv;
-  __shared__ int s_bi;
+  __shared__ unsigned long long s_G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cpr = p.cpr;
   const int grp = blockIdx.x / cpr, c = blockIdx.x - grp * cpr;
   const int n_groups = gridDim.x / cpr;
   unsigned epoch = 0;
   const int N = p.B + 1;
+  const Ws ws{p.ws, (int)gridDim.x};
+  // generation handshake (see the comment on the result words)
+  // done by the last warp, so that warp 0's loads go out first; warp 0 takes
+  // G from shared memory after the first block barrier
+  bool acquired = false;  // this CTA has taken the ready words it reads
+  unsigned long long rdy[POLL_SLOTS];  // ready words read early (warp 0)
+#pragma unroll
+  for (int j = 0; j < POLL_SLOTS; ++j) rdy[j] = 0ull;
+  if (cpr > 1 && warp == THREADS / 32 - 1) {
+    if (lane == 0) {
+      const unsigned long long G = ld_relaxed(ws.gen(grp)) + 1ull;
+      s_G = G;
+      if (c == 0) {
+        st_relaxed(ws.res(grp, 0), 0ull);
+        st_relaxed(ws.res(grp, 1), 0ull);
+        st_release(ws.lready(grp), G);
+      } else {
+        st_relaxed(ws.slot(blockIdx.x, 0), 0ull);
+        st_relaxed(ws.slot(blockIdx.x, 1), 0ull);
+        st_release(ws.ready(blockIdx.x), G);
+      }
+    }
+  }
 
   for (int q = grp; q < p.n_req; q += n_groups) {
+    const int v0 = (int)(((long long)c * p.V) / cpr), v1 = (int)(((long long)(c + 1) * p.V) / cpr);
+    // the root's row and the node table do not depend on anything the walk
+    // computes: their loads go out first, with the request's parameters
+    float pre[PRE];
+    {
+      const float *row0 = p.t + (size_t)q * N * (size_t)p.V;
+#pragma unroll
+      for (int k = 0; k < PRE; ++k) {
+        const int v = v0 + tid + k * THREADS;
+        pre[k] = v < v1 ? __ldcs(row0 + v) : 0.f;
+      }
+    }
+    int par_r[NODE_SLOTS], tok_r[NODE_SLOTS];
+    if (warp == 0) {
+#pragma unroll
+      for (int j = 0; j < NODE_SLOTS; ++j) {
+        const int i = j * 32 + lane;
+        par_r[j] = i < N ? __ldg(p.parent + (size_t)q * N + i) : -2;
+        tok_r[j] = i < N ? __ldg(p.token + (size_t)q * N + i) : -2;
+      }
+    }
     const int n = p.n_nodes[q];
     const float T = p.temperature[q];
     const uint64_t seed = p.seed[q];
@@ -93,20 +192,39 @@ __global__ void __launch_bounds__(THREADS) verify_kernel(const Params p) {
       }
       continue;
     }
-    for (int i = tid; i < n; i += THREADS) {
-      par_s[i] = p.parent[(size_t)q * N + i];
-      tok_s[i] = p.token[(size_t)q * N + i];
+    if (warp == 0) {
+#pragma unroll
+      for (int j = 0; j < NODE_SLOTS; ++j)
+        if (j * 32 + lane >= n) par_r[j] = -2;
+      if (cpr > 1 && !acquired) {
+        // read the ready words now; they are checked at the first exchange
+        if (c == 0) {
+#pragma unroll
+          for (int j = 0; j < POLL_SLOTS; ++j) {
+            const int k = 1 + lane + 32 * j;
+            if (k < cpr) rdy[j] = ld_relaxed(ws.ready(grp * cpr + k));
+          }
+        } else if (lane == 0) {
+          rdy[0] = ld_relaxed(ws.lready(grp));
+        }
+      }
     }
-    __syncthreads();
-    const int v0 = (int)(((long long)c * p.V) / cpr), v1 = (int)(((long long)(c + 1) * p.V) / cpr);
     int cur = 0, accepted = 0;
-    int step = 0;
-    for (; step <= p.L; ++step) {
+    for (int step = 0; step <= p.L; ++step) {
       const float *row = p.t + ((size_t)q * N + cur) * (size_t)p.V;
       float bv = -INFINITY;
       int bi = 0x7FFFFFFF;
+      int v = v0 + tid;
+      if (step == 0) {
+#pragma unroll
+        for (int k = 0; k < PRE; ++k, v += THREADS) {
+          if (v < v1) {
+            const float a = T == 0.f ? pre[k] : __fadd_rn(__fdiv_rn(pre[k], T), gumbel(seed, cur, v));
+            if (vi_before(a, v, bv, bi)) { bv = a; bi = v; }
+          }
+        }
+      }
       if (T == 0.f) {
-        int v = v0 + tid;
         for (; v + 3 * THREADS < v1; v += 4 * THREADS) {
           const float a0 = __ldcs(row + v), a1 = __ldcs(row + v + THREADS), a2 = __ldcs(row + v + 2 * THREADS),
                       a3 = __ldcs(row + v + 3 * THREADS);
@@ -120,12 +238,18 @@ __global__ void __launch_bounds__(THREADS) verify_kernel(const Params p) {
           if (vi_before(a, v, bv, bi)) { bv = a; bi = v; }
         }
       } else {
-        for (int v = v0 + tid; v < v1; v += THREADS) {
+        for (; v + THREADS < v1; v += 2 * THREADS) {
+          const float t0 = __ldcs(row + v), t1 = __ldcs(row + v + THREADS);
+          const float a0 = __fadd_rn(__fdiv_rn(t0, T), gumbel(seed, cur, v));
+          const float a1 = __fadd_rn(__fdiv_rn(t1, T), gumbel(seed, cur, v + THREADS));
+          if (vi_before(a0, v, bv, bi)) { bv = a0; bi = v; }
+          if (vi_before(a1, v + THREADS, bv, bi)) { bv = a1; bi = v + THREADS; }
+        }
+        for (; v < v1; v += THREADS) {
           const float a = __fadd_rn(__fdiv_rn(__ldcs(row + v), T), gumbel(seed, cur, v));
           if (vi_before(a, v, bv, bi)) { bv = a; bi = v; }
         }
       }
-      // CTA reduction
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -146,69 +270,132 @@ __global__ void __launch_bounds__(THREADS) verify_kernel(const Params p) {
           const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
           if (vi_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
         }
-        if (lane == 0) {
-          s_bv = bv;
-          s_bi = bi;
-          s_next = 0x7FFFFFFF;
-        }
-      }
-      __syncthreads();
-      if (cpr > 1) {
-        // publish, meet, read every CTA of the group
-        if (tid == 0) {
-          p.part[(size_t)blockIdx.x * 2 + (epoch & 1u)] = make_float2(s_bv, __int_as_float(s_bi));
-          __threadfence();
-          unsigned *ctr = p.bar + grp;
-          atomicAdd(ctr, 1u);
-          const unsigned target = (epoch + 1u) * (unsigned)cpr;
-          int ok = 1;
-          if (ld_acquire(ctr) < target) {
-            const unsigned long long t0 = globaltimer();
-            while (ld_acquire(ctr) < target) {
-              if (globaltimer() - t0 > kWaitLimitNs) {
+        int ok = 1;
+        if (cpr > 1) {
+          // CTA 0 of the group gathers the other CTAs' slots and publishes
+          // the winner in the group's result word; the others publish their
+          // slot and poll that one word (a few pollers per cache line)
+          const unsigned par = epoch & 1u, tag = 1u + ((epoch >> 1) & 1u);
+          const unsigned long long t_start = globaltimer();
+          const unsigned long long G = s_G;
+          if (c == 0) {
+            // tag and payload share one 64-bit word, so relaxed loads
+            // suffice; a lane's slots are read at once and only the ones
+            // without the tag are read again
+            const int b0 = grp * cpr;
+            if (!acquired) {
+              // every other CTA of the group has cleared its result words
+              for (;;) {
+                bool all = true;
+#pragma unroll
+                for (int j = 0; j < POLL_SLOTS; ++j) all &= 1 + lane + 32 * j >= cpr || rdy[j] == G;
+                if (all) break;
+                if (globaltimer() - t_start > kWaitLimitNs) {
+                  ok = 0;
+                  break;
+                }
+#pragma unroll
+                for (int j = 0; j < POLL_SLOTS; ++j)
+                  if (1 + lane + 32 * j < cpr && rdy[j] != G) rdy[j] = ld_relaxed(ws.ready(b0 + 1 + lane + 32 * j));
+              }
+              fence_acq_rel();
+              acquired = true;
+            }
+            const unsigned long long *sp = ws.slot(b0, par);
+            unsigned long long w[POLL_SLOTS];
+#pragma unroll
+            for (int j = 0; j < POLL_SLOTS; ++j) {
+              const int k = 1 + lane + 32 * j;
+              w[j] = k < cpr ? ld_relaxed(sp + (size_t)k * 2) : (unsigned long long)tag;
+            }
+            for (; ok;) {
+              bool all = true;
+#pragma unroll
+              for (int j = 0; j < POLL_SLOTS; ++j) all &= (unsigned)(w[j] & 3ull) == tag;
+              if (all) break;
+              if (globaltimer() - t_start > kWaitLimitNs) {
                 ok = 0;
                 break;
               }
-              __nanosleep(32);
-            }
-          }
-          __threadfence();
-          s_ok = ok;
-        }
-        __syncthreads();
-        if (!s_ok) {
-          if (tid == 0) report(p.status, MFD_ERR_TIMEOUT);
-          return;
-        }
-        if (warp == 0) {
-          bv = -INFINITY;
-          bi = 0x7FFFFFFF;
-          for (int k = lane; k < cpr; k += 32) {
-            const float2 e = __ldcg(&p.part[(size_t)(grp * cpr + k) * 2 + (epoch & 1u)]);
-            const int ei = __float_as_int(e.y);
-            if (vi_before(e.x, ei, bv, bi)) { bv = e.x; bi = ei; }
-          }
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (vi_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+              for (int j = 0; j < POLL_SLOTS; ++j) {
+                const int k = 1 + lane + 32 * j;
+                if ((unsigned)(w[j] & 3ull) != tag) w[j] = ld_relaxed(sp + (size_t)k * 2);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < POLL_SLOTS; ++j) {
+              const int k = 1 + lane + 32 * j;
+              if (k >= cpr) continue;
+              const float wv = __uint_as_float((uint32_t)(w[j] >> 32));
+              const uint32_t wi = (uint32_t)(w[j] >> 2) & IDX_NONE;
+              const int wii = wi == IDX_NONE ? 0x7FFFFFFF : (int)wi;
+              if (vi_before(wv, wii, bv, bi)) { bv = wv; bi = wii; }
+            }
+            ok = __all_sync(0xffffffffu, ok);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+              const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+              if (vi_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+            }
+            if (lane == 0 && ok) st_relaxed(ws.res(grp, par), slot_pack(bv, bi, tag));
+          } else {
+            unsigned long long w = 0ull;
+            if (lane == 0) {
+              st_relaxed(ws.slot(blockIdx.x, par), slot_pack(bv, bi, tag));
+              if (!acquired) {
+                // the group's first CTA has cleared the result words
+                while (rdy[0] != G) {
+                  if (globaltimer() - t_start > kWaitLimitNs) {
+                    ok = 0;
+                    break;
+                  }
+                  rdy[0] = ld_relaxed(ws.lready(grp));
+                }
+                fence_acq_rel();
+              }
+              w = ld_relaxed(ws.res(grp, par));
+              while (ok && (unsigned)(w & 3ull) != tag) {
+                if (globaltimer() - t_start > kWaitLimitNs) {
+                  ok = 0;
+                  break;
+                }
+                w = ld_relaxed(ws.res(grp, par));
+              }
+            }
+            acquired = true;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            const uint32_t wi = (uint32_t)(__shfl_sync(0xffffffffu, w, 0) >> 2) & IDX_NONE;
+            bi = wi == IDX_NONE ? 0x7FFFFFFF : (int)wi;
           }
-          if (lane == 0) s_bi = bi;
+          ++epoch;
         }
-        ++epoch;
-        __syncthreads();
+        // the child of cur that carries y = bi
+        int nx = 0x7FFFFFFF;
+#pragma unroll
+        for (int j = 0; j < NODE_SLOTS; ++j) {
+          const unsigned hit = __ballot_sync(0xffffffffu, par_r[j] == cur && tok_r[j] == bi && j * 32 + lane >= 1);
+          if (hit && nx == 0x7FFFFFFF) nx = j * 32 + __ffs(hit) - 1;
+        }
+        if (lane == 0) {
+          s_next = nx;
+          s_ok = ok;
+          if (c == 0 && ok) {
+            p.path_nodes[(size_t)q * (p.L + 1) + step] = cur;
+            p.out_tokens[(size_t)q * (p.L + 1) + step] = bi;
+          }
+        }
       }
-      const int y = s_bi;
-      for (int i = 1 + tid; i < n; i += THREADS)
-        if (par_s[i] == cur && tok_s[i] == y) atomicMin(&s_next, i);
       __syncthreads();
-      if (c == 0 && tid == 0) {
-        p.path_nodes[(size_t)q * (p.L + 1) + step] = cur;
-        p.out_tokens[(size_t)q * (p.L + 1) + step] = y;
+      if (!s_ok) {
+        if (tid == 0) {
+          report(p.status, MFD_ERR_TIMEOUT);
+          if (c == 0) st_relaxed(ws.gen(grp), s_G);
+        }
+        return;
       }
       const int nx = s_next;
-      __syncthreads();
       if (nx == 0x7FFFFFFF || step == p.L) break;
       cur = nx;
       accepted = step + 1;
@@ -220,13 +407,24 @@ __global__ void __launch_bounds__(THREADS) verify_kernel(const Params p) {
         p.out_tokens[(size_t)q * (p.L + 1) + j] = -1;
       }
     }
-    __syncthreads();
   }
+  // the next call on this workspace uses the next generation
+  if (c == 0 && tid == 0 && epoch > 0) st_relaxed(ws.gen(grp), s_G);
 }
 
 }  // namespace
 
-int verify_max_grid(int n_sm) { return n_sm; }
+int verify_max_grid(int n_sm) { return n_sm < 256 ? n_sm : 256; }
+
+// CTAs per request group: enough that each CTA scans at least 1024 entries
+// of a row, at most the whole grid.
+static int verify_cpr(int grid, int n_req, int V) {
+  const int n_groups = n_req < grid ? n_req : grid;
+  int cpr = grid / n_groups;
+  const int want = (V + 1023) / 1024;
+  if (want < cpr) cpr = want;
+  return cpr < 1 ? 1 : cpr;
+}
 
 cudaError_t launch_verify(const VerifyLaunch &V, cudaStream_t stream) {
   Params p;
@@ -244,13 +442,21 @@ cudaError_t launch_verify(const VerifyLaunch &V, cudaStream_t stream) {
   p.path_nodes = V.path_nodes;
   p.out_tokens = V.out_tokens;
   p.status = V.status;
-  p.bar = V.bar;
-  p.part = V.part;
+  p.ws = V.ws;
+  p.cpr = verify_cpr(V.grid, V.n_req, V.V);
   const int n_groups = V.n_req < V.grid ? V.n_req : V.grid;
-  p.cpr = V.grid / n_groups;
-  const int grid = n_groups * p.cpr;
-  void *args[] = {&p};
-  cudaError_t e = cudaLaunchCooperativeKernel((const void *)verify_kernel, dim3(grid), dim3(THREADS), args, 0, stream);
+  const int grid = (n_groups < V.grid / p.cpr ? n_groups : V.grid / p.cpr) * p.cpr;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, verify_kernel, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
