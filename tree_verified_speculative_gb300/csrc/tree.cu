@@ -43,6 +43,8 @@ constexpr int NWARPS = THREADS / 32;
 constexpr int MAX_PASSES = 64;
 constexpr int PLIST = 1024;     // parents listed for pair-parallel expansion
 constexpr int PAIR_MAX = 4096;  // (parent, rank) pairs expanded at once
+constexpr int MAX_GROUPS = 17;  // radix groups: one per mode, plus one across modes
+constexpr int RANK_ALL = 1024;  // candidates up to which every primary is ranked
 
 // Pool entry (16 bytes).  k0: row ranks of positions 1..12, 5 bits each,
 // position 1 highest (bits 59..55).  k1: depth at bits 4..0, positions
@@ -55,6 +57,7 @@ struct PE {
 static_assert(sizeof(PE) == 16, "pool entry");
 
 constexpr uint32_t K1_KEY = 0x01FFFFFFu;  // depth and positions 13..16
+constexpr uint32_t K1_OWNED = 1u << 29;   // the entry's mode owns its first token
 
 __device__ __forceinline__ void pk_set(uint64_t &k0, uint32_t &k1, int p, uint32_t s) {
   if (p <= 12) {
@@ -129,7 +132,7 @@ struct Params {
 };
 
 struct Layout {
-  size_t lp, tok, sig, inv, ent, nxt, flg, table, hist1, skk, sel, prim, hslot, nodeid, par, nslot, plist, total;
+  size_t lp, tok, sig, inv, ent, nxt, flg, table, hist1, skk, ra, sel, prim, hslot, nodeid, par, nslot, plist, total;
 };
 
 __host__ __device__ inline size_t al16(size_t o) { return (o + 15) & ~(size_t)15; }
@@ -138,19 +141,21 @@ __host__ __device__ inline Layout make_layout(int K, int L, int topk, int B, int
   Layout y;
   size_t o = 0;
   const size_t klt = (size_t)K * L * topk;
-  const size_t hist = (size_t)16 * 256 * 4, tbl = al16((size_t)tsize * 4) + (size_t)tsize * 8;
+  const size_t hist = (size_t)2 * MAX_GROUPS * 256 * 4, tbl = (size_t)tsize * 14;
   y.ent = o;
   o += (size_t)cap * 16;
   y.table = o = al16(o);  // hash tags then best entries; the radix histograms overlay it
   o += hist > tbl ? hist : tbl;
   y.hist1 = o = al16(o);
-  o += 256 * 4;
+  o += 2 * 256 * 4;
   y.lp = o = al16(o);
   o += klt * 4;
   y.tok = o = al16(o);
   o += klt * 4;
   y.skk = o = al16(o);
-  o += (size_t)(nc + 4) * 4;  // padded to whole 16-byte words
+  o += (size_t)(nc + 32) * 4;  // padded to whole runs of 32
+  y.ra = o = al16(o);
+  o += (size_t)(nc + 32) * 2;
   y.sel = o = al16(o);
   o += (size_t)nc * 2;
   y.hslot = o = al16(o);
@@ -178,9 +183,12 @@ __host__ __device__ inline Layout make_layout(int K, int L, int topk, int B, int
 }
 
 struct Shared {
-  int n_ent, overflow, any, bad, coll, n_prim, n_sel, has_tau, n_par, wsum[NWARPS];
-  int cnt[16], act[16], rem[16], ntie[16];
-  uint32_t pre[16], tau;
+  int n_ent, overflow, any, refine, bad, coll, n_prim, n_sel, has_tau, n_par, n_out, n_in, wbad[NWARPS];
+  int cnt[MAX_GROUPS], act[MAX_GROUPS], rem[MAX_GROUPS], ntie[MAX_GROUPS];
+  uint8_t u1[512];  // per first-row entry: its mode owns its token
+  int f1[16], f2[16];
+  uint32_t kmin, kmax;
+  uint32_t pre[MAX_GROUPS], tau;
 };
 
 struct Ctx {
@@ -218,36 +226,47 @@ __device__ __forceinline__ uint64_t seq_hash(const Ctx &c, const PE &e, int d, u
 // among ent[0, n): digits of the B-th best score key, most significant
 // first, over `passes` 8-bit passes.  Leaves sh.act[g], sh.pre[g] (the digits
 // found, low bits zero), sh.rem[g] (rank of the B-th within that prefix) and
-// sh.ntie[g] (members sharing the prefix).
-template <typename GroupFn>
-__device__ void radix_bound(Shared &sh, const PE *ent, int n, int G, int B, int passes, int *hist, GroupFn grp) {
+// sh.ntie[g] (members sharing the prefix).  With fold_tau, also the smallest
+// bound over the groups, pre[g] with the undetermined low bits set, in
+// sh.tau (sh.has_tau = 0 when no group has B members).  hA and hB hold G * 256
+// counters each; a pass counts into one while the other is cleared.  An
+// entry belongs to group grp(i) and, when grp2(i) >= 0, also to grp2(i).
+template <typename GroupFn, typename Group2Fn>
+__device__ void radix_bound(Shared &sh, const PE *ent, int n, int G, int B, int passes, int *hA, int *hB,
+                            bool fold_tau, GroupFn grp, Group2Fn grp2) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid < 16) {
+  if (tid < MAX_GROUPS) {
     sh.pre[tid] = 0;
     sh.rem[tid] = B;
     sh.ntie[tid] = 0;
     sh.act[tid] = tid < G;  // until the first pass has counted the group
   }
-  for (int i = tid; i < G * 256; i += THREADS) hist[i] = 0;
+  if (fold_tau && tid == 0) {
+    sh.tau = 0xFFFFFFFFu;
+    sh.has_tau = 0;
+  }
+  for (int i = tid; i < G * 256; i += THREADS) hA[i] = 0;
   __syncthreads();
   for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
-    if (pass > 0) {
-      for (int i = tid; i < G * 256; i += THREADS) hist[i] = 0;
-      __syncthreads();
-    }
+    int *hist = (pass & 1) ? hB : hA;
+    int *next = (pass & 1) ? hA : hB;
     for (int base = warp * 32; base < n; base += THREADS) {
       const int i = base + lane;
-      int bin = -1;
+      int bin = -1, bin2 = -1;
       if (i < n) {
-        const int g = grp(i);
-        if (g >= 0 && sh.act[g]) {
-          const uint32_t sk = desc_key(ent[i].score);
-          if (pass == 0 || (sk >> (shift + 8)) == (sh.pre[g] >> (shift + 8))) bin = g * 256 + (int)((sk >> shift) & 255u);
-        }
+        const uint32_t sk = desc_key(ent[i].score);
+        const int g = grp(i), g2 = grp2(i);
+        if (g >= 0 && sh.act[g] && (pass == 0 || (sk >> (shift + 8)) == (sh.pre[g] >> (shift + 8))))
+          bin = g * 256 + (int)((sk >> shift) & 255u);
+        if (g2 >= 0 && sh.act[g2] && (pass == 0 || (sk >> (shift + 8)) == (sh.pre[g2] >> (shift + 8))))
+          bin2 = g2 * 256 + (int)((sk >> shift) & 255u);
       }
       warp_hist_add(hist, bin);
+      if (__any_sync(0xffffffffu, bin2 >= 0)) warp_hist_add(hist, bin2);
     }
+    if (pass + 1 < passes)
+      for (int i = tid; i < G * 256; i += THREADS) next[i] = 0;
     __syncthreads();
     for (int g = warp; g < G; g += NWARPS) {
       if (!sh.act[g]) continue;
@@ -266,12 +285,18 @@ __device__ void radix_bound(Shared &sh, const PE *ent, int n, int G, int B, int 
         }
       }
       const int rem = sh.rem[g];
+      // exactly one (lane, bin) holds the rem-th member
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
         if (run < rem && rem <= run + c[b]) {
-          sh.pre[g] |= (uint32_t)(lane * 8 + b) << shift;
+          const uint32_t pre = sh.pre[g] | ((uint32_t)(lane * 8 + b) << shift);
+          sh.pre[g] = pre;
           sh.rem[g] = rem - run;
           sh.ntie[g] = c[b];
+          if (fold_tau && pass + 1 == passes) {
+            atomicMin(&sh.tau, pre | (passes >= 4 ? 0u : (0xFFFFFFFFu >> (8 * passes))));
+            sh.has_tau = 1;
+          }
         }
         run += c[b];
       }
@@ -280,39 +305,43 @@ __device__ void radix_bound(Shared &sh, const PE *ent, int n, int G, int B, int 
   }
 }
 
-// In-place stable compaction of ent/nxt[0, n) to the entries with keep(i).
+// In-place compaction of ent/nxt[0, n) to the entries with keep(e, i), order
+// not kept.  Batches of THREADS * STAGE entries: every thread holds its
+// entries of the batch in registers across a barrier, then appends the kept
+// ones; a batch's writes land below the end of the batch, and the next
+// batch's sources lie beyond it, so no entry is overwritten before it is read.
+constexpr int STAGE = 6;
 template <typename KeepFn>
-__device__ int block_compact(Shared &sh, PE *ent, uint8_t *nxt, int n, KeepFn keep) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int out = 0;
-  for (int base = 0; base < n; base += THREADS) {
-    const int i = base + tid;
-    PE e;
-    uint8_t nx = 0;
-    bool kp = false;
-    if (i < n) {
-      e = ent[i];
-      nx = nxt[i];
-      kp = keep(i);
+__device__ int compact_pool(Shared &sh, PE *ent, uint8_t *nxt, int n, KeepFn keep) {
+  const int tid = threadIdx.x;
+  if (tid == 0) sh.n_out = 0;
+  for (int b0 = 0; b0 < n; b0 += THREADS * STAGE) {
+    PE e[STAGE];
+    uint8_t nx[STAGE];
+    bool kp[STAGE];
+#pragma unroll
+    for (int j = 0; j < STAGE; ++j) {
+      const int i = b0 + tid + j * THREADS;
+      kp[j] = false;
+      if (i < n) {
+        e[j] = ent[i];
+        nx[j] = nxt[i];
+        kp[j] = keep(e[j], i);
+      }
     }
-    const unsigned m = __ballot_sync(0xffffffffu, kp);
-    if (lane == 0) sh.wsum[warp] = __popc(m);
     __syncthreads();
-    int woff = 0, tot = 0;
-    for (int w = 0; w < NWARPS; ++w) {
-      const int v = sh.wsum[w];
-      woff += w < warp ? v : 0;
-      tot += v;
+#pragma unroll
+    for (int j = 0; j < STAGE; ++j) {
+      if (!__any_sync(0xffffffffu, kp[j])) continue;
+      const int slot = warp_append(&sh.n_out, kp[j]);
+      if (kp[j]) {
+        ent[slot] = e[j];
+        nxt[slot] = nx[j];
+      }
     }
-    if (kp) {
-      const int d = out + woff + __popc(m & lanemask_lt());
-      ent[d] = e;
-      nxt[d] = nx;
-    }
-    out += tot;
-    __syncthreads();
   }
-  return out;
+  __syncthreads();
+  return sh.n_out;
 }
 
 __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm) {
@@ -332,10 +361,13 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   uint8_t *flg = smem + lay.flg;
   int *hist1 = reinterpret_cast<int *>(smem + lay.hist1);
   uint32_t *tag = reinterpret_cast<uint32_t *>(smem + lay.table);
-  uint64_t *best = reinterpret_cast<uint64_t *>(smem + lay.table + al16((size_t)tsize * 4));
+  uint32_t *bkey = tag + tsize;  // per slot: best score key, then (mode << 16 | entry) among those
+  uint32_t *bsub = bkey + tsize;
+  uint16_t *rep = reinterpret_cast<uint16_t *>(bsub + tsize);
   int *hist = reinterpret_cast<int *>(smem + lay.table);
   uint32_t *skk = reinterpret_cast<uint32_t *>(smem + lay.skk);
   uint16_t *sel = reinterpret_cast<uint16_t *>(smem + lay.sel);
+  uint16_t *ra = reinterpret_cast<uint16_t *>(smem + lay.ra);
   uint16_t *hslot = reinterpret_cast<uint16_t *>(smem + lay.hslot);
   int16_t *nodeid = reinterpret_cast<int16_t *>(smem + lay.nodeid);
   uint8_t *prim = smem + lay.prim;
@@ -349,79 +381,248 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   pdl_launch_dependents();
 
   // ---------------------------------------------------- tables and checks
-  if (tid == 0) {
-    sh.bad = 0;
-    sh.n_ent = 0;
-  }
-  __syncthreads();
-  for (int e = tid; e < KLT; e += THREADS) {
-    const float v = glp[e];
-    lp_s[e] = v;
-    tok_s[e] = gtk[e];
-    const int j = e % topk;
-    if (isnan(v) || v > 0.f || (j > 0 && !(glp[e - 1] >= v))) sh.bad = 1;
-  }
-  __syncthreads();
-  for (int e = tid; e < KLT; e += THREADS) {
-    const int j = e % topk, row = e - j;
-    const uint32_t me = (uint32_t)tok_s[e];
-    int s = 0, dup = 0;
-    for (int f = 0; f < topk; ++f) {
-      const uint32_t o = (uint32_t)tok_s[row + f];
-      s += o < me;
-      dup += (o == me) && f != j;
+  // One row per segment of SEG lanes (SEG = topk rounded up to a power of
+  // two): every lane holds one entry, checks it against its left neighbour
+  // (sorted, <= 0, not NaN) and counts the row's smaller and equal tokens by
+  // shuffles.  All rows' loads go out before any is used.
+  {
+    int SEG = 1;
+    while (SEG < topk) SEG <<= 1;
+    const int rows = K * L, spw = 32 / SEG;  // rows per warp per round
+    const int seg = lane / SEG, j = lane - seg * SEG;
+    constexpr int RMAX = 16;                 // rounds: K * L <= 256 rows, 16 warps, >= 1 row a warp
+    float v[RMAX];
+    int tk[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      const int row = (r * NWARPS + warp) * spw + seg;
+      v[r] = -INFINITY;
+      tk[r] = 0;
+      if (row < rows && j < topk) {
+        v[r] = glp[row * topk + j];
+        tk[r] = gtk[row * topk + j];
+      }
     }
-    if (dup) sh.bad = 1;
-    sig_s[e] = (uint8_t)s;
-    inv_s[row + s] = (uint8_t)j;
+    if (tid == 0) sh.n_ent = 0;
+    bool bad = false;
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      const int row0 = (r * NWARPS + warp) * spw;
+      if (row0 >= rows) break;  // warp-uniform
+      const int row = row0 + seg;
+      const bool in = row < rows && j < topk;
+      const float prev = __shfl_up_sync(0xffffffffu, v[r], 1, SEG);
+      const uint32_t me = (uint32_t)tk[r];
+      int sm = 0, dup = 0;
+      for (int f = 0; f < topk; ++f) {
+        const uint32_t o = (uint32_t)__shfl_sync(0xffffffffu, tk[r], f, SEG);
+        sm += o < me;
+        dup += o == me;
+      }
+      if (in) {
+        bad |= isnan(v[r]) || v[r] > 0.f || (j > 0 && !(prev >= v[r])) || dup != 1;
+        const int e = row * topk + j;
+        lp_s[e] = v[r];
+        tok_s[e] = tk[r];
+        sig_s[e] = (uint8_t)sm;
+        inv_s[row * topk + sm] = (uint8_t)j;
+      }
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) sh.wbad[warp] = bad;
   }
   __syncthreads();
-  if (sh.bad) {
-    if (tid == 0) report(prm.status, MFD_ERR_INPUT);
-    return;
+  {
+    int any_bad = 0;
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) any_bad |= sh.wbad[w];
+    if (any_bad) {
+      if (tid == 0) report(prm.status, MFD_ERR_INPUT);
+      return;
+    }
   }
   const Ctx c{lp_s, tok_s, sig_s, inv_s, K, L, topk};
   auto mode_of = [&](int i) { return pk_mode(ent[i].k1); };
 
   // ---------------------------------------------------- depth-1 entries
-  for (int base = warp * 32; base < K * topk; base += THREADS) {
-    const int e = base + lane;
-    const int k = e / topk, j = e - (e / topk) * topk;
-    const bool ok = e < K * topk && lp_s[(k * L) * topk + j] > -INFINITY;
-    const int slot = warp_append(&sh.n_ent, ok);
-    if (ok) {
-      PE en;
-      en.score = lp_s[(k * L) * topk + j];
-      en.k0 = 0;
-      en.k1 = 1u | ((uint32_t)k << 25);
-      pk_set(en.k0, en.k1, 1, sig_s[(k * L) * topk + j]);
-      ent[slot] = en;
-      nxt[slot] = 0;
+  // Ownership: every first-row token is owned by one mode, the one with the
+  // best value for it (smallest mode on ties).  Prefixes whose first token
+  // their mode owns are pairwise distinct: two equal prefixes share their
+  // first token, hence its owner, hence their mode.
+  // With no bound possible yet (every mode holds only its topk first
+  // entries), depth 2 is generated at once when it fits.
+  const bool two = L >= 2 && topk < B && K * topk * (1 + topk) <= CAP;
+  {
+    // T1 threads per first-row entry look for its token in the other modes'
+    // first rows, each through every T1-th mode
+    const int n1 = K * topk;
+    int T1 = 1;
+    while (T1 < 32 && n1 * T1 * 2 <= THREADS) T1 <<= 1;
+    for (int base = warp * 32; base < n1 * T1; base += THREADS) {
+      const int x = base + lane;
+      const int e = x / T1, part = x - e * T1;
+      const bool in = e < n1;
+      const int k = in ? e / topk : 0, j = in ? e - k * topk : 0;
+      const int tkn = in ? tok_s[(k * L) * topk + j] : 0;
+      const float v = in ? lp_s[(k * L) * topk + j] : 0.f;
+      bool beaten = false;
+      if (in)
+        for (int k2 = part; k2 < K; k2 += T1) {
+          if (k2 == k) continue;
+          const int32_t *row = tok_s + (k2 * L) * topk;
+          const float *lrow = lp_s + (k2 * L) * topk;
+          for (int j2 = 0; j2 < topk; ++j2)
+            beaten |= row[j2] == tkn && (lrow[j2] > v || (lrow[j2] == v && k2 < k));
+        }
+      for (int o = T1 / 2; o > 0; o >>= 1) beaten |= __shfl_xor_sync(0xffffffffu, (int)beaten, o) != 0;
+      if (in && part == 0) sh.u1[e] = beaten ? 0 : 1;
+    }
+    // finite entries of each mode's first two rows (the rows are sorted, so
+    // they come first)
+    if (warp < K) {
+      const bool f1 = lane < topk && lp_s[(warp * L) * topk + lane] > -INFINITY;
+      const bool f2 = lane < topk && L >= 2 && lp_s[(warp * L + 1) * topk + lane] > -INFINITY;
+      const int c1 = __popc(__ballot_sync(0xffffffffu, f1)), c2 = __popc(__ballot_sync(0xffffffffu, f2));
+      if (lane == 0) {
+        sh.f1[warp] = c1;
+        sh.f2[warp] = c2;
+      }
     }
   }
   __syncthreads();
+  {
+    // fixed slots, mode-major: depth 1 first, then depth 2
+    int N1 = 0, N2 = 0;
+    for (int k = 0; k < K; ++k) {
+      N1 += sh.f1[k];
+      N2 += sh.f1[k] * sh.f2[k];
+    }
+    if (!two) N2 = 0;
+    for (int x = tid; x < N1; x += THREADS) {
+      int k = 0, off = 0;
+      while (x - off >= sh.f1[k]) off += sh.f1[k++];
+      const int j = x - off, e = (k * L) * topk + j;
+      PE en;
+      en.score = lp_s[e];
+      en.k0 = 0;
+      en.k1 = 1u | ((uint32_t)k << 25) | (sh.u1[k * topk + j] ? K1_OWNED : 0u);
+      pk_set(en.k0, en.k1, 1, sig_s[e]);
+      ent[x] = en;
+      nxt[x] = two ? (uint8_t)topk : 0;
+    }
+    for (int x = tid; x < N2; x += THREADS) {
+      int k = 0, off = 0;
+      while (x - off >= sh.f1[k] * sh.f2[k]) {
+        off += sh.f1[k] * sh.f2[k];
+        ++k;
+      }
+      const int r = x - off, f2 = sh.f2[k];
+      const int a = r / f2, b2 = r - a * f2;
+      const int ea = (k * L) * topk + a, eb = (k * L + 1) * topk + b2;
+      PE en;
+      en.score = __fadd_rn(lp_s[ea], lp_s[eb]);
+      en.k0 = 0;
+      en.k1 = 2u | ((uint32_t)k << 25) | (sh.u1[k * topk + a] ? K1_OWNED : 0u);
+      pk_set(en.k0, en.k1, 1, sig_s[ea]);
+      pk_set(en.k0, en.k1, 2, sig_s[eb]);
+      ent[N1 + x] = en;
+      nxt[N1 + x] = 0;
+    }
+    if (tid == 0) sh.n_ent = N1 + N2;
+  }
+  __syncthreads();
 
-  // the best (smallest) per-mode bound into sh.tau / sh.has_tau
-  auto set_tau = [&](int passes) {
-    radix_bound(sh, ent, sh.n_ent, K, B, passes, hist, mode_of);
+  // The bound: the B-th best score key among the owned entries (distinct
+  // prefixes, each scoring no better than its mixture score), found to 8
+  // bits below the highest bit where the owned keys differ, rounded to the
+  // worse end of its bin.  sh.has_tau = 0 while fewer than B entries are owned.
+  auto no_group = [](int) { return -1; };
+  auto set_tau = [&]() {
     if (tid == 0) {
-      uint32_t t = 0xFFFFFFFFu;
-      int h = 0;
-      for (int k = 0; k < K; ++k)
-        if (sh.act[k]) {
-          const uint32_t tk = sh.pre[k] | (passes >= 4 ? 0u : (0xFFFFFFFFu >> (8 * passes)));
-          if (!h || tk < t) t = tk;
-          h = 1;
-        }
-      sh.tau = t;
-      sh.has_tau = h;
+      sh.kmin = 0xFFFFFFFFu;
+      sh.kmax = 0u;
+      sh.tau = 0xFFFFFFFFu;
+      sh.has_tau = 0;
+    }
+    if (tid < 256) hist[tid] = 0;
+    const int n = sh.n_ent;
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;  // over the owned entries
+    for (int i = tid; i < n; i += THREADS) {
+      const PE e = ent[i];
+      if (e.k1 & K1_OWNED) {
+        const uint32_t k = desc_key(e.score);
+        lo = min(lo, k);
+        hi = max(hi, k);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
     }
     __syncthreads();
+    if (lane == 0 && lo <= hi) {
+      atomicMin(&sh.kmin, lo);
+      atomicMax(&sh.kmax, hi);
+    }
+    __syncthreads();
+    const uint32_t kmin = sh.kmin, kmax = sh.kmax;
+    const int hb = (kmin ^ kmax) ? 31 - __clz((int)(kmin ^ kmax)) : 0;
+    // digits of 8 bits from the highest differing bit down; a second digit
+    // only when the first leaves many entries in the boundary bin
+    int shift = hb > 7 ? hb - 7 : 0;
+    uint32_t prefix = shift + 8 >= 32 ? 0u : (kmin >> (shift + 8)) << (shift + 8);
+    for (int digit = 0; digit < 2; ++digit) {
+      const uint32_t hi_mask = shift + 8 >= 32 ? 0u : ~((1u << (shift + 8)) - 1u);
+      for (int base = warp * 32; base < n; base += THREADS) {
+        const int i = base + lane;
+        int bin = -1;
+        if (i < n) {
+          const PE e = ent[i];
+          const uint32_t k = desc_key(e.score);
+          if ((e.k1 & K1_OWNED) && (k & hi_mask) == prefix) bin = (int)((k >> shift) & 255u);
+        }
+        warp_hist_add(digit ? hist + 256 : hist, bin);
+      }
+      if (digit == 0 && tid < 256) hist[256 + tid] = 0;
+      __syncthreads();
+      if (warp == 0) {
+        const int *h = digit ? hist + 256 : hist;
+        const int need = digit ? sh.rem[0] : B;
+        int c8[8], sum = 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          c8[b] = h[lane * 8 + b];
+          sum += c8[b];
+        }
+        int run = warp_excl_scan(sum, lane);
+        const int total = __shfl_sync(0xffffffffu, run + sum, 31);
+        if (lane == 0) sh.refine = 0;
+        if (total >= need) {
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            if (run < need && need <= run + c8[b]) {
+              const uint32_t pre = prefix | ((uint32_t)(lane * 8 + b) << shift);
+              sh.tau = pre | ((1u << shift) - 1u);
+              sh.has_tau = 1;
+              sh.pre[0] = pre;
+              sh.rem[0] = need - run;
+              sh.refine = c8[b] > 64 && shift > 0;
+            }
+            run += c8[b];
+          }
+        }
+      }
+      __syncthreads();
+      if (!sh.refine) break;
+      prefix = sh.pre[0];
+      shift = shift > 8 ? shift - 8 : 0;
+    }
   };
 
   // prune to each mode's exact B best (only when the pool is full)
   auto prune_exact = [&]() {
-    radix_bound(sh, ent, sh.n_ent, K, B, 4, hist, mode_of);
+    radix_bound(sh, ent, sh.n_ent, K, B, 4, hist, hist + MAX_GROUPS * 256, false, mode_of, no_group);
     const int n = sh.n_ent;
     // among a mode's entries tied at its B-th score, keep the first rem[k]
     // in token order; decided for every entry before any entry moves
@@ -446,24 +647,31 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       flg[i] = kp;
     }
     __syncthreads();
-    const int out = block_compact(sh, ent, nxt, n, [&](int i) { return flg[i] != 0; });
+    const int out = compact_pool(sh, ent, nxt, n, [&](const PE &, int i) { return flg[i] != 0; });
     if (tid == 0) sh.n_ent = out;
     __syncthreads();
   };
 
   // ---------------------------------------------------- level expansion
   bool failed = false, tau_current = false;
-  for (int t = 1; t < L && !failed; ++t) {
+  for (int t = two ? 2 : 1; t < L && !failed; ++t) {
     if (tid == 0) sh.any = 0;
     int pass = 0;
     for (; pass < MAX_PASSES; ++pass) {
+      int n_pool = -1;
       if (t == 1 && pass == 0 && topk < B) {
         if (tid == 0) sh.has_tau = 0;  // each mode holds only its topk depth-1 entries
       } else {
-        set_tau(2);
+        set_tau();
+        if (sh.has_tau) {
+          // entries outside the bound can neither be in the tree nor lead to it
+          const uint32_t tau = sh.tau;
+          n_pool = compact_pool(sh, ent, nxt, sh.n_ent, [&](const PE &e, int) { return desc_key(e.score) <= tau; });
+        }
       }
       tau_current = true;
       if (tid == 0) {
+        if (n_pool >= 0) sh.n_ent = n_pool;
         sh.overflow = 0;
         sh.n_par = 0;
       }
@@ -477,7 +685,13 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         bool isp = false;
         if (i < n0) {
           const PE e = ent[i];
-          isp = pk_depth(e.k1) == t && nxt[i] < topk && (!ht || desc_key(e.score) <= tau);
+          const int j = nxt[i];
+          if (pk_depth(e.k1) == t && j < topk) {
+            // the next rank is the best remaining child: if it misses the
+            // bound, so do the others
+            const float lv = lp_s[(pk_mode(e.k1) * L + t) * topk + j];
+            isp = lv > -INFINITY && (!ht || desc_key(__fadd_rn(e.score, lv)) <= tau);
+          }
         }
         const int k = warp_append(&sh.n_par, isp);
         if (isp && k < PLIST) plist[k] = (uint16_t)i;
@@ -584,13 +798,14 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   }
 
   // ---------------------------------------------------- candidates
-  if (!tau_current) set_tau(2);  // else: nothing was added since the last bound
-  {
-    const bool ht = sh.has_tau;
-    const uint32_t tau = sh.tau;
-    const int n = block_compact(sh, ent, nxt, sh.n_ent, [&](int i) { return !ht || desc_key(ent[i].score) <= tau; });
-    if (tid == 0) sh.n_ent = n;
-    __syncthreads();
+  if (!tau_current) {  // else: the pool was cut to the bound and nothing was added since
+    set_tau();
+    if (sh.has_tau) {
+      const uint32_t tau = sh.tau;
+      const int n = compact_pool(sh, ent, nxt, sh.n_ent, [&](const PE &e, int) { return desc_key(e.score) <= tau; });
+      if (tid == 0) sh.n_ent = n;
+      __syncthreads();
+    }
   }
   if (sh.n_ent > NC) {  // many ties within the bound: keep each mode's exact B best
     prune_exact();
@@ -602,31 +817,48 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   const int n = sh.n_ent;
 
   // ---------------------------------------------------- one entry per prefix
+  // Open addressing on the sequence hash: a slot's tag is claimed by CAS
+  // (read first), its first claimant is the representative every other entry
+  // of the slot is compared with (a different sequence is a collision: the
+  // table is rebuilt with another seed), and the best (score key, then mode)
+  // of the slot is found by two 32-bit atomicMins.
   uint64_t seed = 0;
   for (int attempt = 0; attempt < 4; ++attempt) {
     for (int s = tid; s < tsize; s += THREADS) {
       tag[s] = 0;
-      best[s] = ~0ull;
+      bkey[s] = 0xFFFFFFFFu;
+      bsub[s] = 0xFFFFFFFFu;
     }
     if (tid == 0) sh.coll = 0;
     __syncthreads();
     for (int i = tid; i < n; i += THREADS) {
-      const uint64_t h = seq_hash(c, ent[i], pk_depth(ent[i].k1), seed);
+      const PE e = ent[i];
+      const uint64_t h = seq_hash(c, e, pk_depth(e.k1), seed);
       const uint32_t tg = (uint32_t)(h >> 32) | 1u;
       uint32_t s = (uint32_t)h & (uint32_t)(tsize - 1);
       for (int probe = 0; probe < tsize; ++probe) {
-        const uint32_t prev = atomicCAS(&tag[s], 0u, tg);
-        if (prev == 0u || prev == tg) break;
+        const uint32_t t0 = tag[s];
+        if (t0 == tg) break;
+        if (t0 == 0u) {
+          const uint32_t prev = atomicCAS(&tag[s], 0u, tg);
+          if (prev == 0u) {
+            rep[s] = (uint16_t)i;
+            break;
+          }
+          if (prev == tg) break;
+        }
         s = (s + 1) & (uint32_t)(tsize - 1);
       }
       hslot[i] = (uint16_t)s;
-      const uint64_t packed = ((uint64_t)desc_key(ent[i].score) << 32) | ((uint64_t)pk_mode(ent[i].k1) << 16) | i;
-      atomicMin(reinterpret_cast<unsigned long long *>(&best[s]), (unsigned long long)packed);
+      atomicMin(&bkey[s], desc_key(e.score));
     }
     __syncthreads();
     for (int i = tid; i < n; i += THREADS) {
-      const int r = (int)(best[hslot[i]] & 0xFFFF);
-      if (r != i && seq_cmp(c, ent[i], ent[r]) != 0) sh.coll = 1;
+      const PE e = ent[i];
+      const int s = hslot[i];
+      const int r = rep[s];
+      if (r != i && seq_cmp(c, e, ent[r]) != 0) sh.coll = 1;
+      if (desc_key(e.score) == bkey[s]) atomicMin(&bsub[s], ((uint32_t)pk_mode(e.k1) << 16) | (uint32_t)i);
     }
     __syncthreads();
     if (!sh.coll) break;
@@ -638,65 +870,104 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     return;
   }
   for (int i = tid; i < n; i += THREADS) {
-    prim[i] = (int)(best[hslot[i]] & 0xFFFF) == i;
+    prim[i] = (int)(bsub[hslot[i]] & 0xFFFF) == i;
     nodeid[i] = -1;
   }
   __syncthreads();
 
   // ---------------------------------------------------- the B best prefixes
-  radix_bound(sh, ent, n, 1, B, 2, hist1, [&](int i) { return prim[i] ? 0 : -1; });
+  // With few candidates every primary is ranked; otherwise a radix bound on
+  // the primaries' score keys first leaves about B of them.
+  bool ht_sel = false;
+  uint32_t tau_sel = 0xFFFFFFFFu;
+  if (n > RANK_ALL) {
+    radix_bound(sh, ent, n, 1, B, 2, hist1, hist1 + 256, false, [&](int i) { return prim[i] ? 0 : -1; }, no_group);
+    ht_sel = sh.act[0];
+    tau_sel = sh.pre[0] | 0xFFFFu;
+  }
   if (tid == 0) sh.n_sel = 0;
   __syncthreads();
-  {
-    const bool ht = sh.act[0];
-    const uint32_t tau = sh.pre[0] | 0xFFFFu;
-    for (int base = warp * 32; base < n; base += THREADS) {
-      const int i = base + lane;
-      const bool in = i < n && prim[i] && (!ht || desc_key(ent[i].score) <= tau);
-      const int k = warp_append(&sh.n_sel, in);
-      if (in) {
-        sel[k] = (uint16_t)i;
-        skk[k] = desc_key(ent[i].score);
-      }
+  for (int base = warp * 32; base < n; base += THREADS) {
+    const int i = base + lane;
+    const bool in = i < n && prim[i] && (!ht_sel || desc_key(ent[i].score) <= tau_sel);
+    const int k = warp_append(&sh.n_sel, in);
+    if (in) {
+      sel[k] = (uint16_t)i;
+      skk[k] = desc_key(ent[i].score);
     }
   }
   __syncthreads();
   const int ns = sh.n_sel;
-  const int ns4 = (ns + 3) & ~3;
-  for (int b = ns + tid; b < ns4; b += THREADS) skk[b] = 0xFFFFFFFFu;  // never before a real key
+  const int nruns = (ns + 31) >> 5;
+  // rank of each selected prefix = how many others come before it.  Runs of
+  // 32 are sorted by (score key, selection index) in registers; a prefix's
+  // rank is its place in its run plus, per other run, the keys below its own
+  // (a branch-free binary search).  Equal keys of different prefixes are
+  // ordered by their token sequences instead, on a slow path.
+  for (int r = warp; r < nruns; r += NWARPS) {
+    const int a = r * 32 + lane;
+    uint32_t key = a < ns ? skk[a] : 0xFFFFFFFFu;
+    int ia = a;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const uint32_t ok = __shfl_xor_sync(0xffffffffu, key, j);
+        const int oi = __shfl_xor_sync(0xffffffffu, ia, j);
+        const bool other_less = ok < key || (ok == key && oi < ia);
+        const bool keep_min = ((lane & j) == 0) == ((lane & k) == 0);
+        if (keep_min == other_less) {
+          key = ok;
+          ia = oi;
+        }
+      }
+    }
+    skk[a] = key;
+    ra[a] = (uint16_t)ia;
+  }
   __syncthreads();
-  // rank of each selected prefix = how many others come before it: score
-  // keys first (four per load, two threads per prefix, each half of the
-  // keys), then token order for the rare equal scores
-  {
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(skk);
-    const int nw = ns4 >> 2, h4 = nw >> 1;  // words of four keys; the first half
-    for (int base = warp * 32; base < 2 * ns; base += THREADS) {
-      const int a2 = base + lane;
-      const bool valid = a2 < 2 * ns;
-      const int a = valid ? a2 >> 1 : 0, half = a2 & 1;
-      int lt = 0;
-      if (valid) {
-        const uint32_t ka = skk[a];
-        const int w0 = half ? h4 : 0, w1 = half ? nw : h4;
-        int eq = 0;
-        for (int w = w0; w < w1; ++w) {
-          const uint4 v = s4[w];
-          lt += (v.x < ka) + (v.y < ka) + (v.z < ka) + (v.w < ka);
-          eq += (v.x == ka) + (v.y == ka) + (v.z == ka) + (v.w == ka);
-        }
-        const int self = (a >= 4 * w0 && a < 4 * w1) ? 1 : 0;
-        if (eq > self) {  // another prefix has the same score key
-          const PE ea = ent[sel[a]];
-          for (int b = 4 * w0; b < 4 * w1 && b < ns; ++b)
-            if (b != a && skk[b] == ka && seq_cmp(c, ent[sel[b]], ea) < 0) ++lt;
+  for (int r = warp; r < nruns; r += NWARPS) {
+    const int pos = r * 32 + lane;
+    const uint32_t key = skk[pos];
+    const int ia = ra[pos];
+    const bool real = ia < ns;
+    int lt = lane;  // the run's entries before this one
+    bool tie = (__popc(__match_any_sync(0xffffffffu, key)) > 1) && real;
+    for (int r0 = 0; r0 < nruns; r0 += 4) {
+      // four independent searches in flight
+      int cnt[4] = {0, 0, 0, 0};
+      const uint32_t *run[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) run[u] = skk + (r0 + u < nruns ? r0 + u : r) * 32;
+#pragma unroll
+      for (int st = 16; st > 0; st >>= 1)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) cnt[u] += run[u][cnt[u] + st - 1] < key ? st : 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        cnt[u] += run[u][cnt[u]] < key ? 1 : 0;
+        if (r0 + u < nruns && r0 + u != r) {
+          lt += cnt[u];
+          tie |= cnt[u] < 32 && run[u][cnt[u]] == key;
         }
       }
-      lt += __shfl_xor_sync(0xffffffffu, lt, 1);
-      if (valid && half == 0 && lt < B) {
-        nslot[lt + 1] = sel[a];
-        nodeid[sel[a]] = (int16_t)(lt + 1);
+    }
+    if (real && tie) {
+      // keys below, then token order among the equal keys
+      lt = 0;
+      const PE ea = ent[sel[ia]];
+      for (int b = 0; b < nruns * 32; ++b) {
+        const uint32_t kb = skk[b];
+        if (kb < key) {
+          ++lt;
+        } else if (kb == key && ra[b] != ia && ra[b] < ns && seq_cmp(c, ent[sel[ra[b]]], ea) < 0) {
+          ++lt;
+        }
       }
+    }
+    if (real && lt < B) {
+      nslot[lt + 1] = sel[ia];
+      nodeid[sel[ia]] = (int16_t)(lt + 1);
     }
   }
   if (tid == 0) {
@@ -721,7 +992,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         const uint32_t t0 = tag[s];
         if (t0 == 0u) break;
         if (t0 == tg) {
-          const int r = (int)(best[s] & 0xFFFF);
+          const int r = (int)(bsub[s] & 0xFFFF);
           const PE g = ent[r];
           if (pk_depth(g.k1) == d - 1) {
             bool same = true;
