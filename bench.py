@@ -205,8 +205,10 @@ def run_gpu(args, ws, rank, local):
 
     def ahead(n):
         # untimed device work that keeps the GPU busy while the host enqueues
-        # the next rounds, so that no event interval contains a host gap
-        torch.cuda._sleep(int(n * 400_000))
+        # the next rounds, so that no event interval contains a host gap: about
+        # 0.5 ms a round, more than the host needs to enqueue one even when
+        # the host is busy with other work
+        torch.cuda._sleep(int(n * 1_000_000))
 
     # phase A: LM head + log-softmax + top-k, then the tree, for every round
     def phase_a(rounds_idx):
@@ -273,6 +275,8 @@ def run_gpu(args, ws, rank, local):
     st = int(rd.status.item())
     if st != 0:
         raise RuntimeError(f"device status {st}: {mfd.status_string(st)}")
+    med = {nm: round(float(np.median([ev[i][a].elapsed_time(ev[i][b]) for i in timed])) * 1e3, 2)
+           for nm, a, b in (("lmhead_topk", 0, 1), ("build_tree", 1, 2), ("verify", 3, 4))}
     lm = bd = vf = 0.0
     for i in timed:
         e0, ea, e1, s2, e3 = ev[i]
@@ -304,6 +308,7 @@ def run_gpu(args, ws, rank, local):
                    "timing": "sum of per-round CUDA-event intervals around the three calls, with the queue kept ahead of the GPU; the target plant (input generation that needs the round's tree) is untimed"},
         "stages_us": {"lmhead_topk": round(lm_us, 2), "build_tree": round(bd / steps * 1e3, 2),
                       "verify": round(vf / steps * 1e3, 2)},
+        "stages_us_median": med,
         "mean_accept_len": round(float(acc.mean()), 4),
         "roofline": {"kernel": "mfd_lmhead_topk (lmhead_topk_kernel + merge_topk_kernel)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
