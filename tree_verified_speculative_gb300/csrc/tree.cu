@@ -6,32 +6,33 @@
 //
 // One CTA (512 threads) builds one request's tree in shared memory.
 //
-// Entries.  The pool holds (mode, prefix) entries scored by their own mode.
-// Within one mode a prefix is a tuple of ranks, one per position; replacing
-// each rank by its token's rank inside that row (5 bits, token ids compared
-// unsigned) turns the lexicographic token order into an unsigned compare of
-// packed keys, depth last.  Across modes, prefixes are compared by their
-// token ids (looked up through the rows).
+// Entries.  The pool holds (mode, prefix) entries scored by their own mode;
+// a prefix is packed as its tuple of row ranks (5 bits a position, depth
+// last), and its tokens are read back through the rows.  Prefixes are
+// compared by their token ids (unsigned, a proper prefix first).
 //
-// Search, level by level.  A per-mode score bound tau_k -- a value with at
-// least B of mode k's entries scoring no worse -- comes from a two-digit
-// radix select on the score key.  Each mode's entries are distinct
-// prefixes and a prefix's mixture score is at least its mode score, so at
-// least B distinct prefixes score no worse than min_k tau_k: the tree's
-// cut-off is never worse, and every entry that can reach the tree, or lead
-// to it, scores within the bound.  Level t expands the depth-t entries in
-// rank order (child scores only fall) while the child is within the bound.
-// When the pool fills, it is pruned to each mode's exact B best (radix
-// select on the full score key, then the token order among equal scores)
-// and expansion resumes where each entry stopped.
+// The bound.  Every first-row token is owned by one mode; entries whose
+// first token their mode owns are pairwise distinct prefixes, and a prefix's
+// mixture score is at least its mode score.  So with tau the B-th best score
+// among the owned entries, at least B distinct prefixes score no worse than
+// tau: the tree's cut-off is never worse, and an entry scoring worse than tau
+// can neither be in the tree nor lead to it (scores only fall along a path).
+// tau is found by a radix select of one or two 8-bit digits below the
+// highest bit where the owned score keys differ, rounded to the worse end.
+//
+// Search, level by level.  Depth 1 and 2 are generated at once; then at
+// each level the pool is cut to the bound and the entries of that depth are
+// expanded in rank order (child scores only fall) while the child is within
+// the bound.  When the pool fills, it is pruned to each mode's exact B best
+// (radix select on the full score key, then the token order among equal
+// scores) and expansion resumes where each entry stopped.
 //
 // Result.  The entries within the final bound are hashed by token sequence;
 // a table keeps per sequence the entry with the best (score, smallest mode),
 // equality checked on the full sequence (a collision reseeds the table).
-// These primaries are distinct prefixes.  A radix bound over the primaries
-// leaves about B of them; rank counting among those gives both the B best
-// and their order.  Parents are looked up in the table by the hash of the
-// sequence without its last token.
+// These primaries are distinct prefixes.  Their order comes from runs of 32
+// sorted in registers and binary searches between the runs; a prefix's
+// parent is the table slot of its sequence without the last token.
 #include "lmhead.h"
 #include "mfd_device.cuh"
 
@@ -56,7 +57,6 @@ struct PE {
 };
 static_assert(sizeof(PE) == 16, "pool entry");
 
-constexpr uint32_t K1_KEY = 0x01FFFFFFu;  // depth and positions 13..16
 constexpr uint32_t K1_OWNED = 1u << 29;   // the entry's mode owns its first token
 
 __device__ __forceinline__ void pk_set(uint64_t &k0, uint32_t &k1, int p, uint32_t s) {
@@ -132,7 +132,8 @@ struct Params {
 };
 
 struct Layout {
-  size_t lp, tok, sig, inv, ent, nxt, flg, table, hist1, skk, ra, sel, prim, hslot, nodeid, par, nslot, plist, total;
+  size_t lp, tok, ent, nxt, flg, table, hist1, skk, ra, sel, prim, hslot, pslot, nodeid, par, nslot, plist,
+      total;
 };
 
 __host__ __device__ inline size_t al16(size_t o) { return (o + 15) & ~(size_t)15; }
@@ -154,11 +155,11 @@ __host__ __device__ inline Layout make_layout(int K, int L, int topk, int B, int
   o += klt * 4;
   y.skk = o = al16(o);
   o += (size_t)(nc + 32) * 4;  // padded to whole runs of 32
-  y.ra = o = al16(o);
-  o += (size_t)(nc + 32) * 2;
   y.sel = o = al16(o);
   o += (size_t)nc * 2;
-  y.hslot = o = al16(o);
+  y.hslot = y.ra = o = al16(o);  // hash slots die with the primaries; the rank's run order reuses them
+  o += (size_t)(nc + 32) * 2;
+  y.pslot = o = al16(o);
   o += (size_t)nc * 2;
   y.nodeid = o = al16(o);
   o += (size_t)nc * 2;
@@ -172,10 +173,6 @@ __host__ __device__ inline Layout make_layout(int K, int L, int topk, int B, int
   o += (size_t)cap;
   y.flg = o = al16(o);
   o += (size_t)cap;
-  y.sig = o = al16(o);
-  o += klt;
-  y.inv = o = al16(o);
-  o += klt;
   y.prim = o = al16(o);
   o += (size_t)nc;
   y.total = (o + 127) & ~(size_t)127;
@@ -187,6 +184,7 @@ struct Shared {
   int cnt[MAX_GROUPS], act[MAX_GROUPS], rem[MAX_GROUPS], ntie[MAX_GROUPS];
   uint8_t u1[512];  // per first-row entry: its mode owns its token
   int f1[16], f2[16];
+  float lo1[16], lo2[16];
   uint32_t kmin, kmax;
   uint32_t pre[MAX_GROUPS], tau;
 };
@@ -194,14 +192,13 @@ struct Shared {
 struct Ctx {
   const float *lp;
   const int32_t *tok;
-  const uint8_t *sig, *inv;
   int K, L, topk;
 };
 
 // token at position p (1-based) of an entry
 __device__ __forceinline__ uint32_t token_at(const Ctx &c, const PE &e, int p) {
   const int row = (pk_mode(e.k1) * c.L + p - 1) * c.topk;
-  return (uint32_t)c.tok[row + c.inv[row + pk_get(e.k0, e.k1, p)]];
+  return (uint32_t)c.tok[row + pk_get(e.k0, e.k1, p)];
 }
 
 // Token order of two prefixes of any modes (unsigned ids, a proper prefix
@@ -219,6 +216,18 @@ __device__ int seq_cmp(const Ctx &c, const PE &a, const PE &b) {
 __device__ __forceinline__ uint64_t seq_hash(const Ctx &c, const PE &e, int d, uint64_t seed) {
   uint64_t h = 0x2545F4914F6CDD1Dull ^ seed;
   for (int p = 1; p <= d; ++p) h = mix64(h ^ ((uint64_t)token_at(c, e, p) + ((uint64_t)p << 40)));
+  return h;
+}
+
+// The hash of the whole sequence and (in *hp) of the sequence without its
+// last token, which is the parent's hash.
+__device__ __forceinline__ uint64_t seq_hash2(const Ctx &c, const PE &e, int d, uint64_t seed, uint64_t *hp) {
+  uint64_t h = 0x2545F4914F6CDD1Dull ^ seed;
+  *hp = h;
+  for (int p = 1; p <= d; ++p) {
+    *hp = h;
+    h = mix64(h ^ ((uint64_t)token_at(c, e, p) + ((uint64_t)p << 40)));
+  }
   return h;
 }
 
@@ -354,8 +363,6 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   const Layout lay = make_layout(K, L, topk, B, CAP, NC, tsize);
   float *lp_s = reinterpret_cast<float *>(smem + lay.lp);
   int32_t *tok_s = reinterpret_cast<int32_t *>(smem + lay.tok);
-  uint8_t *sig_s = smem + lay.sig;
-  uint8_t *inv_s = smem + lay.inv;
   PE *ent = reinterpret_cast<PE *>(smem + lay.ent);
   uint8_t *nxt = smem + lay.nxt;
   uint8_t *flg = smem + lay.flg;
@@ -369,6 +376,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   uint16_t *sel = reinterpret_cast<uint16_t *>(smem + lay.sel);
   uint16_t *ra = reinterpret_cast<uint16_t *>(smem + lay.ra);
   uint16_t *hslot = reinterpret_cast<uint16_t *>(smem + lay.hslot);
+  uint16_t *pslot = reinterpret_cast<uint16_t *>(smem + lay.pslot);
   int16_t *nodeid = reinterpret_cast<int16_t *>(smem + lay.nodeid);
   uint8_t *prim = smem + lay.prim;
   int16_t *par_s = reinterpret_cast<int16_t *>(smem + lay.par);
@@ -382,50 +390,40 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
 
   // ---------------------------------------------------- tables and checks
   // One row per segment of SEG lanes (SEG = topk rounded up to a power of
-  // two): every lane holds one entry, checks it against its left neighbour
-  // (sorted, <= 0, not NaN) and counts the row's smaller and equal tokens by
-  // shuffles.  All rows' loads go out before any is used.
+  // two).  Every warp first copies its own rows to shared memory (all loads
+  // in flight at once), then checks them there: each entry against its left
+  // neighbour (sorted, <= 0, not NaN) and against the row's other tokens.
   {
     int SEG = 1;
     while (SEG < topk) SEG <<= 1;
     const int rows = K * L, spw = 32 / SEG;  // rows per warp per round
     const int seg = lane / SEG, j = lane - seg * SEG;
     constexpr int RMAX = 16;                 // rounds: K * L <= 256 rows, 16 warps, >= 1 row a warp
-    float v[RMAX];
-    int tk[RMAX];
 #pragma unroll
     for (int r = 0; r < RMAX; ++r) {
       const int row = (r * NWARPS + warp) * spw + seg;
-      v[r] = -INFINITY;
-      tk[r] = 0;
       if (row < rows && j < topk) {
-        v[r] = glp[row * topk + j];
-        tk[r] = gtk[row * topk + j];
+        lp_s[row * topk + j] = glp[row * topk + j];
+        tok_s[row * topk + j] = gtk[row * topk + j];
       }
     }
     if (tid == 0) sh.n_ent = 0;
+    if (tid < 512) hist[tid] = 0;  // the first bound's two digit histograms
+    __syncwarp();
     bool bad = false;
-#pragma unroll
+#pragma unroll 1
     for (int r = 0; r < RMAX; ++r) {
-      const int row0 = (r * NWARPS + warp) * spw;
-      if (row0 >= rows) break;  // warp-uniform
-      const int row = row0 + seg;
-      const bool in = row < rows && j < topk;
-      const float prev = __shfl_up_sync(0xffffffffu, v[r], 1, SEG);
-      const uint32_t me = (uint32_t)tk[r];
-      int sm = 0, dup = 0;
-      for (int f = 0; f < topk; ++f) {
-        const uint32_t o = (uint32_t)__shfl_sync(0xffffffffu, tk[r], f, SEG);
-        sm += o < me;
-        dup += o == me;
-      }
-      if (in) {
-        bad |= isnan(v[r]) || v[r] > 0.f || (j > 0 && !(prev >= v[r])) || dup != 1;
-        const int e = row * topk + j;
-        lp_s[e] = v[r];
-        tok_s[e] = tk[r];
-        sig_s[e] = (uint8_t)sm;
-        inv_s[row * topk + sm] = (uint8_t)j;
+      const int row = (r * NWARPS + warp) * spw + seg;
+      if (row < rows && j < topk) {
+        const float *lr = lp_s + row * topk;
+        const int32_t *tr = tok_s + row * topk;
+        const float v = lr[j];
+        const int32_t tk = tr[j];
+        bad |= isnan(v) || v > 0.f || (j > 0 && !(lr[j - 1] >= v));
+        int dup = 0;
+#pragma unroll 4
+        for (int f = 0; f < topk; ++f) dup += tr[f] == tk;
+        bad |= dup != 1;
       }
     }
     bad = __any_sync(0xffffffffu, bad);
@@ -441,7 +439,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       return;
     }
   }
-  const Ctx c{lp_s, tok_s, sig_s, inv_s, K, L, topk};
+  const Ctx c{lp_s, tok_s, K, L, topk};
   auto mode_of = [&](int i) { return pk_mode(ent[i].k1); };
 
   // ---------------------------------------------------- depth-1 entries
@@ -466,26 +464,43 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       const int tkn = in ? tok_s[(k * L) * topk + j] : 0;
       const float v = in ? lp_s[(k * L) * topk + j] : 0.f;
       bool beaten = false;
+      auto beats = [&](const float *lrow, int j2, int k2) { return lrow[j2] > v || (lrow[j2] == v && k2 < k); };
       if (in)
         for (int k2 = part; k2 < K; k2 += T1) {
           if (k2 == k) continue;
           const int32_t *row = tok_s + (k2 * L) * topk;
           const float *lrow = lp_s + (k2 * L) * topk;
-          for (int j2 = 0; j2 < topk; ++j2)
-            beaten |= row[j2] == tkn && (lrow[j2] > v || (lrow[j2] == v && k2 < k));
+          if ((topk & 3) == 0) {  // rows start on 16-byte boundaries
+#pragma unroll 2
+            for (int j4 = 0; j4 < topk; j4 += 4) {
+              const int4 t4 = *reinterpret_cast<const int4 *>(row + j4);
+              if (t4.x == tkn) beaten |= beats(lrow, j4, k2);
+              if (t4.y == tkn) beaten |= beats(lrow, j4 + 1, k2);
+              if (t4.z == tkn) beaten |= beats(lrow, j4 + 2, k2);
+              if (t4.w == tkn) beaten |= beats(lrow, j4 + 3, k2);
+            }
+          } else {
+            for (int j2 = 0; j2 < topk; ++j2)
+              if (row[j2] == tkn) beaten |= beats(lrow, j2, k2);
+          }
         }
       for (int o = T1 / 2; o > 0; o >>= 1) beaten |= __shfl_xor_sync(0xffffffffu, (int)beaten, o) != 0;
       if (in && part == 0) sh.u1[e] = beaten ? 0 : 1;
     }
     // finite entries of each mode's first two rows (the rows are sorted, so
     // they come first)
+    // and their extremes, which bound every depth-1 and depth-2 score
     if (warp < K) {
-      const bool f1 = lane < topk && lp_s[(warp * L) * topk + lane] > -INFINITY;
-      const bool f2 = lane < topk && L >= 2 && lp_s[(warp * L + 1) * topk + lane] > -INFINITY;
+      const float v1 = lane < topk ? lp_s[(warp * L) * topk + lane] : -INFINITY;
+      const float v2 = lane < topk && L >= 2 ? lp_s[(warp * L + 1) * topk + lane] : -INFINITY;
+      const bool f1 = v1 > -INFINITY, f2 = v2 > -INFINITY;
       const int c1 = __popc(__ballot_sync(0xffffffffu, f1)), c2 = __popc(__ballot_sync(0xffffffffu, f2));
+      const float lo1 = -warp_max(f1 ? -v1 : -INFINITY), lo2 = -warp_max(f2 ? -v2 : -INFINITY);
       if (lane == 0) {
         sh.f1[warp] = c1;
         sh.f2[warp] = c2;
+        sh.lo1[warp] = lo1;  // +inf when the row has no finite entry
+        sh.lo2[warp] = lo2;
       }
     }
   }
@@ -493,40 +508,87 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   {
     // fixed slots, mode-major: depth 1 first, then depth 2
     int N1 = 0, N2 = 0;
+    bool full = true;
+    float hi = -INFINITY, lo = INFINITY;  // bounds of every score generated here
     for (int k = 0; k < K; ++k) {
-      N1 += sh.f1[k];
-      N2 += sh.f1[k] * sh.f2[k];
+      const int f1 = sh.f1[k], f2 = sh.f2[k];
+      N1 += f1;
+      N2 += f1 * f2;
+      full &= f1 == topk && f2 == topk;
+      if (f1 > 0) {
+        hi = fmaxf(hi, lp_s[(k * L) * topk]);
+        lo = fminf(lo, sh.lo1[k]);
+        if (two && f2 > 0) lo = fminf(lo, __fadd_rn(sh.lo1[k], sh.lo2[k]));
+      }
     }
     if (!two) N2 = 0;
-    for (int x = tid; x < N1; x += THREADS) {
-      int k = 0, off = 0;
-      while (x - off >= sh.f1[k]) off += sh.f1[k++];
-      const int j = x - off, e = (k * L) * topk + j;
-      PE en;
-      en.score = lp_s[e];
-      en.k0 = 0;
-      en.k1 = 1u | ((uint32_t)k << 25) | (sh.u1[k * topk + j] ? K1_OWNED : 0u);
-      pk_set(en.k0, en.k1, 1, sig_s[e]);
-      ent[x] = en;
-      nxt[x] = two ? (uint8_t)topk : 0;
+    // the owned entries are counted into the first digit's histogram as they
+    // are made; the digit starts at the highest bit where the score keys of
+    // [lo, hi] differ
+    const uint32_t kmin = desc_key(hi), kmax = desc_key(lo);
+    const int hb = (kmin ^ kmax) ? 31 - __clz((int)(kmin ^ kmax)) : 0;
+    const int shift = hb > 7 ? hb - 7 : 0;
+    if (tid == 0) {
+      sh.kmin = kmin;
+      sh.kmax = kmax;
     }
-    for (int x = tid; x < N2; x += THREADS) {
-      int k = 0, off = 0;
-      while (x - off >= sh.f1[k] * sh.f2[k]) {
-        off += sh.f1[k] * sh.f2[k];
-        ++k;
+    const int TT = topk * topk;
+    for (int base = warp * 32; base < N1 + N2; base += THREADS) {
+      const int x = base + lane;
+      int bin = -1;
+      if (x < N1) {
+        int k, j;
+        if (full) {
+          k = x / topk;
+          j = x - k * topk;
+        } else {
+          int off = 0;
+          k = 0;
+          while (x - off >= sh.f1[k]) off += sh.f1[k++];
+          j = x - off;
+        }
+        const int e = (k * L) * topk + j;
+        PE en;
+        en.score = lp_s[e];
+        en.k0 = 0;
+        const bool own = sh.u1[k * topk + j];
+        en.k1 = 1u | ((uint32_t)k << 25) | (own ? K1_OWNED : 0u);
+        pk_set(en.k0, en.k1, 1, (uint32_t)j);
+        ent[x] = en;
+        nxt[x] = two ? (uint8_t)topk : 0;
+        if (own) bin = (int)((desc_key(en.score) >> shift) & 255u);
+      } else if (x < N1 + N2) {
+        const int y = x - N1;
+        int k, a, b2;
+        if (full) {
+          k = y / TT;
+          const int r = y - k * TT;
+          a = r / topk;
+          b2 = r - a * topk;
+        } else {
+          int off = 0;
+          k = 0;
+          while (y - off >= sh.f1[k] * sh.f2[k]) {
+            off += sh.f1[k] * sh.f2[k];
+            ++k;
+          }
+          const int r = y - off, f2 = sh.f2[k];
+          a = r / f2;
+          b2 = r - a * f2;
+        }
+        const int ea = (k * L) * topk + a, eb = (k * L + 1) * topk + b2;
+        PE en;
+        en.score = __fadd_rn(lp_s[ea], lp_s[eb]);
+        en.k0 = 0;
+        const bool own = sh.u1[k * topk + a];
+        en.k1 = 2u | ((uint32_t)k << 25) | (own ? K1_OWNED : 0u);
+        pk_set(en.k0, en.k1, 1, (uint32_t)a);
+        pk_set(en.k0, en.k1, 2, (uint32_t)b2);
+        ent[x] = en;
+        nxt[x] = 0;
+        if (own) bin = (int)((desc_key(en.score) >> shift) & 255u);
       }
-      const int r = x - off, f2 = sh.f2[k];
-      const int a = r / f2, b2 = r - a * f2;
-      const int ea = (k * L) * topk + a, eb = (k * L + 1) * topk + b2;
-      PE en;
-      en.score = __fadd_rn(lp_s[ea], lp_s[eb]);
-      en.k0 = 0;
-      en.k1 = 2u | ((uint32_t)k << 25) | (sh.u1[k * topk + a] ? K1_OWNED : 0u);
-      pk_set(en.k0, en.k1, 1, sig_s[ea]);
-      pk_set(en.k0, en.k1, 2, sig_s[eb]);
-      ent[N1 + x] = en;
-      nxt[N1 + x] = 0;
+      warp_hist_add(hist, bin);
     }
     if (tid == 0) sh.n_ent = N1 + N2;
   }
@@ -537,35 +599,41 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   // bits below the highest bit where the owned keys differ, rounded to the
   // worse end of its bin.  sh.has_tau = 0 while fewer than B entries are owned.
   auto no_group = [](int) { return -1; };
-  auto set_tau = [&]() {
+  // pre: the key range is in sh.kmin/kmax and the first digit's histogram
+  // was filled when the pool was generated.
+  auto set_tau = [&](bool pre) {
     if (tid == 0) {
-      sh.kmin = 0xFFFFFFFFu;
-      sh.kmax = 0u;
       sh.tau = 0xFFFFFFFFu;
       sh.has_tau = 0;
     }
-    if (tid < 256) hist[tid] = 0;
     const int n = sh.n_ent;
-    uint32_t lo = 0xFFFFFFFFu, hi = 0u;  // over the owned entries
-    for (int i = tid; i < n; i += THREADS) {
-      const PE e = ent[i];
-      if (e.k1 & K1_OWNED) {
-        const uint32_t k = desc_key(e.score);
-        lo = min(lo, k);
-        hi = max(hi, k);
+    if (!pre) {
+      if (tid == 0) {
+        sh.kmin = 0xFFFFFFFFu;
+        sh.kmax = 0u;
       }
-    }
+      if (tid < 256) hist[tid] = 0;
+      uint32_t lo = 0xFFFFFFFFu, hi = 0u;  // over the owned entries
+      for (int i = tid; i < n; i += THREADS) {
+        const PE e = ent[i];
+        if (e.k1 & K1_OWNED) {
+          const uint32_t k = desc_key(e.score);
+          lo = min(lo, k);
+          hi = max(hi, k);
+        }
+      }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      }
+      __syncthreads();
+      if (lane == 0 && lo <= hi) {
+        atomicMin(&sh.kmin, lo);
+        atomicMax(&sh.kmax, hi);
+      }
+      __syncthreads();
     }
-    __syncthreads();
-    if (lane == 0 && lo <= hi) {
-      atomicMin(&sh.kmin, lo);
-      atomicMax(&sh.kmax, hi);
-    }
-    __syncthreads();
     const uint32_t kmin = sh.kmin, kmax = sh.kmax;
     const int hb = (kmin ^ kmax) ? 31 - __clz((int)(kmin ^ kmax)) : 0;
     // digits of 8 bits from the highest differing bit down; a second digit
@@ -574,6 +642,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     uint32_t prefix = shift + 8 >= 32 ? 0u : (kmin >> (shift + 8)) << (shift + 8);
     for (int digit = 0; digit < 2; ++digit) {
       const uint32_t hi_mask = shift + 8 >= 32 ? 0u : ~((1u << (shift + 8)) - 1u);
+      if (!(pre && digit == 0)) {
       for (int base = warp * 32; base < n; base += THREADS) {
         const int i = base + lane;
         int bin = -1;
@@ -586,6 +655,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       }
       if (digit == 0 && tid < 256) hist[256 + tid] = 0;
       __syncthreads();
+      }
       if (warp == 0) {
         const int *h = digit ? hist + 256 : hist;
         const int need = digit ? sh.rem[0] : B;
@@ -639,7 +709,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
           for (int f = 0; f < n; ++f) {
             const PE g = ent[f];
             if (pk_mode(g.k1) != k || desc_key(g.score) != sh.pre[k]) continue;
-            r += (g.k0 < e.k0) || (g.k0 == e.k0 && (g.k1 & K1_KEY) < (e.k1 & K1_KEY));
+            r += seq_cmp(c, g, e) < 0;
           }
           kp = r <= sh.rem[k];
         }
@@ -662,7 +732,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       if (t == 1 && pass == 0 && topk < B) {
         if (tid == 0) sh.has_tau = 0;  // each mode holds only its topk depth-1 entries
       } else {
-        set_tau();
+        set_tau(two && t == 2 && pass == 0);
         if (sh.has_tau) {
           // entries outside the bound can neither be in the tree nor lead to it
           const uint32_t tau = sh.tau;
@@ -714,7 +784,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
               if (!ht || desc_key(ch.score) <= tau) {
                 ch.k0 = par.k0;
                 ch.k1 = par.k1 & ~31u;
-                pk_set(ch.k0, ch.k1, t + 1, sig_s[row + j]);
+                pk_set(ch.k0, ch.k1, t + 1, (uint32_t)j);
                 ch.k1 |= (uint32_t)(t + 1);
                 want = true;
               }
@@ -757,7 +827,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
                 } else {
                   ch.k0 = par.k0;
                   ch.k1 = par.k1 & ~31u;
-                  pk_set(ch.k0, ch.k1, t + 1, sig_s[row + j]);
+                  pk_set(ch.k0, ch.k1, t + 1, (uint32_t)j);
                   ch.k1 |= (uint32_t)(t + 1);
                   want = true;
                 }
@@ -799,7 +869,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
 
   // ---------------------------------------------------- candidates
   if (!tau_current) {  // else: the pool was cut to the bound and nothing was added since
-    set_tau();
+    set_tau(false);
     if (sh.has_tau) {
       const uint32_t tau = sh.tau;
       const int n = compact_pool(sh, ent, nxt, sh.n_ent, [&](const PE &e, int) { return desc_key(e.score) <= tau; });
@@ -822,18 +892,29 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   // of the slot is compared with (a different sequence is a collision: the
   // table is rebuilt with another seed), and the best (score key, then mode)
   // of the slot is found by two 32-bit atomicMins.
+  // Each entry also finds the slot of its parent sequence (its prefix one
+  // token shorter), from the hash taken on the way.
   uint64_t seed = 0;
+  constexpr int JH = 5;  // entries a thread hashes: n <= NC <= THREADS * JH
   for (int attempt = 0; attempt < 4; ++attempt) {
     for (int s = tid; s < tsize; s += THREADS) {
       tag[s] = 0;
       bkey[s] = 0xFFFFFFFFu;
       bsub[s] = 0xFFFFFFFFu;
     }
-    if (tid == 0) sh.coll = 0;
+    if (tid == 0) {
+      sh.coll = 0;
+      sh.n_sel = 0;
+    }
     __syncthreads();
-    for (int i = tid; i < n; i += THREADS) {
+    uint64_t hpr[JH];
+#pragma unroll
+    for (int jj = 0; jj < JH; ++jj) {
+      const int i = tid + jj * THREADS;
+      hpr[jj] = 0;
+      if (i >= n) continue;
       const PE e = ent[i];
-      const uint64_t h = seq_hash(c, e, pk_depth(e.k1), seed);
+      const uint64_t h = seq_hash2(c, e, pk_depth(e.k1), seed, &hpr[jj]);
       const uint32_t tg = (uint32_t)(h >> 32) | 1u;
       uint32_t s = (uint32_t)h & (uint32_t)(tsize - 1);
       for (int probe = 0; probe < tsize; ++probe) {
@@ -853,12 +934,38 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       atomicMin(&bkey[s], desc_key(e.score));
     }
     __syncthreads();
-    for (int i = tid; i < n; i += THREADS) {
+#pragma unroll
+    for (int jj = 0; jj < JH; ++jj) {
+      const int i = tid + jj * THREADS;
+      if (i >= n) continue;
       const PE e = ent[i];
       const int s = hslot[i];
       const int r = rep[s];
       if (r != i && seq_cmp(c, e, ent[r]) != 0) sh.coll = 1;
       if (desc_key(e.score) == bkey[s]) atomicMin(&bsub[s], ((uint32_t)pk_mode(e.k1) << 16) | (uint32_t)i);
+      // the parent's slot: same tag, a representative one token shorter
+      // with the same tokens
+      const int d = pk_depth(e.k1);
+      uint16_t ps = 0xFFFFu;
+      if (d > 1) {
+        const uint32_t tg = (uint32_t)(hpr[jj] >> 32) | 1u;
+        uint32_t q = (uint32_t)hpr[jj] & (uint32_t)(tsize - 1);
+        for (int probe = 0; probe < tsize; ++probe) {
+          const uint32_t t0 = tag[q];
+          if (t0 == 0u) break;
+          if (t0 == tg) {
+            const PE g = ent[rep[q]];
+            bool same = pk_depth(g.k1) == d - 1;
+            for (int p = 1; p < d && same; ++p) same = token_at(c, g, p) == token_at(c, e, p);
+            if (same) {
+              ps = (uint16_t)q;
+              break;
+            }
+          }
+          q = (q + 1) & (uint32_t)(tsize - 1);
+        }
+      }
+      pslot[i] = ps;
     }
     __syncthreads();
     if (!sh.coll) break;
@@ -869,34 +976,46 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     if (tid == 0) report(prm.status, MFD_ERR_UNSUPPORTED);
     return;
   }
-  for (int i = tid; i < n; i += THREADS) {
-    prim[i] = (int)(bsub[hslot[i]] & 0xFFFF) == i;
-    nodeid[i] = -1;
+  // primaries; with few candidates every primary is selected right away
+  // (sh.n_sel was zeroed before the last barrier of the table rounds)
+  for (int base = warp * 32; base < n; base += THREADS) {
+    const int i = base + lane;
+    bool pr = false;
+    if (i < n) {
+      pr = (int)(bsub[hslot[i]] & 0xFFFF) == i;
+      prim[i] = pr;
+      nodeid[i] = -1;
+    }
+    if (n <= RANK_ALL) {
+      const int k = warp_append(&sh.n_sel, pr);
+      if (pr) {
+        sel[k] = (uint16_t)i;
+        skk[k] = desc_key(ent[i].score);
+      }
+    }
   }
   __syncthreads();
 
   // ---------------------------------------------------- the B best prefixes
   // With few candidates every primary is ranked; otherwise a radix bound on
   // the primaries' score keys first leaves about B of them.
-  bool ht_sel = false;
-  uint32_t tau_sel = 0xFFFFFFFFu;
   if (n > RANK_ALL) {
     radix_bound(sh, ent, n, 1, B, 2, hist1, hist1 + 256, false, [&](int i) { return prim[i] ? 0 : -1; }, no_group);
-    ht_sel = sh.act[0];
-    tau_sel = sh.pre[0] | 0xFFFFu;
-  }
-  if (tid == 0) sh.n_sel = 0;
-  __syncthreads();
-  for (int base = warp * 32; base < n; base += THREADS) {
-    const int i = base + lane;
-    const bool in = i < n && prim[i] && (!ht_sel || desc_key(ent[i].score) <= tau_sel);
-    const int k = warp_append(&sh.n_sel, in);
-    if (in) {
-      sel[k] = (uint16_t)i;
-      skk[k] = desc_key(ent[i].score);
+    const bool ht_sel = sh.act[0];
+    const uint32_t tau_sel = sh.pre[0] | 0xFFFFu;
+    if (tid == 0) sh.n_sel = 0;
+    __syncthreads();
+    for (int base = warp * 32; base < n; base += THREADS) {
+      const int i = base + lane;
+      const bool in = i < n && prim[i] && (!ht_sel || desc_key(ent[i].score) <= tau_sel);
+      const int k = warp_append(&sh.n_sel, in);
+      if (in) {
+        sel[k] = (uint16_t)i;
+        skk[k] = desc_key(ent[i].score);
+      }
     }
+    __syncthreads();
   }
-  __syncthreads();
   const int ns = sh.n_sel;
   const int nruns = (ns + 31) >> 5;
   // rank of each selected prefix = how many others come before it.  Runs of
@@ -980,28 +1099,10 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   // ---------------------------------------------------- parents
   for (int nd = 1 + tid; nd <= nn; nd += THREADS) {
     const int i = nslot[nd];
-    const PE e = ent[i];
-    const int d = pk_depth(e.k1);
     int par = 0;
-    if (d > 1) {
-      par = -1;
-      const uint64_t h = seq_hash(c, e, d - 1, seed);
-      const uint32_t tg = (uint32_t)(h >> 32) | 1u;
-      uint32_t s = (uint32_t)h & (uint32_t)(tsize - 1);
-      for (int probe = 0; probe < tsize && par < 0; ++probe) {
-        const uint32_t t0 = tag[s];
-        if (t0 == 0u) break;
-        if (t0 == tg) {
-          const int r = (int)(bsub[s] & 0xFFFF);
-          const PE g = ent[r];
-          if (pk_depth(g.k1) == d - 1) {
-            bool same = true;
-            for (int p = 1; p < d && same; ++p) same = token_at(c, g, p) == token_at(c, e, p);
-            if (same) par = nodeid[r];
-          }
-        }
-        s = (s + 1) & (uint32_t)(tsize - 1);
-      }
+    if (pk_depth(ent[i].k1) > 1) {
+      const int ps = pslot[i];
+      par = ps == 0xFFFF ? -1 : nodeid[bsub[ps] & 0xFFFF];
       if (par < 1 || par >= nd) sh.bad = 1;
     }
     par_s[nd] = (int16_t)par;
