@@ -353,6 +353,106 @@ __device__ int compact_pool(Shared &sh, PE *ent, uint8_t *nxt, int n, KeepFn kee
   return sh.n_out;
 }
 
+// The bound over the owned entries of ent[0, sh.n_ent): sh.tau, sh.has_tau.
+// pre: the key range is in sh.kmin/kmax and the first digit's histogram was
+// filled when the pool was generated.  Out of line: one copy of the code.
+__device__ __noinline__ void bound_owned(Shared &sh, const PE *ent, int *hist, int B, bool pre) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    sh.tau = 0xFFFFFFFFu;
+    sh.has_tau = 0;
+  }
+  const int n = sh.n_ent;
+  if (!pre) {
+    if (tid == 0) {
+      sh.kmin = 0xFFFFFFFFu;
+      sh.kmax = 0u;
+    }
+    if (tid < 256) hist[tid] = 0;
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;  // over the owned entries
+    for (int i = tid; i < n; i += THREADS) {
+      const PE e = ent[i];
+      if (e.k1 & K1_OWNED) {
+        const uint32_t k = desc_key(e.score);
+        lo = min(lo, k);
+        hi = max(hi, k);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    __syncthreads();
+    if (lane == 0 && lo <= hi) {
+      atomicMin(&sh.kmin, lo);
+      atomicMax(&sh.kmax, hi);
+    }
+    __syncthreads();
+  }
+  const uint32_t kmin = sh.kmin, kmax = sh.kmax;
+  const int hb = (kmin ^ kmax) ? 31 - __clz((int)(kmin ^ kmax)) : 0;
+  // digits of 8 bits from the highest differing bit down; a second digit
+  // only when the first leaves many entries in the boundary bin
+  int shift = hb > 7 ? hb - 7 : 0;
+  uint32_t prefix = shift + 8 >= 32 ? 0u : (kmin >> (shift + 8)) << (shift + 8);
+  for (int digit = 0; digit < 2; ++digit) {
+    const uint32_t hi_mask = shift + 8 >= 32 ? 0u : ~((1u << (shift + 8)) - 1u);
+    if (!(pre && digit == 0)) {
+    for (int base = warp * 32; base < n; base += THREADS) {
+      const int i = base + lane;
+      int bin = -1;
+      if (i < n) {
+        const PE e = ent[i];
+        const uint32_t k = desc_key(e.score);
+        if ((e.k1 & K1_OWNED) && (k & hi_mask) == prefix) bin = (int)((k >> shift) & 255u);
+      }
+      warp_hist_add(digit ? hist + 256 : hist, bin);
+    }
+    if (digit == 0 && tid < 256) hist[256 + tid] = 0;
+    __syncthreads();
+    }
+    if (warp == 0) {
+      const int *h = digit ? hist + 256 : hist;
+      const int need = digit ? sh.rem[0] : B;
+      int c8[8], sum = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        c8[b] = h[lane * 8 + b];
+        sum += c8[b];
+      }
+      int run = warp_excl_scan(sum, lane);
+      const int total = __shfl_sync(0xffffffffu, run + sum, 31);
+      if (lane == 0) sh.refine = 0;
+      if (total >= need) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (run < need && need <= run + c8[b]) {
+            const uint32_t pre = prefix | ((uint32_t)(lane * 8 + b) << shift);
+            sh.tau = pre | ((1u << shift) - 1u);
+            sh.has_tau = 1;
+            sh.pre[0] = pre;
+            sh.rem[0] = need - run;
+            sh.refine = c8[b] > 64 && shift > 0;
+          }
+          run += c8[b];
+        }
+      }
+    }
+    __syncthreads();
+    if (!sh.refine) break;
+    prefix = sh.pre[0];
+    shift = shift > 8 ? shift - 8 : 0;
+  }
+}
+
+__device__ __noinline__ int compact_by_tau(Shared &sh, PE *ent, uint8_t *nxt, int n, uint32_t tau) {
+  return compact_pool(sh, ent, nxt, n, [&](const PE &e, int) { return desc_key(e.score) <= tau; });
+}
+__device__ __noinline__ int compact_by_flag(Shared &sh, PE *ent, uint8_t *nxt, int n, const uint8_t *flg) {
+  return compact_pool(sh, ent, nxt, n, [&](const PE &, int i) { return flg[i] != 0; });
+}
+
 __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ Shared sh;
@@ -399,12 +499,21 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     const int rows = K * L, spw = 32 / SEG;  // rows per warp per round
     const int seg = lane / SEG, j = lane - seg * SEG;
     constexpr int RMAX = 16;                 // rounds: K * L <= 256 rows, 16 warps, >= 1 row a warp
+    float v[RMAX];
+    int32_t tk[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      const int row = (r * NWARPS + warp) * spw + seg;
+      const bool in = row < rows && j < topk;
+      v[r] = in ? __ldcg(glp + row * topk + j) : 0.f;  // L2: written by the kernel just before
+      tk[r] = in ? __ldcg(gtk + row * topk + j) : 0;
+    }
 #pragma unroll
     for (int r = 0; r < RMAX; ++r) {
       const int row = (r * NWARPS + warp) * spw + seg;
       if (row < rows && j < topk) {
-        lp_s[row * topk + j] = glp[row * topk + j];
-        tok_s[row * topk + j] = gtk[row * topk + j];
+        lp_s[row * topk + j] = v[r];
+        tok_s[row * topk + j] = tk[r];
       }
     }
     if (tid == 0) sh.n_ent = 0;
@@ -533,13 +642,19 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       sh.kmax = kmax;
     }
     const int TT = topk * topk;
+    // x / topk and x / TT as multiply-highs by ceil(2^32 / d): exact for
+    // x < 2^16 and 1 < d <= 2^10 (d = 1 has no such multiplier)
+    const uint32_t m1 = topk > 1 ? 0xFFFFFFFFu / (uint32_t)topk + 1u : 0u;
+    const uint32_t m2 = TT > 1 ? 0xFFFFFFFFu / (uint32_t)TT + 1u : 0u;
+    auto div1 = [&](int v) { return topk > 1 ? (int)__umulhi((uint32_t)v, m1) : v; };
+    auto div2 = [&](int v) { return TT > 1 ? (int)__umulhi((uint32_t)v, m2) : v; };
     for (int base = warp * 32; base < N1 + N2; base += THREADS) {
       const int x = base + lane;
       int bin = -1;
       if (x < N1) {
         int k, j;
         if (full) {
-          k = x / topk;
+          k = div1(x);
           j = x - k * topk;
         } else {
           int off = 0;
@@ -561,9 +676,9 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         const int y = x - N1;
         int k, a, b2;
         if (full) {
-          k = y / TT;
+          k = div2(y);
           const int r = y - k * TT;
-          a = r / topk;
+          a = div1(r);
           b2 = r - a * topk;
         } else {
           int off = 0;
@@ -588,7 +703,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         nxt[x] = 0;
         if (own) bin = (int)((desc_key(en.score) >> shift) & 255u);
       }
-      warp_hist_add(hist, bin);
+      if (bin >= 0) atomicAdd(&hist[bin], 1);  // bins here are mostly distinct within a warp
     }
     if (tid == 0) sh.n_ent = N1 + N2;
   }
@@ -599,96 +714,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   // bits below the highest bit where the owned keys differ, rounded to the
   // worse end of its bin.  sh.has_tau = 0 while fewer than B entries are owned.
   auto no_group = [](int) { return -1; };
-  // pre: the key range is in sh.kmin/kmax and the first digit's histogram
-  // was filled when the pool was generated.
-  auto set_tau = [&](bool pre) {
-    if (tid == 0) {
-      sh.tau = 0xFFFFFFFFu;
-      sh.has_tau = 0;
-    }
-    const int n = sh.n_ent;
-    if (!pre) {
-      if (tid == 0) {
-        sh.kmin = 0xFFFFFFFFu;
-        sh.kmax = 0u;
-      }
-      if (tid < 256) hist[tid] = 0;
-      uint32_t lo = 0xFFFFFFFFu, hi = 0u;  // over the owned entries
-      for (int i = tid; i < n; i += THREADS) {
-        const PE e = ent[i];
-        if (e.k1 & K1_OWNED) {
-          const uint32_t k = desc_key(e.score);
-          lo = min(lo, k);
-          hi = max(hi, k);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-      }
-      __syncthreads();
-      if (lane == 0 && lo <= hi) {
-        atomicMin(&sh.kmin, lo);
-        atomicMax(&sh.kmax, hi);
-      }
-      __syncthreads();
-    }
-    const uint32_t kmin = sh.kmin, kmax = sh.kmax;
-    const int hb = (kmin ^ kmax) ? 31 - __clz((int)(kmin ^ kmax)) : 0;
-    // digits of 8 bits from the highest differing bit down; a second digit
-    // only when the first leaves many entries in the boundary bin
-    int shift = hb > 7 ? hb - 7 : 0;
-    uint32_t prefix = shift + 8 >= 32 ? 0u : (kmin >> (shift + 8)) << (shift + 8);
-    for (int digit = 0; digit < 2; ++digit) {
-      const uint32_t hi_mask = shift + 8 >= 32 ? 0u : ~((1u << (shift + 8)) - 1u);
-      if (!(pre && digit == 0)) {
-      for (int base = warp * 32; base < n; base += THREADS) {
-        const int i = base + lane;
-        int bin = -1;
-        if (i < n) {
-          const PE e = ent[i];
-          const uint32_t k = desc_key(e.score);
-          if ((e.k1 & K1_OWNED) && (k & hi_mask) == prefix) bin = (int)((k >> shift) & 255u);
-        }
-        warp_hist_add(digit ? hist + 256 : hist, bin);
-      }
-      if (digit == 0 && tid < 256) hist[256 + tid] = 0;
-      __syncthreads();
-      }
-      if (warp == 0) {
-        const int *h = digit ? hist + 256 : hist;
-        const int need = digit ? sh.rem[0] : B;
-        int c8[8], sum = 0;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          c8[b] = h[lane * 8 + b];
-          sum += c8[b];
-        }
-        int run = warp_excl_scan(sum, lane);
-        const int total = __shfl_sync(0xffffffffu, run + sum, 31);
-        if (lane == 0) sh.refine = 0;
-        if (total >= need) {
-#pragma unroll
-          for (int b = 0; b < 8; ++b) {
-            if (run < need && need <= run + c8[b]) {
-              const uint32_t pre = prefix | ((uint32_t)(lane * 8 + b) << shift);
-              sh.tau = pre | ((1u << shift) - 1u);
-              sh.has_tau = 1;
-              sh.pre[0] = pre;
-              sh.rem[0] = need - run;
-              sh.refine = c8[b] > 64 && shift > 0;
-            }
-            run += c8[b];
-          }
-        }
-      }
-      __syncthreads();
-      if (!sh.refine) break;
-      prefix = sh.pre[0];
-      shift = shift > 8 ? shift - 8 : 0;
-    }
-  };
+  auto set_tau = [&](bool pre) { bound_owned(sh, ent, hist, B, pre); };
 
   // prune to each mode's exact B best (only when the pool is full)
   auto prune_exact = [&]() {
@@ -717,7 +743,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       flg[i] = kp;
     }
     __syncthreads();
-    const int out = compact_pool(sh, ent, nxt, n, [&](const PE &, int i) { return flg[i] != 0; });
+    const int out = compact_by_flag(sh, ent, nxt, n, flg);
     if (tid == 0) sh.n_ent = out;
     __syncthreads();
   };
@@ -736,7 +762,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         if (sh.has_tau) {
           // entries outside the bound can neither be in the tree nor lead to it
           const uint32_t tau = sh.tau;
-          n_pool = compact_pool(sh, ent, nxt, sh.n_ent, [&](const PE &e, int) { return desc_key(e.score) <= tau; });
+          n_pool = compact_by_tau(sh, ent, nxt, sh.n_ent, tau);
         }
       }
       tau_current = true;
@@ -872,7 +898,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     set_tau(false);
     if (sh.has_tau) {
       const uint32_t tau = sh.tau;
-      const int n = compact_pool(sh, ent, nxt, sh.n_ent, [&](const PE &e, int) { return desc_key(e.score) <= tau; });
+      const int n = compact_by_tau(sh, ent, nxt, sh.n_ent, tau);
       if (tid == 0) sh.n_ent = n;
       __syncthreads();
     }
