@@ -185,7 +185,11 @@ int mfd_build_tree(const float *tk_logp, const int32_t *tk_tok, int n_req, int K
  *   path_nodes    int32 [n_req][L + 1]  node read at step j (path_nodes[0] = 0)
  *   out_tokens    int32 [n_req][L + 1]  y at step j: accepted tokens, bonus last
  * Entries past accept_len hold -1.  The walk is one cooperative grid with a
- * bounded grid-wide wait per step (MFD_ERR_TIMEOUT if it runs out). */
+ * bounded grid-wide wait per step (MFD_ERR_TIMEOUT if it runs out).  The
+ * CTAs exchange step results through ws, which needs no zeroing: its words
+ * carry a generation counter that each call advances, so ws may be shared
+ * with other calls and replayed in CUDA graphs (only calls overlapping on the
+ * GPU must not share it). */
 int mfd_verify(const float *target_logits, int n_req, int B, int V, int L,
                const int32_t *parent, const int32_t *token, const int32_t *n_nodes,
                const float *temperature, const uint64_t *seed, int32_t *accept_len,
