@@ -104,6 +104,29 @@ int mfd_lmhead_topk(const void *h, int R, int H, const void *W, int V, int topk,
                     float *tk_logp, int32_t *tk_tok, float *lse, int32_t *status, void *ws,
                     size_t ws_bytes, mfd_stream_t stream);
 
+/* The LM-head weight packed for streaming.  The weight is fixed for a model
+ * (model card "MFD drafter for Qwen3.5-4B", Model table: the target's LM
+ * head), so it can be laid out once, when the model is loaded, in the order
+ * mfd_lmhead_topk_packed streams it: per vocabulary tile of 256 rows and per
+ * 64-element K slice, one 32 KB block holding that slice of the 256 rows in
+ * the MMA's 128-byte-swizzled shared-memory order; rows past V are zero.
+ * Every pipeline stage then reads one contiguous piece of memory.
+ *
+ * mfd_lmhead_packed_bytes: bytes of the packed weight for (V, H), or 0 outside
+ *   the limits of mfd_lmhead_topk.
+ * mfd_lmhead_pack: W bf16 [V][H] (16-byte aligned) -> W_packed (device,
+ *   256-byte aligned, packed_bytes >= mfd_lmhead_packed_bytes(V, H)).  Errors:
+ *   INVALID_ARG (NULL, V or H < 1, misaligned), UNSUPPORTED (limits, device),
+ *   WORKSPACE (W_packed too small), CUDA.  Enqueued on `stream`.
+ * mfd_lmhead_topk_packed: mfd_lmhead_topk with the packed weight in place of
+ *   W; same arguments, workspace (MFD_OP_LMHEAD_TOPK), outputs and errors, and
+ *   bit-identical results. */
+size_t mfd_lmhead_packed_bytes(int V, int H);
+int mfd_lmhead_pack(const void *W, int V, int H, void *W_packed, size_t packed_bytes, mfd_stream_t stream);
+int mfd_lmhead_topk_packed(const void *h, int R, int H, const void *W_packed, int V, int topk,
+                           float *tk_logp, int32_t *tk_tok, float *lse, int32_t *status, void *ws,
+                           size_t ws_bytes, mfd_stream_t stream);
+
 /* Log-softmax and top-k of fp32 logits given directly (no LM head): the
  * same outputs as mfd_lmhead_topk with z = logits [R][V].  Non-finite logits
  * are the caller's responsibility. */

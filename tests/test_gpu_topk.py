@@ -131,3 +131,57 @@ def test_lmhead_rejects_bad_arguments():
     with pytest.raises(mfd.MfdError) as e:
         rd.lmhead_topk(h, W)
     assert e.value.code == mfd.MFD_ERR_UNSUPPORTED
+
+
+def _expected_packed(W: np.ndarray) -> np.ndarray:
+    """The packed layout written out plainly (uint16 view of bf16): per
+    256-row tile and 64-element K slice a block of 256 rows x 64 elements,
+    row r's 16-byte chunk j stored at chunk position j ^ (r % 8); rows past V
+    zero."""
+    V, H = W.shape
+    nt, nk = -(-V // 256), H // 64
+    Wpad = np.zeros((nt * 256, H), np.uint16)
+    Wpad[:V] = W
+    out = np.empty((nt, nk, 256, 8, 8), np.uint16)  # tile, slice, row, chunk position, element
+    for r in range(256):
+        for pos in range(8):
+            j = pos ^ (r % 8)
+            out[:, :, r, pos, :] = Wpad.reshape(nt, 256, nk, 8, 8)[:, r, :, j, :]
+    return out.reshape(-1)
+
+
+def test_pack_layout():
+    rng = np.random.default_rng(5)
+    V, H = 300, 128
+    W = torch.from_numpy(rng.standard_normal((V, H)).astype(np.float32)).to(torch.bfloat16)
+    Wp = mfd.pack_lm_head(W.cuda())
+    torch.cuda.synchronize()
+    assert Wp.numel() == mfd.mfd_lmhead_packed_bytes(V, H) == 2 * 256 * H * 2
+    got = Wp.cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(got, _expected_packed(_bits(W).reshape(V, H)))
+
+
+@pytest.mark.parametrize("R,H,V,topk", [(120, 2560, 151936, 16), (37, 128, 1000, 8), (200, 256, 4099, 32),
+                                        (1, 64, 16, 1)])
+def test_packed_weight_bit_identical(R, H, V, topk):
+    """mfd_lmhead_topk_packed gives exactly mfd_lmhead_topk's results."""
+    rng = np.random.default_rng(R + H + V)
+    if V == 151936:
+        W = synth.lm_head(V, H, seed=2024)
+        h = synth.round_inputs(W, 8, 15, 11, seed=3).h
+    else:
+        W = torch.from_numpy((rng.standard_normal((V, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16)
+        h = torch.from_numpy(rng.standard_normal((R, H)).astype(np.float32)).to(torch.bfloat16)
+    Wd, hd = W.cuda(), h.cuda()
+    a = mfd.Round(1, 1, R, topk, 1, V)
+    b = mfd.Round(1, 1, R, topk, 1, V)
+    a.status.zero_()
+    b.status.zero_()
+    a.lmhead_topk(hd, Wd)
+    Wp = mfd.pack_lm_head(Wd)
+    b.lmhead_topk_packed(hd, Wp)
+    torch.cuda.synchronize()
+    assert status_of(a) == 0 and status_of(b) == 0
+    np.testing.assert_array_equal(np_(a.tk_tok), np_(b.tk_tok))
+    np.testing.assert_array_equal(np_(a.tk_logp).view(np.uint32), np_(b.tk_logp).view(np.uint32))
+    np.testing.assert_array_equal(np_(a.lse).view(np.uint32), np_(b.lse).view(np.uint32))

@@ -37,8 +37,8 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;            // one 128-byte swizzle atom of bf16
-constexpr int KSUB = 2;           // K atoms per pipeline stage: 256 contiguous bytes per weight row
-constexpr int STAGES = 2;
+constexpr int KSUB = 1;           // K atoms per pipeline stage
+constexpr int STAGES = 4;
 constexpr int A_SUB = BM * BK * 2;  // one K atom of the hidden tile
 constexpr int B_SUB = BN * BK * 2;  // one K atom of the weight tile
 constexpr int A_BYTES = KSUB * A_SUB;
@@ -63,6 +63,7 @@ struct Params {
   float2 *part_ms;  // [R][P]      (running max, sum exp(z - max))
   int2 *part_cand;  // [R][P][T]   (logit bits, token id), best first
   int32_t *status;
+  const uint8_t *w_packed;  // packed weight (see pack_w_kernel), or null
 };
 
 __device__ __forceinline__ void item_range(const Params &p, int item, int &mt, int &t0, int &t1, int &range) {
@@ -90,7 +91,10 @@ __device__ __forceinline__ void topk_insert(float (&tv)[T], int (&ti)[T], float 
   }
 }
 
-template <int T>
+// PACKED: the weight comes as pack_w_kernel lays it out, so a stage's
+// weight bytes are one contiguous 1-D bulk copy instead of KSUB 2-D boxes of
+// 256 rows x 128 bytes (rows 2H bytes apart), which stream markedly slower.
+template <int T, bool PACKED>
 __global__ void __launch_bounds__(THREADS, 1)
     lmhead_topk_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                        const Params p) {
@@ -126,7 +130,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     *never = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_h);
-    prefetch_tmap(&tmap_w);
+    if (!PACKED) prefetch_tmap(&tmap_w);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -161,8 +165,13 @@ __global__ void __launch_bounds__(THREADS, 1)
               break;
             }
             mbar_arrive_expect_tx(&full[stage], (uint32_t)(nsub * (A_SUB + B_SUB)));
-            for (int sub = 0; sub < nsub; ++sub)
-              tma_load_2d(sB + stage * B_BYTES + sub * B_SUB, &tmap_w, (kc + sub) * BK, t * BN, &full[stage], pol_w);
+            if (PACKED)
+              bulk_load_1d(sB + stage * B_BYTES, p.w_packed + ((size_t)t * nk + kc) * B_SUB, (uint32_t)(nsub * B_SUB),
+                           &full[stage], pol_w);
+            else
+              for (int sub = 0; sub < nsub; ++sub)
+                tma_load_2d(sB + stage * B_BYTES + sub * B_SUB, &tmap_w, (kc + sub) * BK, t * BN, &full[stage],
+                            pol_w);
             for (int sub = 0; sub < nsub; ++sub)
               tma_load_2d(sA + stage * A_BYTES + sub * A_SUB, &tmap_h, (kc + sub) * BK, mt * BM, &full[stage], pol_h);
             issued |= 1u << stage;
@@ -333,7 +342,27 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int T>
+// Packed weight: for vocabulary tile t (256 rows) and K atom a (64 elements)
+// a 32 KB block at ((t * H/64) + a) * 32 KB holding exactly the shared-memory
+// image a 2-D box load of those 256 rows x 64 elements writes with the
+// 128-byte swizzle: row r at r * 128 bytes, its 16-byte chunk j at position
+// j ^ (r % 8).  Rows past V are zero (as the box load's fill).
+__global__ void pack_w_kernel(const uint4 *__restrict__ W, int V, int H, uint4 *__restrict__ Wp, size_t n16) {
+  const int nk = H / BK;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n16; q += stride) {
+    const size_t blk = q / (B_SUB / 16);
+    const int c = (int)(q - blk * (B_SUB / 16));
+    const int t = (int)(blk / nk), a = (int)(blk - (size_t)t * nk);
+    const int r = c >> 3, j = (c & 7) ^ (r & 7);
+    const int row = t * BN + r;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (row < V) v = __ldg(W + (size_t)row * (H / 8) + a * 8 + j);
+    Wp[q] = v;
+  }
+}
+
+template <int T, bool PACKED>
 cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
   static_assert(smem_bytes() <= 232448, "shared memory budget");
   Params p;
@@ -347,7 +376,8 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
   p.part_ms = reinterpret_cast<float2 *>(L.part_ms);
   p.part_cand = reinterpret_cast<int2 *>(L.part_cand);
   p.status = L.status;
-  cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  p.w_packed = static_cast<const uint8_t *>(L.w_packed);
+  cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<T, PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem_bytes());
   if (e != cudaSuccess) return e;
   const int grid = p.n_items < L.n_sm ? p.n_items : L.n_sm;
@@ -361,7 +391,7 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, lmhead_topk_kernel<T>, *L.tmap_h, *L.tmap_w, p);
+  e = cudaLaunchKernelEx(&cfg, lmhead_topk_kernel<T, PACKED>, *L.tmap_h, PACKED ? *L.tmap_h : *L.tmap_w, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -373,12 +403,21 @@ int lmhead_m_rows() { return BM; }
 int lmhead_k_chunk() { return BK; }
 
 cudaError_t launch_lmhead_partials(const LmheadLaunch &L, cudaStream_t stream) {
+  const bool pk = L.w_packed != nullptr;
   switch (L.T) {
-    case 8: return launch_t<8>(L, stream);
-    case 16: return launch_t<16>(L, stream);
-    case 32: return launch_t<32>(L, stream);
+    case 8: return pk ? launch_t<8, true>(L, stream) : launch_t<8, false>(L, stream);
+    case 16: return pk ? launch_t<16, true>(L, stream) : launch_t<16, false>(L, stream);
+    case 32: return pk ? launch_t<32, true>(L, stream) : launch_t<32, false>(L, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+size_t lmhead_packed_bytes(int V, int H) { return (size_t)((V + BN - 1) / BN) * BN * (size_t)H * 2; }
+
+cudaError_t launch_pack_w(const void *W, int V, int H, void *Wp, cudaStream_t stream) {
+  const size_t n16 = lmhead_packed_bytes(V, H) / 16;
+  pack_w_kernel<<<4 * 152, 256, 0, stream>>>(static_cast<const uint4 *>(W), V, H, static_cast<uint4 *>(Wp), n16);
+  return cudaGetLastError();
 }
 
 }  // namespace mfd

@@ -16,12 +16,15 @@ struct LmheadLaunch {
   void *part_ms;    // float2 [R][P]
   void *part_cand;  // int2 [R][P][T]
   int32_t *status;
+  const void *w_packed;  // packed weight (lmhead_packed_bytes), or null: use tmap_w
 };
 
 int lmhead_tile_rows();  // vocabulary rows per tile (256)
 int lmhead_m_rows();     // hidden rows per M tile (128)
 int lmhead_k_chunk();    // K elements per pipeline stage (64)
 cudaError_t launch_lmhead_partials(const LmheadLaunch &L, cudaStream_t stream);
+size_t lmhead_packed_bytes(int V, int H);  // bytes of the packed weight
+cudaError_t launch_pack_w(const void *W, int V, int H, void *Wp, cudaStream_t stream);
 
 // topk.cu
 struct MergeLaunch {

@@ -204,12 +204,16 @@ size_t mfd_workspace_size(int op, int n_req, int K, int L, int topk, int B, int 
   }
 }
 
-int mfd_lmhead_topk(const void *h, int R, int H, const void *W, int V, int topk, float *tk_logp,
-                    int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes,
-                    mfd_stream_t stream) {
-  if (!h || !W || !tk_logp || !tk_tok || !status || R < 1 || H < 1 || V < 1 || topk < 1)
+}  // extern "C"
+
+namespace {
+// The LM head call, from the row-major weight (W, through its tensor map) or
+// from the packed weight (Wp).
+int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int V, int topk, float *tk_logp,
+                int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes, mfd_stream_t stream) {
+  if (!h || (!W && !Wp) || !tk_logp || !tk_tok || !status || R < 1 || H < 1 || V < 1 || topk < 1)
     return MFD_ERR_INVALID_ARG;
-  if (!aligned(h, 16) || !aligned(W, 16)) return MFD_ERR_INVALID_ARG;
+  if (!aligned(h, 16) || (W && !aligned(W, 16)) || (Wp && !aligned(Wp, 256))) return MFD_ERR_INVALID_ARG;
   if (H % mfd::lmhead_k_chunk() != 0 || topk > 32 || V < 16 || topk > V || V >= (1 << 30))
     return MFD_ERR_UNSUPPORTED;
   DeviceInfo d;
@@ -220,11 +224,12 @@ int mfd_lmhead_topk(const void *h, int R, int H, const void *W, int V, int topk,
   if (!ws || ws_bytes < y.total || !aligned(ws, 256)) return MFD_ERR_WORKSPACE;
   const CUtensorMap *mh = nullptr, *mw = nullptr;
   if ((rc = tensor_map(h, R, H, mfd::lmhead_m_rows(), &mh)) != MFD_OK) return rc;
-  if ((rc = tensor_map(W, V, H, mfd::lmhead_tile_rows(), &mw)) != MFD_OK) return rc;
+  if (W && (rc = tensor_map(W, V, H, mfd::lmhead_tile_rows(), &mw)) != MFD_OK) return rc;
   char *base = static_cast<char *>(ws);
   mfd::LmheadLaunch L;
   L.tmap_h = mh;
   L.tmap_w = mw;
+  L.w_packed = W ? nullptr : Wp;
   L.R = R;
   L.H = H;
   L.V = V;
@@ -248,6 +253,41 @@ int mfd_lmhead_topk(const void *h, int R, int H, const void *W, int V, int topk,
   M.lse = lse;
   M.status = status;
   return cuda_status(mfd::launch_merge_topk(M, s));
+}
+}  // namespace
+
+extern "C" {
+
+int mfd_lmhead_topk(const void *h, int R, int H, const void *W, int V, int topk, float *tk_logp,
+                    int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes,
+                    mfd_stream_t stream) {
+  if (!W) return MFD_ERR_INVALID_ARG;
+  return lmhead_call(h, R, H, W, nullptr, V, topk, tk_logp, tk_tok, lse, status, ws, ws_bytes, stream);
+}
+
+size_t mfd_lmhead_packed_bytes(int V, int H) {
+  if (V < 16 || V >= (1 << 30) || H < 1 || H % mfd::lmhead_k_chunk() != 0) return 0;
+  return mfd::lmhead_packed_bytes(V, H);
+}
+
+int mfd_lmhead_pack(const void *W, int V, int H, void *W_packed, size_t packed_bytes, mfd_stream_t stream) {
+  if (!W || !W_packed || V < 1 || H < 1) return MFD_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(W_packed, 256)) return MFD_ERR_INVALID_ARG;
+  const size_t need = mfd_lmhead_packed_bytes(V, H);
+  if (need == 0) return MFD_ERR_UNSUPPORTED;
+  if (packed_bytes < need) return MFD_ERR_WORKSPACE;
+  DeviceInfo d;
+  int rc = current_device_info(&d);
+  if (rc != MFD_OK) return rc;
+  if (!is_sm103(d)) return MFD_ERR_UNSUPPORTED;
+  return cuda_status(mfd::launch_pack_w(W, V, H, W_packed, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mfd_lmhead_topk_packed(const void *h, int R, int H, const void *W_packed, int V, int topk, float *tk_logp,
+                           int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes,
+                           mfd_stream_t stream) {
+  if (!W_packed) return MFD_ERR_INVALID_ARG;
+  return lmhead_call(h, R, H, nullptr, W_packed, V, topk, tk_logp, tk_tok, lse, status, ws, ws_bytes, stream);
 }
 
 int mfd_logits_topk(const float *logits, int R, int V, int topk, float *tk_logp, int32_t *tk_tok, float *lse,

@@ -30,8 +30,9 @@ MFD_OP_LOGITS_TOPK = 1
 MFD_OP_BUILD_TREE = 2
 MFD_OP_VERIFY = 3
 
-EXPORTS = ("mfd_status_string", "mfd_workspace_size", "mfd_lmhead_topk", "mfd_logits_topk",
-           "mfd_logits_topk_noalloc", "mfd_build_tree", "mfd_verify")
+EXPORTS = ("mfd_status_string", "mfd_workspace_size", "mfd_lmhead_topk", "mfd_lmhead_packed_bytes",
+           "mfd_lmhead_pack", "mfd_lmhead_topk_packed", "mfd_logits_topk", "mfd_logits_topk_noalloc",
+           "mfd_build_tree", "mfd_verify")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _lock = threading.Lock()
@@ -61,6 +62,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.mfd_workspace_size.restype = SZ
         lib.mfd_lmhead_topk.argtypes = [P, I, I, P, I, I, P, P, P, P, P, SZ, P]
         lib.mfd_lmhead_topk.restype = I
+        lib.mfd_lmhead_packed_bytes.argtypes = [I, I]
+        lib.mfd_lmhead_packed_bytes.restype = SZ
+        lib.mfd_lmhead_pack.argtypes = [P, I, I, P, SZ, P]
+        lib.mfd_lmhead_pack.restype = I
+        lib.mfd_lmhead_topk_packed.argtypes = [P, I, I, P, I, I, P, P, P, P, P, SZ, P]
+        lib.mfd_lmhead_topk_packed.restype = I
         lib.mfd_logits_topk.argtypes = [P, I, I, I, P, P, P, P, P, SZ, P]
         lib.mfd_logits_topk.restype = I
         lib.mfd_logits_topk_noalloc.argtypes = [P, I, I, I, P, P, P, P, P]
@@ -110,6 +117,36 @@ def mfd_lmhead_topk(h, W, topk, tk_logp, tk_tok, lse, status, ws, stream=None) -
     rc = load().mfd_lmhead_topk(_p(h), R, H, _p(W), V, topk, _p(tk_logp), _p(tk_tok), _p(lse), _p(status),
                                 _p(ws), ws.numel() * ws.element_size(), _s(stream))
     _check(rc, "mfd_lmhead_topk")
+
+
+def mfd_lmhead_packed_bytes(V: int, H: int) -> int:
+    return int(load().mfd_lmhead_packed_bytes(V, H))
+
+
+def mfd_lmhead_pack(W, W_packed, stream=None) -> None:
+    V, H = W.shape
+    assert W.dtype == torch.bfloat16
+    rc = load().mfd_lmhead_pack(_p(W), V, H, _p(W_packed), W_packed.numel() * W_packed.element_size(), _s(stream))
+    _check(rc, "mfd_lmhead_pack")
+
+
+def pack_lm_head(W, stream=None):
+    """The packed copy of W (a new device buffer, allocated here, once)."""
+    V, H = W.shape
+    n = mfd_lmhead_packed_bytes(V, H)
+    if n == 0:
+        raise MfdError(MFD_ERR_UNSUPPORTED, "mfd_lmhead_packed_bytes")
+    Wp = torch.empty((n,), dtype=torch.uint8, device=W.device)
+    mfd_lmhead_pack(W, Wp, stream)
+    return Wp
+
+
+def mfd_lmhead_topk_packed(h, W_packed, V, topk, tk_logp, tk_tok, lse, status, ws, stream=None) -> None:
+    R, H = h.shape
+    assert h.dtype == torch.bfloat16
+    rc = load().mfd_lmhead_topk_packed(_p(h), R, H, _p(W_packed), V, topk, _p(tk_logp), _p(tk_tok), _p(lse),
+                                       _p(status), _p(ws), ws.numel() * ws.element_size(), _s(stream))
+    _check(rc, "mfd_lmhead_topk_packed")
 
 
 def mfd_logits_topk(logits, topk, tk_logp, tk_tok, lse, status, ws, stream=None) -> None:
@@ -185,6 +222,10 @@ class Round:
 
     def lmhead_topk(self, h, W, stream=None):
         mfd_lmhead_topk(h, W, self.topk, self.tk_logp, self.tk_tok, self.lse, self.status, self.ws, stream)
+
+    def lmhead_topk_packed(self, h, W_packed, stream=None):
+        mfd_lmhead_topk_packed(h, W_packed, self.V, self.topk, self.tk_logp, self.tk_tok, self.lse, self.status,
+                               self.ws, stream)
 
     def logits_topk(self, logits, stream=None):
         mfd_logits_topk(logits, self.topk, self.tk_logp, self.tk_tok, self.lse, self.status, self.ws, stream)
