@@ -750,6 +750,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
 
   // ---------------------------------------------------- level expansion
   bool failed = false, tau_current = false;
+  int n_cut = -1;  // pool size right after the last cut to the bound (-1: none yet)
   for (int t = two ? 2 : 1; t < L && !failed; ++t) {
     if (tid == 0) sh.any = 0;
     int pass = 0;
@@ -757,15 +758,24 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       int n_pool = -1;
       if (t == 1 && pass == 0 && topk < B) {
         if (tid == 0) sh.has_tau = 0;  // each mode holds only its topk depth-1 entries
+        tau_current = true;
       } else {
-        set_tau(two && t == 2 && pass == 0);
-        if (sh.has_tau) {
-          // entries outside the bound can neither be in the tree nor lead to it
-          const uint32_t tau = sh.tau;
-          n_pool = compact_by_tau(sh, ent, nxt, sh.n_ent, tau);
+        // The bound only tightens as entries are added, so an earlier one stays
+        // valid (only looser): it is recomputed, and the pool cut to it, once
+        // the pool has grown by a quarter since the last cut, after a prune,
+        // or while there is none.
+        const int ne = sh.n_ent;
+        if (n_cut < 0 || pass > 0 || !sh.has_tau || ne > n_cut + (n_cut >> 2) + 32) {
+          set_tau(two && t == 2 && pass == 0);
+          if (sh.has_tau) {
+            // entries outside the bound can neither be in the tree nor lead to it
+            const uint32_t tau = sh.tau;
+            n_pool = compact_by_tau(sh, ent, nxt, sh.n_ent, tau);
+            n_cut = n_pool;
+          }
+          tau_current = true;
         }
       }
-      tau_current = true;
       if (tid == 0) {
         if (n_pool >= 0) sh.n_ent = n_pool;
         sh.overflow = 0;
