@@ -46,6 +46,7 @@ constexpr int PLIST = 1024;     // parents listed for pair-parallel expansion
 constexpr int PAIR_MAX = 4096;  // (parent, rank) pairs expanded at once
 constexpr int MAX_GROUPS = 17;  // radix groups: one per mode, plus one across modes
 constexpr int RANK_ALL = 1024;  // candidates up to which every primary is ranked
+constexpr int MAX_MASK_WORDS = 17;  // 32-bit words of a mask row for B + 1 <= 513 nodes
 
 // Pool entry (16 bytes).  k0: row ranks of positions 1..12, 5 bits each,
 // position 1 highest (bits 59..55).  k1: depth at bits 4..0, positions
@@ -1178,13 +1179,16 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     prm.mode[ob + nd] = md;
     prm.pos[ob + nd] = ps;
   }
-  for (int x = tid; x < N * W32; x += THREADS) {
-    const int i = x / W32, w = x - (x / W32) * W32;
-    uint32_t word = 0;
+  // mask rows: one ancestor walk per node, its words gathered in a small
+  // per-thread array (N <= 513 nodes: at most 17 words)
+  for (int i = tid; i < N; i += THREADS) {
+    uint32_t m[MAX_MASK_WORDS];
+#pragma unroll
+    for (int w = 0; w < MAX_MASK_WORDS; ++w) m[w] = 0u;
     if (i <= nn)
-      for (int a = i; a >= 0; a = (a == 0) ? -1 : par_s[a])
-        if ((a >> 5) == w) word |= 1u << (a & 31);
-    prm.mask[(size_t)q * N * W32 + x] = word;
+      for (int a = i; a >= 0; a = (a == 0) ? -1 : par_s[a]) m[a >> 5] |= 1u << (a & 31);
+    uint32_t *row = prm.mask + ((size_t)q * N + i) * W32;
+    for (int w = 0; w < W32; ++w) row[w] = m[w];
   }
   if (tid == 0) prm.n_nodes[q] = nn + 1;
 }
