@@ -73,3 +73,25 @@ def test_tree_limits_fit_shared_memory(lib, K, L, topk, B):
     fake = ctypes.c_void_p(0x100000)
     args = [fake] * 2 + [1, K, L, topk, B] + [fake, None] + [fake] * 9 + [fake, 16, None]
     assert lib.mfd_build_tree(*args) == mfd.MFD_ERR_WORKSPACE
+
+
+def test_packed_weight_entry_points_arguments(lib):
+    """mfd_lmhead_packed_bytes, mfd_lmhead_pack and mfd_lmhead_topk_packed:
+    sizes and the argument errors returned before any CUDA call."""
+    assert mfd.mfd_lmhead_packed_bytes(151936, 2560) == 594 * 256 * 2560 * 2
+    assert mfd.mfd_lmhead_packed_bytes(256, 64) == 256 * 64 * 2
+    assert mfd.mfd_lmhead_packed_bytes(257, 64) == 512 * 64 * 2  # the last tile is padded
+    assert mfd.mfd_lmhead_packed_bytes(1000, 100) == 0  # H not a multiple of 64
+    assert mfd.mfd_lmhead_packed_bytes(8, 64) == 0  # V < 16
+    fake = ctypes.c_void_p(0x100000)
+    assert lib.mfd_lmhead_pack(None, 1000, 128, fake, 1 << 30, None) == mfd.MFD_ERR_INVALID_ARG
+    assert lib.mfd_lmhead_pack(fake, 1000, 128, ctypes.c_void_p(0x100010), 1 << 30, None) == mfd.MFD_ERR_INVALID_ARG
+    assert lib.mfd_lmhead_pack(fake, 1000, 100, fake, 1 << 30, None) == mfd.MFD_ERR_UNSUPPORTED
+    assert lib.mfd_lmhead_pack(fake, 1000, 128, fake, 1024, None) == mfd.MFD_ERR_WORKSPACE
+    args = [fake, 4, 64, None, 1000, 8, fake, fake, None, fake, fake, 1 << 20, None]
+    assert lib.mfd_lmhead_topk_packed(*args) == mfd.MFD_ERR_INVALID_ARG  # no packed weight
+    args[3] = ctypes.c_void_p(0x100080)
+    assert lib.mfd_lmhead_topk_packed(*args) == mfd.MFD_ERR_INVALID_ARG  # not 256-byte aligned
+    args[3] = fake
+    args[5] = 40
+    assert lib.mfd_lmhead_topk_packed(*args) == mfd.MFD_ERR_UNSUPPORTED  # topk > 32
