@@ -12,9 +12,8 @@
 //   D[128 x 256] (TMEM, fp32) = h_tile[128 x H] . W_tile[256 x H]^T
 //
 // A = 128 hidden rows (one M tile, zero-filled past R), B = 256 vocabulary
-// rows, K streamed through a 2-stage shared-memory ring; a stage holds two
-// 64-element (128-byte, swizzled) K atoms, so every weight row contributes
-// 256 contiguous bytes per stage (fewer DRAM page openings per byte).  Each TMEM lane is one hidden row, so the
+// rows, K streamed through a 4-stage shared-memory ring of one 64-element
+// (128-byte, swizzled) K atom each.  Each TMEM lane is one hidden row, so the
 // epilogue thread that owns lane r reads its row's logits column by column
 // and keeps the row's running max, running sum of exp and a sorted top-T in
 // registers -- no cross-thread reduction.
@@ -149,7 +148,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------- producer
-      const uint64_t pol_w = policy_evict_first();
+      // a weight tile is read once per M tile: streamed past L2 when there
+      // is one M tile, kept at normal priority for the other M tiles' reuse
+      const uint64_t pol_w = p.n_mt == 1 ? policy_evict_first() : policy_evict_normal();
       const uint64_t pol_h = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_par = 0;
@@ -158,6 +159,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         int mt, t0, t1, range;
         item_range(p, item, mt, t0, t1, range);
         for (int t = t0; t < t1 && ok; ++t) {
+          if (p.n_mt > 1) {
+            // Every M tile of a range reads the same weight tiles at about
+            // the same time, so a weight tile missing in L2 stalls them all.
+            // One tile ahead, the CTAs of the range bring the next weight
+            // tile into L2 between them: M tile mt takes K atoms mt,
+            // mt + n_mt, ...
+            int tn = t + 1;
+            if (tn >= t1) {
+              tn = -1;
+              if (item + (int)gridDim.x < p.n_items) {
+                int mt2, t2, t3, r2;
+                item_range(p, item + (int)gridDim.x, mt2, t2, t3, r2);
+                tn = t2 < t3 ? t2 : -1;
+              }
+            }
+            if (tn >= 0)
+              for (int kb = mt; kb < nk; kb += p.n_mt) {
+                if (PACKED)
+                  bulk_prefetch_l2(p.w_packed + ((size_t)tn * nk + kb) * B_SUB, (uint32_t)B_SUB);
+                else
+                  tma_prefetch_2d(&tmap_w, kb * BK, tn * BN);
+              }
+          }
           for (int kc = 0; kc < nk; kc += KSUB) {
             const int nsub = nk - kc < KSUB ? nk - kc : KSUB;
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {

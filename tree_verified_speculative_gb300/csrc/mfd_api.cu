@@ -105,8 +105,24 @@ struct TopkLayout {
 TopkLayout lmhead_layout(int R, int V, int topk, int n_sm) {
   TopkLayout y;
   const int tiles = (V + mfd::lmhead_tile_rows() - 1) / mfd::lmhead_tile_rows();
+  const int n_mt = (R + mfd::lmhead_m_rows() - 1) / mfd::lmhead_m_rows();
   y.P = tiles < n_sm ? tiles : n_sm;
   if (y.P > 256) y.P = 256;
+  if (n_mt > 1) {
+    // Work items are (range, M tile).  Take the number of ranges that gives
+    // the busiest CTA the fewest weight tiles, and among those the fewest
+    // ranges: fewer partials to merge and fewer top-T restarts per row.
+    long long best = -1;
+    const int pmax = tiles < 256 ? tiles : 256;
+    for (int P = 1; P <= pmax; ++P) {
+      const long long rounds = ((long long)n_mt * P + n_sm - 1) / n_sm;
+      const long long cost = rounds * ((tiles + P - 1) / P);
+      if (best < 0 || cost < best) {
+        best = cost;
+        y.P = P;
+      }
+    }
+  }
   y.T = cand_width(topk);
   y.chunk = 0;
   y.ms_bytes = align256((size_t)R * y.P * 8);
