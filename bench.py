@@ -36,6 +36,14 @@ WORKLOADS = {
     "k8_l15_h5120_v248320_b256_greedy": dict(K=8, L=15, H=5120, V=248320, n_shared=13, topk=32, B=256, T=0.0),
     # a small shape for quick host-side runs (the reference arm in CPU tests)
     "tiny": dict(K=2, L=4, H=64, V=512, n_shared=2, topk=8, B=16, T=1.0),
+    # 32 requests in one round (3840 LM-head rows, one shared W): the
+    # tensor-bound shape; shared positions ~ U{8..14} per request, requests
+    # 0-15 greedy and 16-31 sampled at T = 1
+    "r32_k8_l15_h2560_v151936_b128_mixed": dict(K=8, L=15, H=2560, V=151936, n_shared=None, topk=16, B=128,
+                                                T=None, n_req=32, temps=[0.0] * 16 + [1.0] * 16),
+    # its small counterpart for host-side runs
+    "r4_tiny_mixed": dict(K=2, L=4, H=64, V=512, n_shared=None, topk=8, B=16, T=None, n_req=4,
+                          temps=[0.0, 0.0, 1.0, 1.0]),
 }
 DEFAULT = "k8_l15_h2560_v151936_b256_t1"
 METRIC = "draft-tree rounds/s at K=8,V=151936,B=256; LM-head HBM GB/s vs GB300 peak"
@@ -43,6 +51,7 @@ W_SEED = 2024
 N_NOISE = 4
 N_COPY_STREAMS = 2  # the end-to-end round copies the target logits in this many concurrent pieces
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse():
@@ -59,17 +68,21 @@ def parse():
     return ap.parse_args()
 
 
-def peaks():
+def peaks(kind="hbm"):
+    """Roofline denominator: HBM GB/s (kind "hbm") or dense bf16 TFLOP/s
+    (kind "bf16", the burst figure), measured when MEASURED_PEAKS.json has
+    it, else the fallback."""
+    keys = {"hbm": ("hbm_gbs", "hbm_GBs", "hbm"), "bf16": ("bf16_tflops", "bf16_TFLOPs", "bf16")}[kind]
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         try:
             d = json.load(open(p))
-            for k in ("hbm_gbs", "hbm_GBs", "hbm"):
+            for k in keys:
                 if k in d:
                     return float(d[k]), "measured"
         except Exception:
             pass
-    return FALLBACK_HBM_GBS, "fallback"
+    return (FALLBACK_HBM_GBS if kind == "hbm" else FALLBACK_BF16_TFLOPS), "fallback"
 
 
 def profiled_traffic():
@@ -349,6 +362,176 @@ def run_gpu(args, ws, rank, local):
     return out
 
 
+def batched_inputs(cfg, n_distinct, rank):
+    """n_distinct rounds of n_req requests each: per request its own futures,
+    hidden states and seed; shared positions ~ U{8..14}."""
+    import concurrent.futures as cf
+
+    from tree_verified_speculative_gb300 import synth
+
+    K, L, n_req = cfg["K"], cfg["L"], cfg["n_req"]
+    W = synth.lm_head(cfg["V"], cfg["H"], seed=W_SEED)
+    base = 1_000_000 * (rank + 1)
+
+    def one(r):
+        rng = np.random.default_rng(base + 7919 * r)
+        lo, hi = min(8, L), min(14, L)
+        return [synth.round_inputs(W, K, L, int(rng.integers(lo, hi + 1)), seed=base + r * n_req + q)
+                for q in range(n_req)]
+
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        rounds = list(ex.map(one, range(n_distinct)))
+    return W, rounds
+
+
+def run_gpu_batched(args, ws, rank, local):
+    """n_req requests per round through the same three calls: one LM head
+    over all n_req * K * L rows (one shared W), one tree per request, one
+    walk per request.  Timing as in run_gpu."""
+    import torch
+
+    from tree_verified_speculative_gb300 import mfd, synth
+
+    cfg = WORKLOADS[args.workload]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K, L, H, V, topk, B, n_req = cfg["K"], cfg["L"], cfg["H"], cfg["V"], cfg["topk"], cfg["B"], cfg["n_req"]
+    R, N = n_req * K * L, B + 1
+    n_rounds = args.warmup + args.steps
+    n_distinct = min(n_rounds, 16)  # the timed rounds cycle through these inputs
+    W, rounds = batched_inputs(cfg, n_distinct, rank)
+    Wd = W.to(dev)
+    Wp = mfd.pack_lm_head(Wd)
+    del Wd
+    h_all = torch.stack([torch.cat([r.h for r in rr], 0) for rr in rounds]).to(dev)
+    h_cur = torch.empty_like(h_all[0])
+    g = torch.Generator(device=dev)
+    g.manual_seed(W_SEED + rank)
+    noise = [torch.randn((n_req, N, V), device=dev, generator=g) for _ in range(2)]  # target rows ~ N(0, 1)
+    temp = torch.tensor(cfg["temps"], dtype=torch.float32, device=dev)
+    seeds = [torch.tensor(np.array([r.seed for r in rr], np.uint64).view(np.int64), device=dev) for rr in rounds]
+    rd = mfd.Round(n_req, K, L, topk, B, V, device=dev)
+    rd.status.zero_()
+    acc_buf = torch.zeros((n_rounds, n_req), dtype=torch.int32, device=dev)
+    trees = {k: torch.empty((n_rounds,) + tuple(getattr(rd, k).shape), dtype=torch.int32, device=dev)
+             for k in ("parent", "token", "depth", "n_nodes")}
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_rounds)]
+    CHUNK = 8
+
+    def ahead(n):
+        torch.cuda._sleep(int(n * 4_000_000))
+
+    def phase_a(idx, split=False):
+        for c0 in range(0, len(idx), CHUNK):
+            ahead(len(idx[c0:c0 + CHUNK]))
+            for i in idx[c0:c0 + CHUNK]:
+                e0, ea, e1 = ev[i][0], ev[i][1], ev[i][2]
+                h_cur.copy_(h_all[i % n_distinct])
+                e0.record(stream)
+                rd.lmhead_topk_packed(h_cur, Wp)
+                if split:
+                    ea.record(stream)
+                rd.build_tree()
+                e1.record(stream)
+                for k in trees:
+                    trees[k][i].copy_(getattr(rd, k))
+
+    def plant_sites_of(idx):
+        host = {k: v.cpu().numpy() for k, v in trees.items()}
+        out = {}
+        for i in idx:
+            flat = []
+            for q, r in enumerate(rounds[i % n_distinct]):
+                rows, cols = synth.plant_sites(host["parent"][i][q], host["token"][i][q], host["depth"][i][q],
+                                               int(host["n_nodes"][i][q]), r.fut[r.target_mode])
+                flat.append((q * N + rows.astype(np.int64)) * V + cols.astype(np.int64))
+            out[i] = torch.from_numpy(np.concatenate(flat)).to(dev)
+        return out
+
+    def phase_b(idx, sites):
+        for c0 in range(0, len(idx), CHUNK):
+            ahead(len(idx[c0:c0 + CHUNK]))
+            for i in idx[c0:c0 + CHUNK]:
+                for k in trees:
+                    getattr(rd, k).copy_(trees[k][i])
+                tb = noise[i % 2]
+                flat = tb.view(-1)
+                base = flat[sites[i]]
+                flat[sites[i]] = base + 10.0
+                s2, e3 = ev[i][3], ev[i][4]
+                s2.record(stream)
+                rd.verify(tb, temp, seeds[i % n_distinct])
+                e3.record(stream)
+                flat[sites[i]] = base
+                acc_buf[i].copy_(rd.accept_len)
+
+    warm = list(range(args.warmup))
+    timed = list(range(args.warmup, n_rounds))
+    phase_a(warm)
+    phase_b(warm, plant_sites_of(warm))
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    time.sleep(0.2)
+    phase_a(timed)
+    torch.cuda.synchronize()
+    sites_t = plant_sites_of(timed)
+    phase_b(timed, sites_t)
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    st = int(rd.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {mfd.status_string(st)}")
+    ab = sum(ev[i][0].elapsed_time(ev[i][2]) for i in timed)
+    vf = sum(ev[i][3].elapsed_time(ev[i][4]) for i in timed)
+    total_ms = reduce_max(ab + vf, ws)
+    diag = timed[:min(len(timed), 50)]
+    phase_a(diag, split=True)
+    torch.cuda.synchronize()
+    lm_d = [ev[i][0].elapsed_time(ev[i][1]) for i in diag]
+    bd_d = [ev[i][1].elapsed_time(ev[i][2]) for i in diag]
+    steps = args.steps
+    value = whole_job_rate(steps, ws, total_ms)
+    lm_us = sum(lm_d) / len(diag) * 1e3
+    flops = 2.0 * R * V * H
+    achieved = flops / (lm_us * 1e-6) / 1e12
+    peak, peak_kind = peaks("bf16")
+    acc = acc_buf[args.warmup:].float().cpu().numpy()
+    greedy = np.array(cfg["temps"]) == 0.0
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "rounds/s", "n_gpus": ws, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "K": K, "L": L, "H": H, "V": V, "topk": topk, "B": B,
+                   "n_req": n_req, "rows": R, "temperatures": "requests 0-15 greedy, 16-31 T=1",
+                   "parallelism": f"replicas{ws}" if ws > 1 else "single",
+                   "lm_head_weight": "packed once before timing (mfd_lmhead_pack), streamed by mfd_lmhead_topk_packed",
+                   "l2": "inputs larger than L2 (W = %.0f MB; %d distinct hidden-state batches of %.1f MB cycled)"
+                         % (V * H * 2 / 1e6, n_distinct, R * H * 2 / 1e6),
+                   "timing": "as the single-request workload: one CUDA-event interval around the LM head and the "
+                             "trees, one around the walks, summed over the timed rounds; split from diagnostic rounds"},
+        "requests_per_s": round(value * n_req, 1),
+        "stages_us": {"lmhead_topk_plus_build_tree": round(ab / steps * 1e3, 2), "verify": round(vf / steps * 1e3, 2),
+                      "split_from_diagnostic_rounds": {"lmhead_topk": round(lm_us, 2),
+                                                       "build_tree": round(sum(bd_d) / len(diag) * 1e3, 2),
+                                                       "rounds": len(diag)}},
+        "mean_accept_len": {"greedy": round(float(acc[:, greedy].mean()), 4),
+                            "sampled": round(float(acc[:, ~greedy].mean()), 4)},
+        "roofline": {"kernel": "mfd_lmhead_topk_packed (lmhead_topk_kernel + merge_topk_kernel)", "bound": "tensor",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "algorithmic_flops_per_launch": flops, "traffic": None},
+        "gpu_launches": 4 * steps,
+        "clocks": ck,
+        "e2e": None,
+        "e2e_note": "measured on the single-request workload only",
+    }
+
+
 def run_e2e(args, cfg, rounds, noise, sites, Wp, rd, dev):
     """Same rounds through the public API from pinned host buffers: H2D of the
     round's hidden states and target logits, the three calls, D2H of the
@@ -455,7 +638,10 @@ def run_reference(args, ws, rank):
     from tree_verified_speculative_gb300 import synth
 
     cfg = WORKLOADS[args.workload]
-    K, L, H, V, topk, B, T = cfg["K"], cfg["L"], cfg["H"], cfg["V"], cfg["topk"], cfg["B"], cfg["T"]
+    K, L, H, V, topk, B = cfg["K"], cfg["L"], cfg["H"], cfg["V"], cfg["topk"], cfg["B"]
+    n_req = cfg.get("n_req", 1)
+    temps = cfg.get("temps") or [cfg["T"]]
+    n_shared = cfg["n_shared"] if cfg["n_shared"] is not None else min(11, L)
     R = K * L
     oracle.build()
     bits = lambda x: x.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
@@ -464,7 +650,7 @@ def run_reference(args, ws, rank):
     n_steps = args.warmup + args.steps
     budget_s = 150.0 / max(1, n_steps)  # whole run within a few minutes
     # the vocabulary slice the LM-head sample covers, sized from one calibration
-    r0 = synth.round_inputs(W, K, L, cfg["n_shared"], seed=7)
+    r0 = synth.round_inputs(W, K, L, n_shared, seed=7)
     t0 = time.perf_counter()
     oracle.lmhead_logits(bits(r0.h), wb, 0, 4096)
     per_vocab = (time.perf_counter() - t0) / 4096
@@ -473,7 +659,8 @@ def run_reference(args, ws, rank):
     noise = synth.target_noise(B + 1, V, np.random.default_rng(11))
     times = []
     for s in range(n_steps):
-        r = synth.round_inputs(W, K, L, cfg["n_shared"], seed=2_000_000 + s)
+        r = synth.round_inputs(W, K, L, n_shared, seed=2_000_000 + s)
+        T = temps[s % len(temps)]
         hb = bits(r.h)
         v0 = (s * 9973) % max(1, V - n_v)
         t0 = time.perf_counter()
@@ -495,7 +682,8 @@ def run_reference(args, ws, rank):
         oracle.verify(noise, tr["parent"], tr["token"], int(tr["n_nodes"]), L, T, r.seed)
         t_ver = time.perf_counter() - t0
         if s >= args.warmup:
-            times.append(t_lm + t_sort + t_tree + t_ver)
+            # a round of n_req requests is n_req times one request's work
+            times.append((t_lm + t_sort + t_tree + t_ver) * n_req)
     per_round = sum(times) / len(times)
     value = 1.0 / per_round
     cores = oracle.default_threads()
@@ -503,11 +691,11 @@ def run_reference(args, ws, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_round * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "K": K, "L": L, "H": H, "V": V, "topk": topk, "B": B,
-                       "temperature": T, "n_req": 1},
+                       "temperature": temps[0] if n_req == 1 else "per request", "n_req": n_req},
             "cpu_baseline": {"value": round(value, 4), "unit": "rounds/s", "cores": cores, "kind": "oracle",
                              "sample": f"per step: LM head on {n_v} of {V} vocabulary rows for all {R} rows "
                                        f"(scaled), one full-row log-softmax+top-k (scaled x{R}), full tree and "
-                                       "verification walk"},
+                                       "verification walk" + (f"; one request, scaled x{n_req}" if n_req > 1 else "")},
             "e2e": {"value": round(value, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -521,14 +709,25 @@ def profile_rounds(args, local):
     cfg = WORKLOADS[args.workload]
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    W, rounds, noise = make_inputs(cfg, 1, 0)
+    n_req = cfg.get("n_req", 1)
+    if n_req > 1:
+        W, rr = batched_inputs(cfg, 1, 0)
+        rr = rr[0]
+        h = torch.cat([r.h for r in rr], 0).to(dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(W_SEED)
+        t = torch.randn((n_req, cfg["B"] + 1, cfg["V"]), device=dev, generator=g)
+        temp = torch.tensor(cfg["temps"], dtype=torch.float32, device=dev)
+        seed = torch.tensor(np.array([r.seed for r in rr], np.uint64).view(np.int64), device=dev)
+    else:
+        W, rounds, noise = make_inputs(cfg, 1, 0)
+        h = rounds[0].h.to(dev)
+        t = torch.from_numpy(noise[0]).to(dev)
+        temp = torch.tensor([cfg["T"]], dtype=torch.float32, device=dev)
+        seed = torch.tensor(np.array([rounds[0].seed], np.uint64).view(np.int64), device=dev)
     Wd = W.to(dev)
     Wp = mfd.pack_lm_head(Wd)
-    h = rounds[0].h.to(dev)
-    t = torch.from_numpy(noise[0]).to(dev)
-    temp = torch.tensor([cfg["T"]], dtype=torch.float32, device=dev)
-    seed = torch.tensor(np.array([rounds[0].seed], np.uint64).view(np.int64), device=dev)
-    rd = mfd.Round(1, cfg["K"], cfg["L"], cfg["topk"], cfg["B"], cfg["V"], device=dev)
+    rd = mfd.Round(n_req, cfg["K"], cfg["L"], cfg["topk"], cfg["B"], cfg["V"], device=dev)
     rd.status.zero_()
     for _ in range(args.profile_rounds):
         rd.lmhead_topk_packed(h, Wp)
@@ -551,7 +750,10 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args, ws, rank)))
         return
-    out = run_gpu(args, ws, rank, local)
+    if WORKLOADS[args.workload].get("n_req", 1) > 1:
+        out = run_gpu_batched(args, ws, rank, local)
+    else:
+        out = run_gpu(args, ws, rank, local)
     if rank == 0:
         print(json.dumps(out))
 
