@@ -87,10 +87,23 @@ def test_pages_shape(B):
     _compare(lp, tk, B, anchor=[42], base_pos=[977])
 
 
-def test_wide_shape_topk32():
-    rng = np.random.default_rng(33)
+@pytest.mark.parametrize("seed", [33, 34, 35])
+def test_wide_shape_topk32(seed):
+    rng = np.random.default_rng(seed)
     lp, tk = _planted_tables(rng, 1, 8, 15, 32, 248320, 13)
     _compare(lp, tk, 256)
+
+
+@pytest.mark.parametrize("V", [40, 64, 1000])
+def test_wide_shape_topk32_shared_tokens_and_ties(V):
+    """Top-32 rows whose pairs do not all fit the pool: depth 2 is counted,
+    then made within a first bound.  Few distinct tokens (heavily shared
+    between modes) and a coarse value grid (many equal scores)."""
+    rng = np.random.default_rng(V)
+    vals = np.array([-0.5, -1.0, -1.5, -2.0, -3.0], np.float32)
+    lp, tk = _random_tables(rng, 2, 8, 15, 32, V, vals)
+    for B in (64, 256):
+        _compare(lp, tk, B)
 
 
 def test_batched_32_requests():

@@ -181,7 +181,7 @@ __host__ __device__ inline Layout make_layout(int K, int L, int topk, int B, int
 }
 
 struct Shared {
-  int n_ent, overflow, any, refine, bad, coll, n_prim, n_sel, has_tau, n_par, n_out, n_in, wbad[NWARPS];
+  int n_ent, overflow, any, refine, bad, coll, n_prim, n_sel, has_tau, n_par, n_out, n_in, cut2, wbad[NWARPS];
   int cnt[MAX_GROUPS], act[MAX_GROUPS], rem[MAX_GROUPS], ntie[MAX_GROUPS];
   uint8_t u1[512];  // per first-row entry: its mode owns its token
   int f1[16], f2[16];
@@ -519,6 +519,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     }
     if (tid == 0) sh.n_ent = 0;
     if (tid < 512) hist[tid] = 0;  // the first bound's two digit histograms
+    if (tid < 256) hist[512 + tid] = 0;  // and the count of every depth-1 and depth-2 entry
     __syncwarp();
     bool bad = false;
 #pragma unroll 1
@@ -559,7 +560,13 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   // first token, hence its owner, hence their mode.
   // With no bound possible yet (every mode holds only its topk first
   // entries), depth 2 is generated at once when it fits.
+  // Depth 2 is made with depth 1 when every pair fits the pool (two).
+  // Otherwise, with depth 2 present (pairs), the pairs are first only
+  // counted: the owned ones into the first digit's histogram, all of them
+  // into a second.  They are then made only within the bound that the first
+  // histogram gives, when those fit (sh.cut2), else depth 1 alone.
   const bool two = L >= 2 && topk < B && K * topk * (1 + topk) <= CAP;
+  const bool pairs = L >= 2 && topk < B;
   {
     // T1 threads per first-row entry look for its token in the other modes'
     // first rows, each through every T1-th mode
@@ -619,7 +626,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     // fixed slots, mode-major: depth 1 first, then depth 2
     int N1 = 0, N2 = 0;
     bool full = true;
-    float hi = -INFINITY, lo = INFINITY;  // bounds of every score generated here
+    float hi = -INFINITY, lo = INFINITY;  // bounds of every score counted here
     for (int k = 0; k < K; ++k) {
       const int f1 = sh.f1[k], f2 = sh.f2[k];
       N1 += f1;
@@ -628,10 +635,10 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       if (f1 > 0) {
         hi = fmaxf(hi, lp_s[(k * L) * topk]);
         lo = fminf(lo, sh.lo1[k]);
-        if (two && f2 > 0) lo = fminf(lo, __fadd_rn(sh.lo1[k], sh.lo2[k]));
+        if (pairs && f2 > 0) lo = fminf(lo, __fadd_rn(sh.lo1[k], sh.lo2[k]));
       }
     }
-    if (!two) N2 = 0;
+    if (!pairs) N2 = 0;
     // the owned entries are counted into the first digit's histogram as they
     // are made; the digit starts at the highest bit where the score keys of
     // [lo, hi] differ
@@ -641,6 +648,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     if (tid == 0) {
       sh.kmin = kmin;
       sh.kmax = kmax;
+      sh.cut2 = 0;
     }
     const int TT = topk * topk;
     // x / topk and x / TT as multiply-highs by ceil(2^32 / d): exact for
@@ -649,9 +657,9 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     const uint32_t m2 = TT > 1 ? 0xFFFFFFFFu / (uint32_t)TT + 1u : 0u;
     auto div1 = [&](int v) { return topk > 1 ? (int)__umulhi((uint32_t)v, m1) : v; };
     auto div2 = [&](int v) { return TT > 1 ? (int)__umulhi((uint32_t)v, m2) : v; };
-    for (int base = warp * 32; base < N1 + N2; base += THREADS) {
-      const int x = base + lane;
-      int bin = -1;
+    // entry x of the fixed order (x < N1: depth 1, else depth 2); returns
+    // whether its mode owns its first token
+    auto make = [&](int x, PE &en) {
       if (x < N1) {
         int k, j;
         if (full) {
@@ -663,52 +671,128 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
           while (x - off >= sh.f1[k]) off += sh.f1[k++];
           j = x - off;
         }
-        const int e = (k * L) * topk + j;
-        PE en;
-        en.score = lp_s[e];
-        en.k0 = 0;
         const bool own = sh.u1[k * topk + j];
+        en.score = lp_s[(k * L) * topk + j];
+        en.k0 = 0;
         en.k1 = 1u | ((uint32_t)k << 25) | (own ? K1_OWNED : 0u);
         pk_set(en.k0, en.k1, 1, (uint32_t)j);
-        ent[x] = en;
-        nxt[x] = two ? (uint8_t)topk : 0;
-        if (own) bin = (int)((desc_key(en.score) >> shift) & 255u);
-      } else if (x < N1 + N2) {
-        const int y = x - N1;
-        int k, a, b2;
-        if (full) {
-          k = div2(y);
-          const int r = y - k * TT;
-          a = div1(r);
-          b2 = r - a * topk;
-        } else {
-          int off = 0;
-          k = 0;
-          while (y - off >= sh.f1[k] * sh.f2[k]) {
-            off += sh.f1[k] * sh.f2[k];
-            ++k;
-          }
-          const int r = y - off, f2 = sh.f2[k];
-          a = r / f2;
-          b2 = r - a * f2;
-        }
-        const int ea = (k * L) * topk + a, eb = (k * L + 1) * topk + b2;
-        PE en;
-        en.score = __fadd_rn(lp_s[ea], lp_s[eb]);
-        en.k0 = 0;
-        const bool own = sh.u1[k * topk + a];
-        en.k1 = 2u | ((uint32_t)k << 25) | (own ? K1_OWNED : 0u);
-        pk_set(en.k0, en.k1, 1, (uint32_t)a);
-        pk_set(en.k0, en.k1, 2, (uint32_t)b2);
-        ent[x] = en;
-        nxt[x] = 0;
-        if (own) bin = (int)((desc_key(en.score) >> shift) & 255u);
+        return own;
       }
-      if (bin >= 0) atomicAdd(&hist[bin], 1);  // bins here are mostly distinct within a warp
+      const int y = x - N1;
+      int k, a, b2;
+      if (full) {
+        k = div2(y);
+        const int r = y - k * TT;
+        a = div1(r);
+        b2 = r - a * topk;
+      } else {
+        int off = 0;
+        k = 0;
+        while (y - off >= sh.f1[k] * sh.f2[k]) {
+          off += sh.f1[k] * sh.f2[k];
+          ++k;
+        }
+        const int r = y - off, f2 = sh.f2[k];
+        a = r / f2;
+        b2 = r - a * f2;
+      }
+      const bool own = sh.u1[k * topk + a];
+      en.score = __fadd_rn(lp_s[(k * L) * topk + a], lp_s[(k * L + 1) * topk + b2]);
+      en.k0 = 0;
+      en.k1 = 2u | ((uint32_t)k << 25) | (own ? K1_OWNED : 0u);
+      pk_set(en.k0, en.k1, 1, (uint32_t)a);
+      pk_set(en.k0, en.k1, 2, (uint32_t)b2);
+      return own;
+    };
+    auto bin_of = [&](float score) { return (int)((desc_key(score) >> shift) & 255u); };
+    if (pairs && !two) {
+      int *hall = hist + 512;  // every pair and depth-1 entry, owned or not
+      for (int x = tid; x < N1 + N2; x += THREADS) {
+        PE en;
+        const bool own = make(x, en);
+        const int b = bin_of(en.score);
+        if (own) atomicAdd(&hist[b], 1);
+        atomicAdd(&hall[b], 1);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // the first digit's boundary bin for the B-th owned entry (as in
+        // bound_owned), and how many entries lie within it
+        int c8[8], sum = 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          c8[b] = hist[lane * 8 + b];
+          sum += c8[b];
+        }
+        int run = warp_excl_scan(sum, lane);
+        const int total = __shfl_sync(0xffffffffu, run + sum, 31);
+        int bs = 256;
+        if (total >= B) {
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            if (run < B && B <= run + c8[b]) bs = lane * 8 + b;
+            run += c8[b];
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bs = min(bs, __shfl_xor_sync(0xffffffffu, bs, o));
+        int within = 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) within += lane * 8 + b <= bs ? hall[lane * 8 + b] : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) within += __shfl_xor_sync(0xffffffffu, within, o);
+        if (lane == 0 && bs < 256 && within <= CAP) {
+          const uint32_t prefix = shift + 8 >= 32 ? 0u : (kmin >> (shift + 8)) << (shift + 8);
+          sh.tau = prefix | ((uint32_t)bs << shift) | ((1u << shift) - 1u);
+          sh.cut2 = 1;
+        }
+      }
+      __syncthreads();
+      if (sh.cut2) {
+        // every entry within that first bound; the others can neither be in
+        // the tree nor lead to it
+        const uint32_t tau0 = sh.tau;
+        for (int base = warp * 32; base < N1 + N2; base += THREADS) {
+          const int x = base + lane;
+          PE en;
+          bool want = false;
+          if (x < N1 + N2) {
+            make(x, en);
+            want = desc_key(en.score) <= tau0;
+          }
+          const int slot = warp_append(&sh.n_ent, want);
+          if (want) {
+            ent[slot] = en;
+            nxt[slot] = x < N1 ? (uint8_t)topk : 0;
+          }
+        }
+      } else {
+        for (int x = tid; x < N1; x += THREADS) {
+          PE en;
+          make(x, en);
+          ent[x] = en;
+          nxt[x] = 0;
+        }
+        if (tid == 0) sh.n_ent = N1;
+      }
+    } else {
+      for (int base = warp * 32; base < N1 + N2; base += THREADS) {
+        const int x = base + lane;
+        int bin = -1;
+        if (x < N1 + N2) {
+          PE en;
+          const bool own = make(x, en);
+          ent[x] = en;
+          nxt[x] = x < N1 && two ? (uint8_t)topk : 0;
+          if (own) bin = bin_of(en.score);
+        }
+        if (bin >= 0) atomicAdd(&hist[bin], 1);  // bins here are mostly distinct within a warp
+      }
+      if (tid == 0) sh.n_ent = N1 + N2;
     }
-    if (tid == 0) sh.n_ent = N1 + N2;
   }
   __syncthreads();
+  const bool cut2 = sh.cut2;
 
   // The bound: the B-th best score key among the owned entries (distinct
   // prefixes, each scoring no better than its mixture score), found to 8
@@ -752,7 +836,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   // ---------------------------------------------------- level expansion
   bool failed = false, tau_current = false;
   int n_cut = -1;  // pool size right after the last cut to the bound (-1: none yet)
-  for (int t = two ? 2 : 1; t < L && !failed; ++t) {
+  for (int t = two || cut2 ? 2 : 1; t < L && !failed; ++t) {
     if (tid == 0) sh.any = 0;
     int pass = 0;
     for (; pass < MAX_PASSES; ++pass) {
