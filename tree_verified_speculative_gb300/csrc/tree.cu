@@ -1193,15 +1193,20 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       }
     }
     if (real && tie) {
-      // keys below, then token order among the equal keys
+      // keys below, then token order among the equal keys: per run, the
+      // keys below its lower bound, then its block of equal keys
       lt = 0;
       const PE ea = ent[sel[ia]];
-      for (int b = 0; b < nruns * 32; ++b) {
-        const uint32_t kb = skk[b];
-        if (kb < key) {
-          ++lt;
-        } else if (kb == key && ra[b] != ia && ra[b] < ns && seq_cmp(c, ent[sel[ra[b]]], ea) < 0) {
-          ++lt;
+      for (int u = 0; u < nruns; ++u) {
+        const uint32_t *run = skk + u * 32;
+        int lo = 0;
+#pragma unroll
+        for (int st = 16; st > 0; st >>= 1) lo += run[lo + st - 1] < key ? st : 0;
+        lo += run[lo] < key ? 1 : 0;
+        lt += lo;
+        for (int p = lo; p < 32 && run[p] == key; ++p) {
+          const int b = u * 32 + p;
+          if (ra[b] != ia && ra[b] < ns && seq_cmp(c, ent[sel[ra[b]]], ea) < 0) ++lt;
         }
       }
     }
