@@ -199,7 +199,12 @@ int mfd_build_tree(const float *tk_logp, const int32_t *tk_tok, int n_req, int K
  * to the smaller v.  If a child of cur carries y the walk moves there,
  * otherwise y is the bonus token and the walk stops.
  *
- *   target_logits fp32 [n_req][B + 1][V]; only the rows on the walk are read
+ *   target_logits fp32 [n_req][B + 1][V]; only the rows on the walk are read.
+ *                 Device memory, or page-locked host memory mapped into the
+ *                 device's address space (cudaHostAlloc, or cudaHostRegister
+ *                 with mapping), which the walk reads in place: then only the
+ *                 rows on the walk cross the host link (NVLink-C2C on GB300).
+ *                 Pageable host memory -> MFD_ERR_INVALID_ARG.
  *   parent, token int32 [n_req][B + 1] and n_nodes int32 [n_req] from
  *                 mfd_build_tree (or any tree in that format)
  *   temperature   fp32 [n_req]  0 = greedy; < 0 or NaN -> MFD_ERR_INPUT

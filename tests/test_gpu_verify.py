@@ -189,3 +189,45 @@ def test_workspace_reuse_and_graph_replay():
     for _ in range(4):
         g.replay()
         check()
+
+
+def test_target_logits_in_pinned_host_memory():
+    """Target logits left in page-locked host memory are read in place (only
+    the rows on the walk cross the host link): the walks are the oracle's,
+    bit for bit those of device-resident logits; pageable host memory is
+    refused before any launch."""
+    import ctypes
+
+    rng = np.random.default_rng(77)
+    tree, futs = _trees(rng, 4, 8, 15, 16, 151936, 64)
+    t = _targets(rng, tree, futs, 151936, [0, 2, 4, 6])
+    temps, seeds = [0.0, 0.0, 1.0, 1.0], [5, 6, 7, 8]
+    n_req, N, V = t.shape
+    rd = mfd.Round(n_req, 1, 15, 1, N - 1, V)
+    rd.parent.copy_(torch.from_numpy(tree["parent"]))
+    rd.token.copy_(torch.from_numpy(tree["token"]))
+    rd.n_nodes.copy_(torch.from_numpy(tree["n_nodes"]))
+    temp = torch.tensor(np.asarray(temps, np.float32), device="cuda")
+    seed = torch.tensor(np.asarray(seeds, np.uint64).view(np.int64), device="cuda")
+    outs = []
+    for where in ("device", "pinned"):
+        tt = torch.from_numpy(t).cuda() if where == "device" else torch.from_numpy(t).pin_memory()
+        rd.status.zero_()
+        rd.verify(tt, temp, seed)
+        torch.cuda.synchronize()
+        assert status_of(rd) == 0
+        outs.append((np_(rd.accept_len), np_(rd.path_nodes), np_(rd.out_tokens)))
+    for a, b in zip(*outs):
+        np.testing.assert_array_equal(a, b)
+    exact = 0
+    for q in range(n_req):
+        o = oracle.verify(t[q], tree["parent"][q], tree["token"][q], int(tree["n_nodes"][q]), 15, temps[q], seeds[q])
+        exact += check_walk(int(outs[1][0][q]), outs[1][1][q], outs[1][2][q], *o, sampled=temps[q] > 0)
+    assert exact >= 3
+    pageable = np.ascontiguousarray(t)
+    lib = mfd.load()
+    rc = lib.mfd_verify(ctypes.c_void_p(pageable.ctypes.data), n_req, N - 1, V, 15, rd.parent.data_ptr(),
+                        rd.token.data_ptr(), rd.n_nodes.data_ptr(), temp.data_ptr(), seed.data_ptr(),
+                        rd.accept_len.data_ptr(), rd.path_nodes.data_ptr(), rd.out_tokens.data_ptr(),
+                        rd.status.data_ptr(), rd.ws.data_ptr(), rd.ws.numel(), None)
+    assert rc == mfd.MFD_ERR_INVALID_ARG

@@ -422,9 +422,24 @@ int mfd_verify(const float *target_logits, int n_req, int B, int V, int L, const
   int rc = current_device_info(&d);
   if (rc != MFD_OK) return rc;
   if (!ws || ws_bytes < verify_bytes(d.n_sm) || !aligned(ws, 256)) return MFD_ERR_WORKSPACE;
+  // the target logits: device memory, or page-locked host memory mapped into
+  // the device's address space, which the walk reads in place (only the rows
+  // on the walk cross the host link)
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, target_logits) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MFD_ERR_INVALID_ARG;
+  }
+  const float *t = target_logits;
+  if (pa.type == cudaMemoryTypeHost) {
+    if (!pa.devicePointer) return MFD_ERR_INVALID_ARG;
+    t = static_cast<const float *>(pa.devicePointer);
+  } else if (pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged) {
+    return MFD_ERR_INVALID_ARG;  // pageable host memory
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   mfd::VerifyLaunch Vl;
-  Vl.t = target_logits;
+  Vl.t = t;
   Vl.n_req = n_req;
   Vl.B = B;
   Vl.V = V;

@@ -92,6 +92,14 @@ def _p(t) -> int | None:
     return t.data_ptr()
 
 
+def _p_dev_or_pinned(t) -> int:
+    """A device tensor, or a page-locked host tensor (read in place by the
+    kernel through its mapped address)."""
+    assert isinstance(t, torch.Tensor) and t.is_contiguous() and (t.is_cuda or t.is_pinned()), \
+        "device or pinned host tensor, contiguous"
+    return t.data_ptr()
+
+
 def _s(stream) -> int | None:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -178,7 +186,7 @@ def mfd_build_tree(tk_logp, tk_tok, n_req, K, L, topk, B, anchor_tok, base_pos, 
 
 def mfd_verify(target_logits, n_req, B, V, L, parent, token, n_nodes, temperature, seed, accept_len,
                path_nodes, out_tokens, status, ws, stream=None) -> None:
-    rc = load().mfd_verify(_p(target_logits), n_req, B, V, L, _p(parent), _p(token), _p(n_nodes),
+    rc = load().mfd_verify(_p_dev_or_pinned(target_logits), n_req, B, V, L, _p(parent), _p(token), _p(n_nodes),
                            _p(temperature), _p(seed), _p(accept_len), _p(path_nodes), _p(out_tokens),
                            _p(status), _p(ws), ws.numel() * ws.element_size(), _s(stream))
     _check(rc, "mfd_verify")
