@@ -712,6 +712,8 @@ def profile_rounds(args, local):
         seed = torch.tensor(np.array([rounds[0].seed], np.uint64).view(np.int64), device=dev)
     Wd = W.to(dev)
     Wp = mfd.pack_lm_head(Wd)
+    del Wd  # the packed copy is all the rounds read; less device memory under the profiler
+    torch.cuda.empty_cache()
     rd = mfd.Round(n_req, cfg["K"], cfg["L"], cfg["topk"], cfg["B"], cfg["V"], device=dev)
     rd.status.zero_()
     for _ in range(args.profile_rounds):
