@@ -162,13 +162,16 @@ def test_pack_layout():
 
 
 @pytest.mark.parametrize("R,H,V,topk", [(120, 2560, 151936, 16), (37, 128, 1000, 8), (200, 256, 4099, 32),
-                                        (1, 64, 16, 1)])
+                                        (1, 64, 16, 1), (300, 128, 5000, 16), (3840, 2560, 151936, 16)])
 def test_packed_weight_bit_identical(R, H, V, topk):
-    """mfd_lmhead_topk_packed gives exactly mfd_lmhead_topk's results."""
+    """mfd_lmhead_topk_packed gives exactly mfd_lmhead_topk's results.  Above
+    128 rows the packed path runs in CTA pairs that multicast the weight
+    halves (300 rows: three M tiles, the last pair has an empty one; 3840:
+    32 requests of 120 rows)."""
     rng = np.random.default_rng(R + H + V)
     if V == 151936:
         W = synth.lm_head(V, H, seed=2024)
-        h = synth.round_inputs(W, 8, 15, 11, seed=3).h
+        h = torch.cat([synth.round_inputs(W, 8, 15, 11, seed=3 + q).h for q in range(R // 120)], 0)
     else:
         W = torch.from_numpy((rng.standard_normal((V, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16)
         h = torch.from_numpy(rng.standard_normal((R, H)).astype(np.float32)).to(torch.bfloat16)

@@ -12,6 +12,7 @@ struct LmheadLaunch {
   int R, H, V;
   int T;     // candidates kept per (row, range): 8, 16 or 32
   int P;     // vocabulary ranges (<= number of 256-row tiles)
+  bool pairs;  // packed weight, R > 128: clusters of two CTAs multicast each weight block
   int n_sm;  // persistent grid size
   void *part_ms;    // float2 [R][P]
   void *part_cand;  // int2 [R][P][T]

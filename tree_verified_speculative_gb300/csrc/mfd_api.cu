@@ -99,8 +99,28 @@ int tensor_map(const void *ptr, int rows, int cols, int box_rows, const CUtensor
 // ---------------------------------------------------------------- layouts
 struct TopkLayout {
   int P, T, chunk;
+  bool pairs;  // LM head: CTA pairs sharing each weight tile (packed weight only)
   size_t ms_bytes, cand_bytes, total;
 };
+
+// Fewest weight tiles for the busiest worker when n_groups M groups share
+// `workers` workers: over P vocabulary ranges, a worker takes
+// ceil(n_groups * P / workers) items of ceil(tiles / P) tiles.  Among equal
+// costs the fewest ranges win: fewer partials to merge and fewer top-T
+// restarts per row.
+static long long best_ranges(int tiles, int n_groups, int workers, int *P_out) {
+  long long best = -1;
+  const int pmax = tiles < 256 ? tiles : 256;
+  for (int P = 1; P <= pmax; ++P) {
+    const long long rounds = ((long long)n_groups * P + workers - 1) / workers;
+    const long long cost = rounds * ((tiles + P - 1) / P);
+    if (best < 0 || cost < best) {
+      best = cost;
+      *P_out = P;
+    }
+  }
+  return best;
+}
 
 TopkLayout lmhead_layout(int R, int V, int topk, int n_sm) {
   TopkLayout y;
@@ -108,20 +128,17 @@ TopkLayout lmhead_layout(int R, int V, int topk, int n_sm) {
   const int n_mt = (R + mfd::lmhead_m_rows() - 1) / mfd::lmhead_m_rows();
   y.P = tiles < n_sm ? tiles : n_sm;
   if (y.P > 256) y.P = 256;
+  y.pairs = false;
   if (n_mt > 1) {
-    // Work items are (range, M tile).  Take the number of ranges that gives
-    // the busiest CTA the fewest weight tiles, and among those the fewest
-    // ranges: fewer partials to merge and fewer top-T restarts per row.
-    long long best = -1;
-    const int pmax = tiles < 256 ? tiles : 256;
-    for (int P = 1; P <= pmax; ++P) {
-      const long long rounds = ((long long)n_mt * P + n_sm - 1) / n_sm;
-      const long long cost = rounds * ((tiles + P - 1) / P);
-      if (best < 0 || cost < best) {
-        best = cost;
-        y.P = P;
-      }
-    }
+    // Work items are (range, M tile) for single CTAs, or (range, pair of M
+    // tiles) for CTA pairs; pairs read each weight tile once from L2 between
+    // them, so they win ties.  The row-major weight path takes the same
+    // ranges with single CTAs.
+    int P1 = 1, P2 = 1;
+    const long long c1 = best_ranges(tiles, n_mt, n_sm, &P1);
+    const long long c2 = n_sm >= 2 ? best_ranges(tiles, (n_mt + 1) / 2, n_sm / 2, &P2) : c1 + 1;
+    y.pairs = c2 <= c1;
+    y.P = y.pairs ? P2 : P1;
   }
   y.T = cand_width(topk);
   y.chunk = 0;
@@ -137,6 +154,7 @@ TopkLayout logits_layout(int R, int V, int topk) {
   chunk = (chunk + 31) / 32 * 32;
   if (chunk < 1024) chunk = 1024;
   y.chunk = chunk;
+  y.pairs = false;
   y.P = (V + chunk - 1) / chunk;
   y.T = cand_width(topk);
   y.ms_bytes = align256((size_t)R * y.P * 8);
@@ -251,6 +269,7 @@ int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int 
   L.V = V;
   L.T = y.T;
   L.P = y.P;
+  L.pairs = y.pairs && !W;
   L.n_sm = d.n_sm;
   L.part_ms = base;
   L.part_cand = base + y.ms_bytes;
