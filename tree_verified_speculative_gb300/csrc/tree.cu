@@ -214,12 +214,6 @@ __device__ int seq_cmp(const Ctx &c, const PE &a, const PE &b) {
   return da - db;
 }
 
-__device__ __forceinline__ uint64_t seq_hash(const Ctx &c, const PE &e, int d, uint64_t seed) {
-  uint64_t h = 0x2545F4914F6CDD1Dull ^ seed;
-  for (int p = 1; p <= d; ++p) h = mix64(h ^ ((uint64_t)token_at(c, e, p) + ((uint64_t)p << 40)));
-  return h;
-}
-
 // The hash of the whole sequence and (in *hp) of the sequence without its
 // last token, which is the parent's hash.
 __device__ __forceinline__ uint64_t seq_hash2(const Ctx &c, const PE &e, int d, uint64_t seed, uint64_t *hp) {
