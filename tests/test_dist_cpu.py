@@ -75,3 +75,19 @@ def test_two_gloo_ranks():
     assert line["impl"] == "reference" and line["unit"] == "rounds/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert out1.strip() == ""
+
+
+@pytest.mark.timeout(300)
+def test_reference_arm_batched_workload():
+    """The reference arm on a batched workload (4 requests, per-request
+    temperatures): one line, the per-request work scaled by the batch."""
+    import subprocess
+
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                          "--warmup", "0", "--workload", "r4_tiny_mixed"], capture_output=True, text=True,
+                         timeout=280, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["config"]["n_req"] == 4 and line["value"] > 0
+    assert "scaled x4" in line["cpu_baseline"]["sample"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
