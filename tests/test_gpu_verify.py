@@ -231,3 +231,30 @@ def test_target_logits_in_pinned_host_memory():
                         rd.accept_len.data_ptr(), rd.path_nodes.data_ptr(), rd.out_tokens.data_ptr(),
                         rd.status.data_ptr(), rd.ws.data_ptr(), rd.ws.numel(), None)
     assert rc == mfd.MFD_ERR_INVALID_ARG
+
+
+def test_sampled_coverage_identity():
+    """Over many seeds the GPU's sampled walks accept, on average, the tree's
+    covered target mass (project page, How it works, step 1: the accepted
+    length is the probability mass the tree covers):
+    E = sum over nodes of the product of softmax(t / T) along the path."""
+    rng = np.random.default_rng(21)
+    parent = np.array([-1, 0, 0, 1, 1, 2, 3, 3, 6], np.int32)
+    token = np.array([0, 1, 3, 0, 2, 4, 1, 3, 2], np.int32)
+    N, V, L, T, n_req = 9, 4096, 3, 1.0, 2048
+    t = rng.normal(0, 1.0, size=(N, V)).astype(np.float32)
+    for n in range(1, N):
+        t[parent[n], token[n]] += 7.0  # the tree's tokens carry real mass
+    p = np.exp(t.astype(np.float64) / T)
+    p /= p.sum(axis=1, keepdims=True)
+    reach = np.zeros(N)
+    reach[0] = 1.0
+    for n in range(1, N):
+        reach[n] = reach[parent[n]] * p[parent[n], token[n]]
+    expect = reach[1:].sum()
+    acc, _, _, st = _gpu_verify(np.tile(t, (n_req, 1, 1)), np.tile(parent, (n_req, 1)), np.tile(token, (n_req, 1)),
+                                [N] * n_req, L, [T] * n_req, [s * 7919 + 3 for s in range(n_req)])
+    assert st == 0
+    se = acc.std() / np.sqrt(n_req)
+    assert 0.3 < expect < 2.5
+    assert abs(acc.mean() - expect) < 4 * se, (acc.mean(), expect, se)
