@@ -742,7 +742,12 @@ def main():
     else:
         out = run_gpu(args, ws, rank, local)
     if rank == 0:
-        print(json.dumps(out))
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        barrier(ws)
+        dist.destroy_process_group()
 
 
 if __name__ == "__main__":
