@@ -34,6 +34,10 @@ WORKLOADS = {
     "k8_l15_h2560_v151936_b256_t1": dict(K=8, L=15, H=2560, V=151936, n_shared=11, topk=16, B=256, T=1.0),
     "k8_l15_h2560_v151936_b64_greedy": dict(K=8, L=15, H=2560, V=151936, n_shared=11, topk=16, B=64, T=0.0),
     "k8_l15_h5120_v248320_b256_greedy": dict(K=8, L=15, H=5120, V=248320, n_shared=13, topk=32, B=256, T=0.0),
+    # the default workload with a 65,536-token draft vocabulary: the drafter's
+    # head covers a subset of the vocabulary, the walk verifies the full one
+    "k8_l15_h2560_v151936_sub65536_b256_t1": dict(K=8, L=15, H=2560, V=151936, V_draft=65536, n_shared=11,
+                                                  topk=16, B=256, T=1.0),
     # a small shape for quick host-side runs (the reference arm in CPU tests)
     "tiny": dict(K=2, L=4, H=64, V=512, n_shared=2, topk=8, B=16, T=1.0),
     # 32 requests in one round (3840 LM-head rows, one shared W): the
@@ -174,16 +178,52 @@ def barrier(ws):
 
 
 # ---------------------------------------------------------------------------
+def draft_vocab(cfg):
+    """The draft vocabulary's ids (increasing) for a subset-head workload, else None."""
+    from tree_verified_speculative_gb300 import synth
+
+    if not cfg.get("V_draft"):
+        return None
+    return synth.vocab_subset(cfg["V"], cfg["V_draft"], seed=W_SEED + 7)
+
+
+class DraftHead:
+    """The drafter's LM head as the rounds stream it: W packed once (as at
+    model load), over the whole vocabulary or over a draft-vocabulary subset
+    with its id table."""
+
+    def __init__(self, cfg, W, dev):
+        import torch
+
+        from tree_verified_speculative_gb300 import mfd
+
+        self.ids = draft_vocab(cfg)
+        self.W_host = W if self.ids is None else W[torch.from_numpy(self.ids.astype(np.int64))].contiguous()
+        self.V = self.W_host.shape[0]
+        Wd = self.W_host.to(dev)
+        self.Wp = mfd.pack_lm_head(Wd)
+        del Wd
+        self.ids_d = None if self.ids is None else torch.from_numpy(self.ids).to(dev)
+        self.name = "mfd_lmhead_topk_packed" if self.ids is None else "mfd_lmhead_topk_subset"
+
+    def __call__(self, rd, h):
+        if self.ids_d is None:
+            rd.lmhead_topk_packed(h, self.Wp)
+        else:
+            rd.lmhead_topk_subset(h, self.Wp, self.ids_d)
+
+
 def make_inputs(cfg, n_rounds, rank):
     import concurrent.futures as cf
 
     from tree_verified_speculative_gb300 import synth
 
     W = synth.lm_head(cfg["V"], cfg["H"], seed=W_SEED)
+    vocab = draft_vocab(cfg)
     base = 1_000_000 * (rank + 1)
     with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
-        rounds = list(ex.map(lambda r: synth.round_inputs(W, cfg["K"], cfg["L"], cfg["n_shared"], seed=base + r),
-                             range(n_rounds)))
+        rounds = list(ex.map(lambda r: synth.round_inputs(W, cfg["K"], cfg["L"], cfg["n_shared"], seed=base + r,
+                                                          vocab=vocab), range(n_rounds)))
     rng = np.random.default_rng(base + 999)
     noise = [synth.target_noise(cfg["B"] + 1, cfg["V"], rng) for _ in range(N_NOISE)]
     return W, rounds, noise
@@ -201,8 +241,7 @@ def run_gpu(args, ws, rank, local):
     R = K * L
     n_rounds = args.warmup + args.steps
     W, rounds, noise = make_inputs(cfg, n_rounds, rank)
-    Wd = W.to(dev)
-    Wp = mfd.pack_lm_head(Wd)  # once, as at model load: the streamed weight layout
+    head = DraftHead(cfg, W, dev)  # packed once, as at model load: the streamed weight layout
     h_all = torch.stack([r.h for r in rounds]).to(dev)
     # the drafter writes its hidden states into the same buffer every round;
     # each round's are staged there before its timed interval
@@ -210,7 +249,7 @@ def run_gpu(args, ws, rank, local):
     t_dev = [torch.from_numpy(x).to(dev) for x in noise]
     temp = torch.tensor([T], dtype=torch.float32, device=dev)
     seeds = torch.tensor(np.array([r.seed for r in rounds], np.uint64).view(np.int64), device=dev)
-    rd = mfd.Round(1, K, L, topk, B, V, device=dev)
+    rd = mfd.Round(1, K, L, topk, B, V, device=dev, V_draft=head.V)
     rd.status.zero_()
     N = B + 1
     acc_buf = torch.zeros((n_rounds,), dtype=torch.int32, device=dev)
@@ -239,7 +278,7 @@ def run_gpu(args, ws, rank, local):
                 e0, ea, e1 = ev[i][0], ev[i][1], ev[i][2]
                 h_cur.copy_(h_all[i])
                 e0.record(stream)
-                rd.lmhead_topk_packed(h_cur, Wp)
+                head(rd, h_cur)
                 if split:
                     ea.record(stream)
                 rd.build_tree()
@@ -324,12 +363,12 @@ def run_gpu(args, ws, rank, local):
     sites = {**sites_t}
 
     # ------------------------------------------------------------ e2e
-    e2e = run_e2e(args, cfg, rounds, noise, sites, Wp, rd, dev)
+    e2e = run_e2e(args, cfg, rounds, noise, sites, head, rd, dev)
 
     # ------------------------------------------------------------ roofline
     peak, peak_kind = peaks()
     lm_us = lm / steps * 1e3
-    algo_bytes = V * H * 2 + R * H * 2
+    algo_bytes = head.V * H * 2 + R * H * 2
     achieved = algo_bytes / (lm_us * 1e-6) / 1e9
     traffic = profiled_traffic()
     out = {
@@ -338,7 +377,8 @@ def run_gpu(args, ws, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "K": K, "L": L, "H": H, "V": V, "topk": topk, "B": B,
                    "temperature": T, "n_req": 1, "parallelism": f"replicas{ws}" if ws > 1 else "single",
-                   "lm_head_weight": "packed once before timing (mfd_lmhead_pack), streamed by mfd_lmhead_topk_packed",
+                   **({"V_draft": head.V} if head.ids is not None else {}),
+                   "lm_head_weight": f"packed once before timing (mfd_lmhead_pack), streamed by {head.name}",
                    "l2": "inputs larger than L2 (W = %.0f MB streamed every round)" % (V * H * 2 / 1e6),
                    "timing": "sum over the timed rounds of two CUDA-event intervals per round, one around the LM head and the tree (back to back, as in a real round) and one around the verification, with the queue kept ahead of the GPU; the target plant (input generation that needs the round's tree) is untimed; the per-stage split comes from separate diagnostic rounds"},
         "stages_us": {"lmhead_topk_plus_build_tree": round(ab / steps * 1e3, 2), "verify": round(vf / steps * 1e3, 2),
@@ -347,7 +387,7 @@ def run_gpu(args, ws, rank, local):
                                                        "rounds": len(diag)}},
         "stages_us_median": med,
         "mean_accept_len": round(float(acc.mean()), 4),
-        "roofline": {"kernel": "mfd_lmhead_topk_packed (lmhead_topk_kernel + merge_topk_kernel)", "bound": "hbm",
+        "roofline": {"kernel": f"{head.name} (lmhead_topk_kernel + merge_topk_kernel)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": algo_bytes, "traffic": traffic},
@@ -357,7 +397,7 @@ def run_gpu(args, ws, rank, local):
         "e2e": e2e,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(cfg, W, rounds[args.warmup], rd, noise, sites[args.warmup])
+        out["cpu_baseline"] = cpu_baseline(cfg, head, rounds[args.warmup], rd, noise, sites[args.warmup])
     return out
 
 
@@ -531,7 +571,7 @@ def run_gpu_batched(args, ws, rank, local):
     }
 
 
-def run_e2e(args, cfg, rounds, noise, sites, Wp, rd, dev):
+def run_e2e(args, cfg, rounds, noise, sites, head, rd, dev):
     """Same rounds through the public API from pinned host buffers, all
     inside the timed interval: the round's hidden states are copied to the
     device; the target logits stay in page-locked host memory, where the walk
@@ -562,7 +602,7 @@ def run_e2e(args, cfg, rounds, noise, sites, Wp, rd, dev):
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         h_d.copy_(h_pin[i], non_blocking=True)
-        rd.lmhead_topk_packed(h_d, Wp)
+        head(rd, h_d)
         rd.build_tree()
         rd.verify(t_pin[i][None], temp, seeds[i:i + 1])
         out_pin[0:1].copy_(rd.accept_len, non_blocking=True)
@@ -579,7 +619,7 @@ def run_e2e(args, cfg, rounds, noise, sites, Wp, rd, dev):
             "d2h_bytes_per_step": int((1 + rd.L + 1) * 4)}
 
 
-def cpu_baseline(cfg, W, r, rd, noise, site):
+def cpu_baseline(cfg, head, r, rd, noise, site):
     """The oracle as it stands, on this machine's host cores, on one full
     round of the workload (LM head + log-softmax + top-k for all rows, the
     tree from those tables, the verification walk)."""
@@ -592,11 +632,13 @@ def cpu_baseline(cfg, W, r, rd, noise, site):
     K, L, topk, B, V, T = cfg["K"], cfg["L"], cfg["topk"], cfg["B"], cfg["V"], cfg["T"]
     R = K * L
     rows = R
-    hb, wb = bits(r.h[:rows]), bits(W)
+    hb, wb = bits(r.h[:rows]), bits(head.W_host)
     oracle.build()
     t0 = time.perf_counter()
     lp, tk, _ = oracle.lmhead_topk(hb, wb, topk)
     t_lm = (time.perf_counter() - t0) * (R / rows)
+    if head.ids is not None:
+        tk = head.ids[tk]  # draft-vocabulary rows to vocabulary ids
     lp, tk = lp.reshape(K, L, topk), tk.reshape(K, L, topk)
     t0 = time.perf_counter()
     tr = oracle.build_tree(lp, tk, B)
@@ -631,6 +673,10 @@ def run_reference(args, ws, rank):
     oracle.build()
     bits = lambda x: x.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
     W = synth.lm_head(V, H, seed=W_SEED)
+    ids = draft_vocab(cfg)
+    if ids is not None:  # the drafter's head covers the draft vocabulary only
+        W = W[torch.from_numpy(ids.astype(np.int64))].contiguous()
+    V_lm = W.shape[0]
     wb = bits(W)
     n_steps = args.warmup + args.steps
     budget_s = 150.0 / max(1, n_steps)  # whole run within a few minutes
@@ -639,18 +685,18 @@ def run_reference(args, ws, rank):
     t0 = time.perf_counter()
     oracle.lmhead_logits(bits(r0.h), wb, 0, 4096)
     per_vocab = (time.perf_counter() - t0) / 4096
-    n_v = int(max(256, min(V, 0.5 * budget_s / max(per_vocab, 1e-9))))
-    z_row = np.random.default_rng(3).standard_normal((1, V)).astype(np.float32)
+    n_v = int(max(256, min(V_lm, 0.5 * budget_s / max(per_vocab, 1e-9))))
+    z_row = np.random.default_rng(3).standard_normal((1, V_lm)).astype(np.float32)
     noise = synth.target_noise(B + 1, V, np.random.default_rng(11))
     times = []
     for s in range(n_steps):
         r = synth.round_inputs(W, K, L, n_shared, seed=2_000_000 + s)
         T = temps[s % len(temps)]
         hb = bits(r.h)
-        v0 = (s * 9973) % max(1, V - n_v)
+        v0 = (s * 9973) % max(1, V_lm - n_v)
         t0 = time.perf_counter()
         oracle.lmhead_logits(hb, wb, v0, v0 + n_v)
-        t_lm = (time.perf_counter() - t0) * V / n_v
+        t_lm = (time.perf_counter() - t0) * V_lm / n_v
         t0 = time.perf_counter()
         oracle.logits_topk(z_row, topk)
         t_sort = (time.perf_counter() - t0) * R
@@ -678,7 +724,7 @@ def run_reference(args, ws, rank):
             "config": {"workload": args.workload, "K": K, "L": L, "H": H, "V": V, "topk": topk, "B": B,
                        "temperature": temps[0] if n_req == 1 else "per request", "n_req": n_req},
             "cpu_baseline": {"value": round(value, 4), "unit": "rounds/s", "cores": cores, "kind": "oracle",
-                             "sample": f"per step: LM head on {n_v} of {V} vocabulary rows for all {R} rows "
+                             "sample": f"per step: LM head on {n_v} of {V_lm} draft-head rows for all {R} rows "
                                        f"(scaled), one full-row log-softmax+top-k (scaled x{R}), full tree and "
                                        "verification walk" + (f"; one request, scaled x{n_req}" if n_req > 1 else "")},
             "e2e": {"value": round(value, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -710,14 +756,13 @@ def profile_rounds(args, local):
         t = torch.from_numpy(noise[0]).to(dev)
         temp = torch.tensor([cfg["T"]], dtype=torch.float32, device=dev)
         seed = torch.tensor(np.array([rounds[0].seed], np.uint64).view(np.int64), device=dev)
-    Wd = W.to(dev)
-    Wp = mfd.pack_lm_head(Wd)
-    del Wd  # the packed copy is all the rounds read; less device memory under the profiler
+    head = DraftHead(cfg, W, dev)  # the packed copy is all the rounds read
+    del W
     torch.cuda.empty_cache()
-    rd = mfd.Round(n_req, cfg["K"], cfg["L"], cfg["topk"], cfg["B"], cfg["V"], device=dev)
+    rd = mfd.Round(n_req, cfg["K"], cfg["L"], cfg["topk"], cfg["B"], cfg["V"], device=dev, V_draft=head.V)
     rd.status.zero_()
     for _ in range(args.profile_rounds):
-        rd.lmhead_topk_packed(h, Wp)
+        head(rd, h)
         rd.build_tree()
         rd.verify(t, temp, seed)
     torch.cuda.synchronize()

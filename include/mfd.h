@@ -127,6 +127,25 @@ int mfd_lmhead_topk_packed(const void *h, int R, int H, const void *W_packed, in
                            float *tk_logp, int32_t *tk_tok, float *lse, int32_t *status, void *ws,
                            size_t ws_bytes, mfd_stream_t stream);
 
+/* Draft-vocabulary subset head (project page "Multi-Future Drafting", In a
+ * serving engine: the serving build drafts only over the target's most
+ * frequent tokens, about 64K of them, while the walk still checks against
+ * every token, so the output distribution is the target's).  As
+ * mfd_lmhead_topk_packed over the subset:
+ *   W_packed     the packed (mfd_lmhead_pack) weight of the V_sub subset rows
+ *   vocab_ids    int32 [V_sub] device: the vocabulary id of each subset row,
+ *                strictly increasing, each in [0, V_full)
+ * The log-softmax and top-k are over the subset (the drafter's
+ * distribution); tk_tok holds vocabulary ids (vocab_ids[row]), in the order
+ * (log p desc, id asc).  A mapped id outside [0, V_full) sets MFD_ERR_INPUT
+ * in *status and is written as -1; a table that is not increasing gives ties
+ * in subset order.  Workspace: mfd_workspace_size(MFD_OP_LMHEAD_TOPK, ...)
+ * with V = V_sub.  Errors: as mfd_lmhead_topk_packed; NULL vocab_ids or
+ * V_full < V_sub -> MFD_ERR_INVALID_ARG. */
+int mfd_lmhead_topk_subset(const void *h, int R, int H, const void *W_packed, int V_sub, const int32_t *vocab_ids,
+                           int V_full, int topk, float *tk_logp, int32_t *tk_tok, float *lse, int32_t *status,
+                           void *ws, size_t ws_bytes, mfd_stream_t stream);
+
 /* Log-softmax and top-k of fp32 logits given directly (no LM head): the
  * same outputs as mfd_lmhead_topk with z = logits [R][V].  Non-finite logits
  * are the caller's responsibility. */

@@ -138,3 +138,45 @@ def test_batched_32_requests(head):
         exact += check_walk(int(np_(rd.accept_len)[q]), np_(rd.path_nodes)[q], np_(rd.out_tokens)[q], *oa,
                             sampled=temps[q] > 0)
     assert exact >= 30
+
+
+@pytest.mark.parametrize("temperature", [0.0, 1.0])
+def test_subset_head_rounds(head, temperature):
+    """Rounds with a 65,536-token draft vocabulary (project page "Multi-Future
+    Drafting", In a serving engine): the drafter's head is the subset's rows
+    of W, its futures lie in the subset, and the walk verifies against the
+    target's full 151,936-token rows.  Tables against the oracle on the
+    subset rows (ids looked up), the tree bit-exact, the walk exact."""
+    W, _ = head
+    ids = synth.vocab_subset(151936, 65536, seed=64)
+    Wsub = W[torch.from_numpy(ids.astype(np.int64))].contiguous()
+    Wp = mfd.pack_lm_head(Wsub.cuda())
+    ids_d = torch.from_numpy(ids).cuda()
+    rd = mfd.Round(1, 8, 15, 16, 256, 151936, V_draft=65536)
+    exact = 0
+    for i in range(3):
+        r = synth.round_inputs(W, 8, 15, 11, seed=700 + i, vocab=ids)
+        assert np.isin(r.fut, ids).all()
+        rd.status.zero_()
+        rd.lmhead_topk_subset(r.h.cuda(), Wp, ids_d)
+        rd.build_tree()
+        torch.cuda.synchronize()
+        assert int(rd.status.item()) == 0
+        lp, tk = np_(rd.tk_logp), np_(rd.tk_tok)
+        rows = np.arange(i, 120, 17)
+        o_lp, o_idx, _ = oracle.lmhead_topk(_bits(r.h[rows]), _bits(Wsub), 16)
+        check_topk(lp[rows], tk[rows], o_lp, ids[o_idx])
+        g = tree_outputs(rd)
+        o = oracle.build_tree(lp.reshape(8, 15, 16), tk.reshape(8, 15, 16), 256)
+        assert_tree_equal(g, o, 0)
+        noise = synth.target_noise(257, 151936, np.random.default_rng(r.seed % (2**32)))
+        prow, pcol = synth.plant_sites(o["parent"], o["token"], o["depth"], int(o["n_nodes"]), r.fut[r.target_mode])
+        t = synth.plant(noise, prow, pcol)
+        rd.verify(torch.from_numpy(t[None]).cuda(), torch.tensor([temperature], device="cuda"),
+                  torch.tensor([r.seed], dtype=torch.int64, device="cuda"))
+        torch.cuda.synchronize()
+        assert int(rd.status.item()) == 0
+        oa = oracle.verify(t, o["parent"], o["token"], int(o["n_nodes"]), 15, temperature, r.seed)
+        exact += check_walk(int(np_(rd.accept_len)[0]), np_(rd.path_nodes)[0], np_(rd.out_tokens)[0], *oa,
+                            sampled=temperature > 0)
+    assert exact >= 2

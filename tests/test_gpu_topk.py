@@ -188,3 +188,49 @@ def test_packed_weight_bit_identical(R, H, V, topk):
     np.testing.assert_array_equal(np_(a.tk_tok), np_(b.tk_tok))
     np.testing.assert_array_equal(np_(a.tk_logp).view(np.uint32), np_(b.tk_logp).view(np.uint32))
     np.testing.assert_array_equal(np_(a.lse).view(np.uint32), np_(b.lse).view(np.uint32))
+
+
+@pytest.mark.parametrize("R", [120, 300])
+def test_subset_head(R):
+    """Draft-vocabulary subset head (project page "Multi-Future Drafting", In
+    a serving engine): the LM head, log-softmax and top-k over the subset's
+    rows, with tokens written as vocabulary ids.  Exactly the packed head on
+    the subset rows with the ids looked up, and the oracle's top-k on sampled
+    rows.  300 rows run in CTA pairs."""
+    rng = np.random.default_rng(R + 7)
+    V_full, H, n_sub, topk = 20000, 256, 4096, 16
+    ids = synth.vocab_subset(V_full, n_sub, seed=R)
+    assert np.all(np.diff(ids) > 0)
+    W = torch.from_numpy((rng.standard_normal((V_full, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16)
+    Wsub = W[torch.from_numpy(ids.astype(np.int64))].contiguous()
+    h = torch.from_numpy(rng.standard_normal((R, H)).astype(np.float32)).to(torch.bfloat16)
+    Wp = mfd.pack_lm_head(Wsub.cuda())
+    a = mfd.Round(1, 1, R, topk, 1, V_full, V_draft=n_sub)
+    b = mfd.Round(1, 1, R, topk, 1, n_sub)
+    a.status.zero_()
+    b.status.zero_()
+    a.lmhead_topk_subset(h.cuda(), Wp, torch.from_numpy(ids).cuda())
+    b.lmhead_topk_packed(h.cuda(), Wp)
+    torch.cuda.synchronize()
+    assert status_of(a) == 0 and status_of(b) == 0
+    np.testing.assert_array_equal(np_(a.tk_tok), ids[np_(b.tk_tok)])
+    np.testing.assert_array_equal(np_(a.tk_logp).view(np.uint32), np_(b.tk_logp).view(np.uint32))
+    np.testing.assert_array_equal(np_(a.lse).view(np.uint32), np_(b.lse).view(np.uint32))
+    rows = np.array([0, 1, R // 2, R - 1])
+    o_lp, o_idx, _ = oracle.lmhead_topk(_bits(h[rows]), _bits(Wsub), topk)
+    check_topk(np_(a.tk_logp)[rows], np_(a.tk_tok)[rows], o_lp, ids[o_idx])
+
+
+def test_subset_head_rejects_ids_out_of_range():
+    """A vocabulary id at or past V_full sets MFD_ERR_INPUT and is written as -1."""
+    rng = np.random.default_rng(3)
+    V_full, H, n_sub, topk = 5000, 128, 1024, 8
+    ids = synth.vocab_subset(V_full, n_sub, seed=4) + V_full  # every id out of range
+    W = torch.from_numpy((rng.standard_normal((n_sub, H)) / np.sqrt(H)).astype(np.float32)).to(torch.bfloat16)
+    h = torch.from_numpy(rng.standard_normal((16, H)).astype(np.float32)).to(torch.bfloat16)
+    a = mfd.Round(1, 1, 16, topk, 1, V_full, V_draft=n_sub)
+    a.status.zero_()
+    a.lmhead_topk_subset(h.cuda(), mfd.pack_lm_head(W.cuda()), torch.from_numpy(ids.astype(np.int32)).cuda())
+    torch.cuda.synchronize()
+    assert status_of(a) == mfd.MFD_ERR_INPUT
+    assert np.all(np_(a.tk_tok) == -1)

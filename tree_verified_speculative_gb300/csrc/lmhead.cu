@@ -84,20 +84,22 @@ __device__ __forceinline__ void item_range(const Params &p, int item, int rank, 
 }
 
 // Insert (x, v) into the sorted (value desc, id asc) list; the caller has
-// checked that x beats the last entry.
+// checked that x beats the last entry.  Its place is the number of entries
+// before it, and every entry from there on moves down one: T independent
+// compares and T independent selects, not a chain of T compare-swaps.
 template <int T>
 __device__ __forceinline__ void topk_insert(float (&tv)[T], int (&ti)[T], float x, int v) {
-  float cv = x;
-  int ci = v;
+  int pos = 0;
 #pragma unroll
-  for (int s = 0; s < T; ++s) {
-    const bool sw = vi_before(cv, ci, tv[s], ti[s]);
-    const float ov = tv[s];
-    const int oi = ti[s];
-    tv[s] = sw ? cv : ov;
-    ti[s] = sw ? ci : oi;
-    cv = sw ? ov : cv;
-    ci = sw ? oi : ci;
+  for (int s = 0; s < T; ++s) pos += vi_before(tv[s], ti[s], x, v) ? 1 : 0;
+#pragma unroll
+  for (int s = T - 1; s > 0; --s) {  // tv[s - 1] is still the old entry here
+    tv[s] = s > pos ? tv[s - 1] : (s == pos ? x : tv[s]);
+    ti[s] = s > pos ? ti[s - 1] : (s == pos ? v : ti[s]);
+  }
+  if (pos == 0) {
+    tv[0] = x;
+    ti[0] = v;
   }
 }
 

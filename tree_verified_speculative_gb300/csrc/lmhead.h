@@ -36,6 +36,10 @@ struct MergeLaunch {
   int32_t *tk_tok;
   float *lse;  // may be NULL
   int32_t *status;
+  // draft-vocabulary subset: candidate ids are rows of the subset weight and
+  // are written as vocab_ids[id] (ids in [0, V_full)); null: written as is
+  const int32_t *vocab_ids;
+  int V_sub, V_full;
 };
 cudaError_t launch_merge_topk(const MergeLaunch &M, cudaStream_t stream);
 

@@ -243,8 +243,11 @@ size_t mfd_workspace_size(int op, int n_req, int K, int L, int topk, int B, int 
 namespace {
 // The LM head call, from the row-major weight (W, through its tensor map) or
 // from the packed weight (Wp).
+// vocab_ids: null, or the draft-vocabulary subset (V rows of the weight are
+// vocabulary ids vocab_ids[0..V), increasing, below V_full)
 int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int V, int topk, float *tk_logp,
-                int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes, mfd_stream_t stream) {
+                int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes, mfd_stream_t stream,
+                const int32_t *vocab_ids = nullptr, int V_full = 0) {
   if (!h || (!W && !Wp) || !tk_logp || !tk_tok || !status || R < 1 || H < 1 || V < 1 || topk < 1)
     return MFD_ERR_INVALID_ARG;
   if (!aligned(h, 16) || (W && !aligned(W, 16)) || (Wp && !aligned(Wp, 256))) return MFD_ERR_INVALID_ARG;
@@ -287,6 +290,9 @@ int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int 
   M.tk_tok = tk_tok;
   M.lse = lse;
   M.status = status;
+  M.vocab_ids = vocab_ids;
+  M.V_sub = V;
+  M.V_full = vocab_ids ? V_full : V;
   return cuda_status(mfd::launch_merge_topk(M, s));
 }
 }  // namespace
@@ -325,6 +331,15 @@ int mfd_lmhead_topk_packed(const void *h, int R, int H, const void *W_packed, in
   return lmhead_call(h, R, H, nullptr, W_packed, V, topk, tk_logp, tk_tok, lse, status, ws, ws_bytes, stream);
 }
 
+int mfd_lmhead_topk_subset(const void *h, int R, int H, const void *W_packed, int V_sub, const int32_t *vocab_ids,
+                           int V_full, int topk, float *tk_logp, int32_t *tk_tok, float *lse, int32_t *status,
+                           void *ws, size_t ws_bytes, mfd_stream_t stream) {
+  if (!W_packed || !vocab_ids || !aligned(vocab_ids, 4)) return MFD_ERR_INVALID_ARG;
+  if (V_full < V_sub || V_full >= (1 << 30)) return MFD_ERR_INVALID_ARG;
+  return lmhead_call(h, R, H, nullptr, W_packed, V_sub, topk, tk_logp, tk_tok, lse, status, ws, ws_bytes, stream,
+                     vocab_ids, V_full);
+}
+
 int mfd_logits_topk(const float *logits, int R, int V, int topk, float *tk_logp, int32_t *tk_tok, float *lse,
                     int32_t *status, void *ws, size_t ws_bytes, mfd_stream_t stream) {
   if (!logits || !tk_logp || !tk_tok || !status || R < 1 || V < 1 || topk < 1) return MFD_ERR_INVALID_ARG;
@@ -355,6 +370,8 @@ int mfd_logits_topk(const float *logits, int R, int V, int topk, float *tk_logp,
   M.tk_tok = tk_tok;
   M.lse = lse;
   M.status = status;
+  M.vocab_ids = nullptr;
+  M.V_sub = M.V_full = V;
   return cuda_status(mfd::launch_merge_topk(M, s));
 }
 
@@ -391,6 +408,8 @@ int mfd_logits_topk_noalloc(const float *logits, int R, int V, int topk, float *
   M.tk_tok = tk_tok;
   M.lse = lse;
   M.status = status;
+  M.vocab_ids = nullptr;
+  M.V_sub = M.V_full = V;
   return cuda_status(mfd::launch_merge_topk(M, s));
 }
 

@@ -53,7 +53,8 @@ __device__ __forceinline__ Cand warp_best(Cand c) {
 template <int T>
 __global__ void __launch_bounds__(MERGE_THREADS)
     merge_topk_kernel(const float2 *__restrict__ part_ms, const int2 *__restrict__ part_cand, int R, int P,
-                      int topk, float *__restrict__ tk_logp, int32_t *__restrict__ tk_tok, float *__restrict__ lse_out) {
+                      int topk, float *__restrict__ tk_logp, int32_t *__restrict__ tk_tok, float *__restrict__ lse_out,
+                      const int32_t *__restrict__ vocab_ids, int V_sub, int V_full, int32_t *status) {
   __shared__ Cand surv[SURV_CAP];
   __shared__ Cand top[32];
   __shared__ Cand gbest[MERGE_WARPS][32];
@@ -222,8 +223,18 @@ __global__ void __launch_bounds__(MERGE_THREADS)
       if (o == tid) continue;
       r2 += vi_before(top[o].v - lse, top[o].i, lp, e.i);
     }
+    int tok = e.i;
+    if (vocab_ids) {
+      // a subset row index back to its vocabulary id; the table is
+      // increasing, so (log p desc, subset index asc) is (log p desc, id asc)
+      tok = (tok >= 0 && tok < V_sub) ? __ldg(vocab_ids + tok) : -1;
+      if (tok < 0 || tok >= V_full) {
+        report(status, MFD_ERR_INPUT);
+        tok = -1;
+      }
+    }
     tk_logp[(size_t)row * topk + r2] = lp;
-    tk_tok[(size_t)row * topk + r2] = e.i;
+    tk_tok[(size_t)row * topk + r2] = tok;
   }
   if (tid == 0 && lse_out) lse_out[row] = lse;
 }
@@ -311,7 +322,8 @@ cudaError_t merge_t(const MergeLaunch &M, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, merge_topk_kernel<T>, reinterpret_cast<const float2 *>(M.part_ms),
-                         reinterpret_cast<const int2 *>(M.part_cand), M.R, M.P, M.topk, M.tk_logp, M.tk_tok, M.lse);
+                         reinterpret_cast<const int2 *>(M.part_cand), M.R, M.P, M.topk, M.tk_logp, M.tk_tok, M.lse,
+                         M.vocab_ids, M.V_sub, M.V_full, M.status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

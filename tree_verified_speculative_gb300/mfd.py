@@ -31,7 +31,8 @@ MFD_OP_BUILD_TREE = 2
 MFD_OP_VERIFY = 3
 
 EXPORTS = ("mfd_status_string", "mfd_workspace_size", "mfd_lmhead_topk", "mfd_lmhead_packed_bytes",
-           "mfd_lmhead_pack", "mfd_lmhead_topk_packed", "mfd_logits_topk", "mfd_logits_topk_noalloc",
+           "mfd_lmhead_pack", "mfd_lmhead_topk_packed", "mfd_lmhead_topk_subset", "mfd_logits_topk",
+           "mfd_logits_topk_noalloc",
            "mfd_build_tree", "mfd_verify")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -68,6 +69,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.mfd_lmhead_pack.restype = I
         lib.mfd_lmhead_topk_packed.argtypes = [P, I, I, P, I, I, P, P, P, P, P, SZ, P]
         lib.mfd_lmhead_topk_packed.restype = I
+        lib.mfd_lmhead_topk_subset.argtypes = [P, I, I, P, I, P, I, I, P, P, P, P, P, SZ, P]
+        lib.mfd_lmhead_topk_subset.restype = I
         lib.mfd_logits_topk.argtypes = [P, I, I, I, P, P, P, P, P, SZ, P]
         lib.mfd_logits_topk.restype = I
         lib.mfd_logits_topk_noalloc.argtypes = [P, I, I, I, P, P, P, P, P]
@@ -157,6 +160,18 @@ def mfd_lmhead_topk_packed(h, W_packed, V, topk, tk_logp, tk_tok, lse, status, w
     _check(rc, "mfd_lmhead_topk_packed")
 
 
+def mfd_lmhead_topk_subset(h, W_packed, vocab_ids, V_full, topk, tk_logp, tk_tok, lse, status, ws,
+                           stream=None) -> None:
+    """The LM head over a draft-vocabulary subset: W_packed holds the packed
+    rows of the subset, vocab_ids (int32, increasing) their vocabulary ids;
+    tk_tok receives vocabulary ids."""
+    assert vocab_ids.dtype == torch.int32
+    rc = load().mfd_lmhead_topk_subset(_p(h), h.shape[0], h.shape[1], _p(W_packed), vocab_ids.numel(),
+                                       _p(vocab_ids), V_full, topk, _p(tk_logp), _p(tk_tok), _p(lse), _p(status),
+                                       _p(ws), ws.numel() * ws.element_size(), _s(stream))
+    _check(rc, "mfd_lmhead_topk_subset")
+
+
 def mfd_logits_topk(logits, topk, tk_logp, tk_tok, lse, status, ws, stream=None) -> None:
     R, V = logits.shape
     assert logits.dtype == torch.float32
@@ -197,7 +212,9 @@ class Round:
     """Device buffers for one drafting round of n_req requests, reused from
     call to call (allocation happens here, once, never inside the calls)."""
 
-    def __init__(self, n_req: int, K: int, L: int, topk: int, B: int, V: int, device="cuda"):
+    def __init__(self, n_req: int, K: int, L: int, topk: int, B: int, V: int, device="cuda", V_draft: int | None = None):
+        """V: the target vocabulary (verification); V_draft: the draft
+        vocabulary of a subset head (lmhead_topk_subset), if any."""
         self.n_req, self.K, self.L, self.topk, self.B, self.V = n_req, K, L, topk, B, V
         R = n_req * K * L
         N = B + 1
@@ -223,6 +240,7 @@ class Round:
         self.anchor = torch.zeros((n_req,), **i32)
         self.base_pos = torch.zeros((n_req,), **i32)
         ws = max(mfd_workspace_size(MFD_OP_LMHEAD_TOPK, n_req, K, L, topk, B, R, V),
+                 mfd_workspace_size(MFD_OP_LMHEAD_TOPK, n_req, K, L, topk, B, R, V_draft or V),
                  mfd_workspace_size(MFD_OP_LOGITS_TOPK, n_req, K, L, topk, B, R, V),
                  mfd_workspace_size(MFD_OP_BUILD_TREE, n_req, K, L, topk, B, R, V),
                  mfd_workspace_size(MFD_OP_VERIFY, n_req, K, L, topk, B, R, V))
@@ -234,6 +252,12 @@ class Round:
     def lmhead_topk_packed(self, h, W_packed, stream=None):
         mfd_lmhead_topk_packed(h, W_packed, self.V, self.topk, self.tk_logp, self.tk_tok, self.lse, self.status,
                                self.ws, stream)
+
+    def lmhead_topk_subset(self, h, W_packed, vocab_ids, stream=None):
+        """Draft over the subset whose packed rows are W_packed; tk_tok gets
+        vocabulary ids (< self.V)."""
+        mfd_lmhead_topk_subset(h, W_packed, vocab_ids, self.V, self.topk, self.tk_logp, self.tk_tok, self.lse,
+                               self.status, self.ws, stream)
 
     def logits_topk(self, logits, stream=None):
         mfd_logits_topk(logits, self.topk, self.tk_logp, self.tk_tok, self.lse, self.status, self.ws, stream)

@@ -64,13 +64,25 @@ def lm_head(V: int, H: int, seed: int, sigma: float | None = None, chunk_rows: i
     return W
 
 
-def futures(K: int, L: int, V: int, n_shared: int, rng: np.random.Generator) -> np.ndarray:
-    """Per-mode planted futures int32 [K, L] sharing n_shared positions."""
-    t = rng.integers(0, V, size=(K, L), dtype=np.int64)
+def futures(K: int, L: int, V: int, n_shared: int, rng: np.random.Generator,
+            vocab: np.ndarray | None = None) -> np.ndarray:
+    """Per-mode planted futures int32 [K, L] sharing n_shared positions;
+    tokens uniform on [0, V), or on the ids of `vocab` (a draft vocabulary)."""
+    hi = V if vocab is None else len(vocab)
+    t = rng.integers(0, hi, size=(K, L), dtype=np.int64)
     shared = rng.choice(L, size=n_shared, replace=False)
-    common = rng.integers(0, V, size=(n_shared,), dtype=np.int64)
+    common = rng.integers(0, hi, size=(n_shared,), dtype=np.int64)
     t[:, shared] = common[None, :]
+    if vocab is not None:
+        t = np.asarray(vocab, np.int64)[t]
     return t.astype(np.int32)
+
+
+def vocab_subset(V: int, n: int, seed: int) -> np.ndarray:
+    """A draft vocabulary: n distinct ids of [0, V), increasing -- the
+    stand-in for the target's most frequent tokens."""
+    rng = _rng(seed)
+    return np.sort(rng.choice(V, size=n, replace=False)).astype(np.int32)
 
 
 def hidden(W: torch.Tensor, fut: np.ndarray, rng: np.random.Generator, scale: float = 6.0) -> torch.Tensor:
@@ -154,9 +166,12 @@ class Round:
     seed: int  # Philox seed for sampled verification
 
 
-def round_inputs(W: torch.Tensor, K: int, L: int, n_shared: int, seed: int) -> Round:
+def round_inputs(W: torch.Tensor, K: int, L: int, n_shared: int, seed: int,
+                 vocab: np.ndarray | None = None) -> Round:
+    """W is the full-vocabulary head; with `vocab`, the futures are drawn from
+    that draft vocabulary."""
     rng = _rng(seed)
-    fut = futures(K, L, W.shape[0], n_shared, rng)
+    fut = futures(K, L, W.shape[0], n_shared, rng, vocab)
     h = hidden(W, fut, rng)
     m = int(rng.integers(0, K))
     s = int(rng.integers(0, 2**63 - 1))
