@@ -103,6 +103,31 @@ __device__ __forceinline__ void topk_insert(float (&tv)[T], int (&ti)[T], float 
   }
 }
 
+// Sort 32 (value, id) pairs best first (value desc, id asc) with a bitonic
+// network: 15 stages of 16 independent compare-exchanges, all in registers.
+__device__ __forceinline__ void sort32_best_first(float (&sv)[32], int (&si)[32]) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          // blocks with (i & k) == 0 put the better pair first, the others last
+          const bool sw = (i & k) == 0 ? vi_before(sv[l], si[l], sv[i], si[i]) : vi_before(sv[i], si[i], sv[l], si[l]);
+          const float a = sv[i], b = sv[l];
+          const int ia = si[i], ib = si[l];
+          sv[i] = sw ? b : a;
+          sv[l] = sw ? a : b;
+          si[i] = sw ? ib : ia;
+          si[l] = sw ? ia : ib;
+        }
+      }
+    }
+  }
+}
+
 // PACKED: the weight comes as pack_w_kernel lays it out, so a stage's
 // weight bytes are one contiguous 1-D bulk copy instead of KSUB 2-D boxes of
 // 256 rows x 128 bytes (rows 2H bytes apart), which stream markedly slower.
@@ -340,6 +365,26 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float mb = m * LOG2E;
 #pragma unroll
             for (int j = 0; j < 32; ++j) S += exp2f(fmaf(x[j], LOG2E, -mb));
+          }
+          if (t == t0 && c == 0) {
+            // the range's first chunk meets an empty list: its T best, by a
+            // sort of the chunk, are the list (columns past V, at -inf, stay
+            // (-inf, none) as the empty list's entries)
+            float sv[32];
+            int si[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {  // as the insert path: only columns above -inf enter
+              const bool in = x[j] > -INFINITY;
+              sv[j] = in ? x[j] : -INFINITY;
+              si[j] = in ? v0 + j : 0x7FFFFFFF;
+            }
+            sort32_best_first(sv, si);
+#pragma unroll
+            for (int s = 0; s < T; ++s) {
+              tv[s] = sv[s];
+              ti[s] = si[s];
+            }
+            continue;
           }
           // Top-T: one bit per column that beats this row's current T-th
           // entry (a later column never ties its way in: its id is larger).
