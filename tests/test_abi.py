@@ -95,3 +95,18 @@ def test_packed_weight_entry_points_arguments(lib):
     args[3] = fake
     args[5] = 40
     assert lib.mfd_lmhead_topk_packed(*args) == mfd.MFD_ERR_UNSUPPORTED  # topk > 32
+
+
+def test_subset_head_entry_point_arguments(lib):
+    """mfd_lmhead_topk_subset: argument errors returned before any CUDA call."""
+    fake = ctypes.c_void_p(0x100000)
+    def call(Wp=fake, V_sub=1000, ids=fake, V_full=5000, topk=8):
+        return lib.mfd_lmhead_topk_subset(fake, 4, 64, Wp, V_sub, ids, V_full, topk, fake, fake, None, fake, fake,
+                                          1 << 20, None)
+    assert call(Wp=None) == mfd.MFD_ERR_INVALID_ARG  # no packed weight
+    assert call(ids=None) == mfd.MFD_ERR_INVALID_ARG  # no id table
+    assert call(ids=ctypes.c_void_p(0x100002)) == mfd.MFD_ERR_INVALID_ARG  # id table not 4-byte aligned
+    assert call(V_full=999) == mfd.MFD_ERR_INVALID_ARG  # the full vocabulary is smaller than the subset
+    assert call(V_full=1 << 30) == mfd.MFD_ERR_INVALID_ARG
+    assert call(Wp=ctypes.c_void_p(0x100080)) == mfd.MFD_ERR_INVALID_ARG  # packed weight not 256-byte aligned
+    assert call(topk=40) == mfd.MFD_ERR_UNSUPPORTED
