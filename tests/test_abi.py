@@ -110,3 +110,21 @@ def test_subset_head_entry_point_arguments(lib):
     assert call(V_full=1 << 30) == mfd.MFD_ERR_INVALID_ARG
     assert call(Wp=ctypes.c_void_p(0x100080)) == mfd.MFD_ERR_INVALID_ARG  # packed weight not 256-byte aligned
     assert call(topk=40) == mfd.MFD_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++17")])
+def test_header_compiles_standalone(lang, std, tmp_path):
+    """include/mfd.h is plain C: it compiles on its own as C99 and as C++17,
+    with no CUDA or torch headers."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("use.c" if lang == "c" else "use.cpp")
+    src.write_text('#include "mfd.h"\nint main(void) { return (int)mfd_workspace_size(MFD_OP_BUILD_TREE, 1, 8, 15, 16,'
+                   ' 256, 120, 151936) == 0; }\n')
+    r = subprocess.run([cc, "-x", lang, f"-std={std}", "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(HERE, "..", "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
