@@ -2,14 +2,17 @@
 
 Workload (default): K=8 modes, L=15 drafted positions, H=2560, V=151936,
 top-k 16, tree budget B=256, sampled verification at T=1, batch 1 -- one
-round = mfd_lmhead_topk + mfd_build_tree + mfd_verify on fresh seeded inputs
-(W fixed).  Inputs are synthetic (tree_verified_speculative_gb300.synth).
+round = mfd_lmhead_topk_packed (the weight packed once, as at model load) +
+mfd_build_tree + mfd_verify on fresh seeded inputs (W fixed).  Other
+workloads: configs 2 and 4, 32 batched requests, and a draft-vocabulary
+subset head.  Inputs are synthetic (tree_verified_speculative_gb300.synth).
 
-Timing: CUDA events on the launching stream around the three calls of every
-round; the target logits' plant (+10 on the chosen mode's future, input
-generation that needs the round's tree) is applied between the tree and the
-verification call and is not timed.  W (778 MB) is larger than L2, so every
-round streams it from HBM.
+Timing: CUDA events on the launching stream, one interval around the LM head
+and the tree (back to back, as in a round) and one around the verification;
+the target logits' plant (+10 on the chosen mode's future, input generation
+that needs the round's tree) sits between them and is not timed.  W (778 MB)
+is larger than L2, so every round streams it from HBM.  The end-to-end
+figure drives the same calls from pinned host buffers.
 
 ``--impl reference`` times the CPU oracle (the only reference on this
 workload) on a bounded sample per step and prints the same JSON line.
