@@ -48,6 +48,10 @@ WORKLOADS = {
     # 0-15 greedy and 16-31 sampled at T = 1
     "r32_k8_l15_h2560_v151936_b128_mixed": dict(K=8, L=15, H=2560, V=151936, n_shared=None, topk=16, B=128,
                                                 T=None, n_req=32, temps=[0.0] * 16 + [1.0] * 16),
+    # K = 1 (one mode, the product-ranked tree) over a batch of requests:
+    # the single-mode path with batch-size sweeps (--n-req)
+    "k1_l15_h2560_v151936_b64_greedy_batch": dict(K=1, L=15, H=2560, V=151936, n_shared=None, topk=16, B=64,
+                                                  T=None, n_req=8, temps=[0.0]),
     # its small counterpart for host-side runs
     "r4_tiny_mixed": dict(K=2, L=4, H=64, V=512, n_shared=None, topk=8, B=16, T=None, n_req=4,
                           temps=[0.0, 0.0, 1.0, 1.0]),
@@ -69,9 +73,23 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n-req", type=int, default=0,
+                    help="requests per round for a batched workload (0: the workload's own); temperatures cycle")
     ap.add_argument("--profile-rounds", type=int, default=0,
                     help="run this many untimed rounds (LM head, tree, verify) and exit: the ncu capture target")
     return ap.parse_args()
+
+
+def workload(args):
+    """The workload's settings, with --n-req applied to a batched one (the
+    per-request temperatures cycle through the workload's list)."""
+    cfg = dict(WORKLOADS[args.workload])
+    n = getattr(args, "n_req", 0) or 0
+    if n > 0 and cfg.get("n_req", 1) > 1:
+        temps = cfg["temps"]
+        cfg["n_req"] = n
+        cfg["temps"] = [temps[i % len(temps)] for i in range(n)]
+    return cfg
 
 
 def peaks(kind="hbm"):
@@ -237,7 +255,7 @@ def run_gpu(args, ws, rank, local):
 
     from tree_verified_speculative_gb300 import mfd, synth
 
-    cfg = WORKLOADS[args.workload]
+    cfg = workload(args)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     K, L, H, V, topk, B, T = cfg["K"], cfg["L"], cfg["H"], cfg["V"], cfg["topk"], cfg["B"], cfg["T"]
@@ -434,7 +452,7 @@ def run_gpu_batched(args, ws, rank, local):
 
     from tree_verified_speculative_gb300 import mfd, synth
 
-    cfg = WORKLOADS[args.workload]
+    cfg = workload(args)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     K, L, H, V, topk, B, n_req = cfg["K"], cfg["L"], cfg["H"], cfg["V"], cfg["topk"], cfg["B"], cfg["n_req"]
@@ -540,16 +558,28 @@ def run_gpu_batched(args, ws, rank, local):
     value = whole_job_rate(steps, ws, total_ms)
     lm_us = sum(lm_d) / len(diag) * 1e3
     flops = 2.0 * R * V * H
-    achieved = flops / (lm_us * 1e-6) / 1e12
-    peak, peak_kind = peaks("bf16")
+    if R <= 128:  # one M tile: the weight stream bounds the LM head
+        algo = V * H * 2 + R * H * 2
+        peak, peak_kind = peaks("hbm")
+        roof = {"bound": "hbm", "achieved": round(algo / (lm_us * 1e-6) / 1e9, 1), "unit": "GB/s",
+                "algorithmic_bytes_per_launch": algo}
+    else:
+        peak, peak_kind = peaks("bf16")
+        roof = {"bound": "tensor", "achieved": round(flops / (lm_us * 1e-6) / 1e12, 1), "unit": "TFLOP/s",
+                "algorithmic_flops_per_launch": flops}
+    roof.update({"kernel": "mfd_lmhead_topk_packed (lmhead_topk_kernel + merge_topk_kernel)", "peak": peak,
+                 "frac": round(roof["achieved"] / peak, 4), "peak_kind": peak_kind, "traffic": None})
     acc = acc_buf[args.warmup:].float().cpu().numpy()
     greedy = np.array(cfg["temps"]) == 0.0
+    accept = {name: round(float(acc[:, sel].mean()), 4)
+              for name, sel in (("greedy", greedy), ("sampled", ~greedy)) if sel.any()}
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "rounds/s", "n_gpus": ws, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "K": K, "L": L, "H": H, "V": V, "topk": topk, "B": B,
-                   "n_req": n_req, "rows": R, "temperatures": "requests 0-15 greedy, 16-31 T=1",
+                   "n_req": n_req, "rows": R,
+                   "temperatures": f"{int(greedy.sum())} greedy, {int((~greedy).sum())} sampled (T={sorted(set(cfg['temps']))})",
                    "parallelism": f"replicas{ws}" if ws > 1 else "single",
                    "lm_head_weight": "packed once before timing (mfd_lmhead_pack), streamed by mfd_lmhead_topk_packed",
                    "l2": "inputs larger than L2 (W = %.0f MB; %d distinct hidden-state batches of %.1f MB cycled)"
@@ -561,12 +591,8 @@ def run_gpu_batched(args, ws, rank, local):
                       "split_from_diagnostic_rounds": {"lmhead_topk": round(lm_us, 2),
                                                        "build_tree": round(sum(bd_d) / len(diag) * 1e3, 2),
                                                        "rounds": len(diag)}},
-        "mean_accept_len": {"greedy": round(float(acc[:, greedy].mean()), 4),
-                            "sampled": round(float(acc[:, ~greedy].mean()), 4)},
-        "roofline": {"kernel": "mfd_lmhead_topk_packed (lmhead_topk_kernel + merge_topk_kernel)", "bound": "tensor",
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "algorithmic_flops_per_launch": flops, "traffic": None},
+        "mean_accept_len": accept,
+        "roofline": roof,
         "gpu_launches": 4 * steps,
         "clocks": ck,
         "e2e": None,
@@ -667,7 +693,7 @@ def run_reference(args, ws, rank):
     import oracle
     from tree_verified_speculative_gb300 import synth
 
-    cfg = WORKLOADS[args.workload]
+    cfg = workload(args)
     K, L, H, V, topk, B = cfg["K"], cfg["L"], cfg["H"], cfg["V"], cfg["topk"], cfg["B"]
     n_req = cfg.get("n_req", 1)
     temps = cfg.get("temps") or [cfg["T"]]
@@ -740,7 +766,7 @@ def profile_rounds(args, local):
 
     from tree_verified_speculative_gb300 import mfd
 
-    cfg = WORKLOADS[args.workload]
+    cfg = workload(args)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     n_req = cfg.get("n_req", 1)
@@ -785,7 +811,7 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args, ws, rank)))
         return
-    if WORKLOADS[args.workload].get("n_req", 1) > 1:
+    if workload(args).get("n_req", 1) > 1:
         out = run_gpu_batched(args, ws, rank, local)
     else:
         out = run_gpu(args, ws, rank, local)

@@ -78,16 +78,19 @@ def test_two_gloo_ranks():
 
 
 @pytest.mark.timeout(300)
-def test_reference_arm_batched_workload():
+@pytest.mark.parametrize("n_req", [0, 6])
+def test_reference_arm_batched_workload(n_req):
     """The reference arm on a batched workload (4 requests, per-request
-    temperatures): one line, the per-request work scaled by the batch."""
+    temperatures; --n-req overrides the batch): one line, the per-request work
+    scaled by the batch."""
     import subprocess
 
-    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
-                          "--warmup", "0", "--workload", "r4_tiny_mixed"], capture_output=True, text=True,
-                         timeout=280, cwd=ROOT)
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2", "--warmup", "0",
+           "--workload", "r4_tiny_mixed"] + (["--n-req", str(n_req)] if n_req else [])
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=280, cwd=ROOT)
     assert out.returncode == 0, out.stderr[-2000:]
     line = json.loads(out.stdout.strip().splitlines()[-1])
-    assert line["impl"] == "reference" and line["config"]["n_req"] == 4 and line["value"] > 0
-    assert "scaled x4" in line["cpu_baseline"]["sample"]
+    want = n_req or 4
+    assert line["impl"] == "reference" and line["config"]["n_req"] == want and line["value"] > 0
+    assert f"scaled x{want}" in line["cpu_baseline"]["sample"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0
