@@ -400,7 +400,7 @@ def run_gpu(args, ws, rank, local):
                    "temperature": T, "n_req": 1, "parallelism": f"replicas{ws}" if ws > 1 else "single",
                    **({"V_draft": head.V} if head.ids is not None else {}),
                    "lm_head_weight": f"packed once before timing (mfd_lmhead_pack), streamed by {head.name}",
-                   "l2": "inputs larger than L2 (W = %.0f MB streamed every round)" % (V * H * 2 / 1e6),
+                   "l2": "inputs larger than L2 (W = %.0f MB streamed every round)" % (head.V * H * 2 / 1e6),
                    "timing": "sum over the timed rounds of two CUDA-event intervals per round, one around the LM head and the tree (back to back, as in a real round) and one around the verification, with the queue kept ahead of the GPU; the target plant (input generation that needs the round's tree) is untimed; the per-stage split comes from separate diagnostic rounds"},
         "stages_us": {"lmhead_topk_plus_build_tree": round(ab / steps * 1e3, 2), "verify": round(vf / steps * 1e3, 2),
                       "split_from_diagnostic_rounds": {"lmhead_topk": round(sum(lm_d) / len(diag) * 1e3, 2),
