@@ -166,7 +166,9 @@ int mfd_logits_topk(const float *logits, int R, int V, int topk, float *tk_logp,
  * mfd_workspace_size(MFD_OP_LOGITS_TOPK, ...) for the same R, V and topk;
  * larger problems are rejected with MFD_ERR_WORKSPACE (use mfd_logits_topk).
  * The first call on a device looks up that array's device address (once per
- * device); make that first call before any stream capture.  All calls share
+ * device); make that first call before any stream capture.  The address is
+ * kept for the life of the process: after cudaDeviceReset it is stale, so a
+ * caller that resets a device must not call this entry point on it again.  All calls share
  * the one array and it keeps the last call's contents: calls that may
  * overlap on the GPU (different streams, or different host threads) race on
  * it, so serialise them.  Arguments and results are those of
@@ -242,6 +244,36 @@ int mfd_verify(const float *target_logits, int n_req, int B, int V, int L,
                const float *temperature, const uint64_t *seed, int32_t *accept_len,
                int32_t *path_nodes, int32_t *out_tokens, int32_t *status, void *ws,
                size_t ws_bytes, mfd_stream_t stream);
+
+/* MFD-D, the single-mode default path (project page "Multi-Future Drafting",
+ * In a serving engine, the MFD-D paragraph and Figure 5): the same drafter
+ * drafts all K modes while few requests are in flight and switches to its
+ * single-mode default path from three requests on, where the draft cost of
+ * K modes grows with the batch while the acceptance length does not.  The
+ * returned count is the K to pass to the round's calls (the single-mode
+ * round is the same three calls with K = 1: its tree is the product-ranked
+ * one).  Host only; no device work.
+ *   returns K for 1 <= n_req < MFD_MFDD_SWITCH_REQUESTS, 1 for n_req at or
+ *   above it, and 0 for n_req < 1 or K outside [1, 16]. */
+#define MFD_MFDD_SWITCH_REQUESTS 3
+int mfd_mfdd_modes(int n_req, int K);
+
+/* Fault injection for the walk's bounded waits, for tests (the pages have no
+ * counterpart: it exists so that the timeout path can be exercised without
+ * faulting or hanging a GPU).  Arguments and outputs as mfd_verify, plus
+ * wait_limit_ns in [1e3, 1e8]: every bounded wait of this call gives up after
+ * that long.  In every request group of more than one CTA (V >= 2048), the
+ * CTAs other than the group's first never publish their step result, so the
+ * first CTA's gather runs out, nobody publishes a winner, and the others' waits
+ * run out too: every CTA returns and *status = MFD_ERR_TIMEOUT.  The
+ * workspace's generation still advances, so the next mfd_verify on the same
+ * workspace is correct.  Errors: those of mfd_verify; INVALID_ARG for a limit
+ * outside the range. */
+int mfd_verify_withheld_test(const float *target_logits, int n_req, int B, int V, int L,
+                             const int32_t *parent, const int32_t *token, const int32_t *n_nodes,
+                             const float *temperature, const uint64_t *seed, int32_t *accept_len,
+                             int32_t *path_nodes, int32_t *out_tokens, int32_t *status, void *ws,
+                             size_t ws_bytes, uint64_t wait_limit_ns, mfd_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -128,3 +128,12 @@ def test_header_compiles_standalone(lang, std, tmp_path):
     r = subprocess.run([cc, "-x", lang, f"-std={std}", "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
                         "-I", os.path.join(HERE, "..", "include"), str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_mfdd_switch_rule(lib):
+    """MFD-D (project page "Multi-Future Drafting", In a serving engine): all
+    K modes below three requests in flight, the single-mode path from three
+    on; invalid arguments give 0."""
+    assert [mfd.mfd_mfdd_modes(n, 8) for n in (1, 2, 3, 4, 32)] == [8, 8, 1, 1, 1]
+    assert mfd.mfd_mfdd_modes(2, 1) == 1
+    assert mfd.mfd_mfdd_modes(0, 8) == 0 and mfd.mfd_mfdd_modes(1, 0) == 0 and mfd.mfd_mfdd_modes(1, 17) == 0

@@ -113,17 +113,6 @@ def test_lmhead_batched_3840_rows_sampled(head_2560):
     check_topk(g[0][rows], g[1][rows], o[0], o[1])
 
 
-@pytest.mark.slow
-def test_lmhead_wide_shape_sampled_rows():
-    """H=5120, V=248320, top-k 32 (about 2.5 GB of weights)."""
-    W = synth.lm_head(248320, 5120, seed=4048)
-    r = synth.round_inputs(W, 8, 15, 13, seed=9)
-    g = _gpu_lmhead(r.h, W, 32)
-    rows = np.array([0, 17, 59, 119])
-    o = oracle.lmhead_topk(_bits(r.h[rows]), _bits(W), 32)
-    check_topk(g[0][rows], g[1][rows], o[0], o[1])
-
-
 def test_lmhead_rejects_bad_arguments():
     h = torch.zeros((4, 100), dtype=torch.bfloat16, device="cuda")  # H not a multiple of 64
     W = torch.zeros((64, 100), dtype=torch.bfloat16, device="cuda")
@@ -164,10 +153,9 @@ def test_pack_layout():
 @pytest.mark.parametrize("R,H,V,topk", [(120, 2560, 151936, 16), (37, 128, 1000, 8), (200, 256, 4099, 32),
                                         (1, 64, 16, 1), (300, 128, 5000, 16), (3840, 2560, 151936, 16)])
 def test_packed_weight_bit_identical(R, H, V, topk):
-    """mfd_lmhead_topk_packed gives exactly mfd_lmhead_topk's results.  Above
-    128 rows the packed path runs in CTA pairs that multicast the weight
-    halves (300 rows: three M tiles, the last pair has an empty one; 3840:
-    32 requests of 120 rows)."""
+    """mfd_lmhead_topk_packed gives exactly mfd_lmhead_topk's results, at one
+    M tile and at several (300 rows: three M tiles, the last one ragged;
+    3840: 32 requests of 120 rows)."""
     rng = np.random.default_rng(R + H + V)
     if V == 151936:
         W = synth.lm_head(V, H, seed=2024)
@@ -196,7 +184,7 @@ def test_subset_head(R):
     a serving engine): the LM head, log-softmax and top-k over the subset's
     rows, with tokens written as vocabulary ids.  Exactly the packed head on
     the subset rows with the ids looked up, and the oracle's top-k on sampled
-    rows.  300 rows run in CTA pairs."""
+    rows.  300 rows span three M tiles."""
     rng = np.random.default_rng(R + 7)
     V_full, H, n_sub, topk = 20000, 256, 4096, 16
     ids = synth.vocab_subset(V_full, n_sub, seed=R)
@@ -234,3 +222,72 @@ def test_subset_head_rejects_ids_out_of_range():
     torch.cuda.synchronize()
     assert status_of(a) == mfd.MFD_ERR_INPUT
     assert np.all(np_(a.tk_tok) == -1)
+
+
+def _ranges(V: int) -> list[tuple[int, int]]:
+    """The LM head's vocabulary ranges at one M tile, as 256-row tile spans
+    [t0, t1): min(tiles, SMs) contiguous ranges (the split the library's
+    host code plans for R <= 128 rows)."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    n_vt = -(-V // 256)
+    P = min(n_vt, n_sm, 256)
+    return [(r * n_vt // P, (r + 1) * n_vt // P) for r in range(P)]
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_lmhead_ties_duplicate_rows(packed):
+    """Equal logits must come out in increasing token-id order, and a tie
+    across the cut must keep the smallest ids (model card "MFD drafter for
+    Qwen3.5-4B", first paragraph: the B best prefixes, ties to the smaller
+    ids; project page, How it works, step 3).  Groups of identical weight
+    rows give exactly equal logits on both sides: (i) inside one range's
+    first 32 columns (the sorted first chunk), (ii) in different 256-row
+    tiles of one range, (iii) in different vocabulary ranges, and (iv) six
+    copies across ranges with top-4, so the cut falls inside the tie.  Each
+    hidden row points at one group, whose members are then its best
+    logits."""
+    V, H, topk = 51200, 128, 4
+    rng = np.random.default_rng(31)
+    ranges = _ranges(V)
+    two = [rg for rg in ranges if rg[1] - rg[0] >= 2]
+    assert two, "expected a range with two tiles"
+    t2 = two[len(two) // 2]
+    groups = [
+        [ranges[5][0] * 256 + 3, ranges[5][0] * 256 + 17, ranges[5][0] * 256 + 30],
+        [t2[0] * 256 + 100, (t2[0] + 1) * 256 + 7],
+        [ranges[0][0] * 256 + 200, ranges[40][0] * 256 + 5, ranges[100][0] * 256 + 250, ranges[-1][0] * 256 + 1],
+        [ranges[i][0] * 256 + 11 * i % 256 for i in (2, 30, 31, 77, 120, 151 % len(ranges))],
+    ]
+    members = [v for g in groups for v in g]
+    assert len(set(members)) == len(members) and max(members) < V
+    Wf = (rng.standard_normal((V, H)) / np.sqrt(H)).astype(np.float32)
+    for g in groups:
+        for v in g[1:]:
+            Wf[v] = Wf[g[0]]
+    W = synth.bf16_round(Wf)
+    Wr = W.float().numpy()
+    hrows = []
+    for g in groups:
+        for rep in range(2):  # two hidden rows per group
+            u = Wr[g[0]] / np.linalg.norm(Wr[g[0]])
+            hrows.append(8.0 * u + 0.3 * rng.standard_normal(H))
+    h = synth.bf16_round(np.asarray(hrows, np.float32))
+    R = h.shape[0]
+    rd = mfd.Round(1, 1, R, topk, 1, V)
+    rd.status.zero_()
+    if packed:
+        rd.lmhead_topk_packed(h.cuda(), mfd.pack_lm_head(W.cuda()))
+    else:
+        rd.lmhead_topk(h.cuda(), W.cuda())
+    torch.cuda.synchronize()
+    assert status_of(rd) == 0
+    g_lp, g_tok = np_(rd.tk_logp), np_(rd.tk_tok)
+    o_lp, o_tok, _ = oracle.lmhead_topk(_bits(h), _bits(W), topk)
+    check_topk(g_lp, g_tok, o_lp, o_tok)
+    for gi, g in enumerate(groups):
+        want = sorted(g)[:topk]
+        for r in (2 * gi, 2 * gi + 1):
+            # the group members are the row's best logits, tied exactly
+            assert list(o_tok[r, :len(want)]) == want, (gi, r, o_tok[r])
+            assert list(g_tok[r, :len(want)]) == want, (gi, r, g_tok[r])
+            assert len(set(g_lp[r, :len(want)].view(np.uint32).tolist())) == 1

@@ -258,3 +258,39 @@ def test_sampled_coverage_identity():
     se = acc.std() / np.sqrt(n_req)
     assert 0.3 < expect < 2.5
     assert abs(acc.mean() - expect) < 4 * se, (acc.mean(), expect, se)
+
+
+def test_bounded_wait_runs_out_and_workspace_recovers():
+    """The walk's exchange waits are bounded: with the other CTAs' step
+    results withheld (the library's fault-injection entry point) and a 200 us
+    limit, every CTA gives up, the call ends with MFD_ERR_TIMEOUT instead of
+    hanging, and the next ordinary call on the same workspace is exact."""
+    rng = np.random.default_rng(23)
+    V, L, B = 20000, 6, 15
+    tree, futs = _trees(rng, 2, 2, L, 4, V, B)
+    t = _targets(rng, tree, futs, V, [0, 1])
+    rd = mfd.Round(2, 1, L, 1, B, V)
+    rd.parent.copy_(torch.from_numpy(tree["parent"]))
+    rd.token.copy_(torch.from_numpy(tree["token"]))
+    rd.n_nodes.copy_(torch.from_numpy(tree["n_nodes"]))
+    td = torch.from_numpy(t).cuda()
+    temp = torch.zeros(2, device="cuda")
+    seed = torch.zeros(2, dtype=torch.int64, device="cuda")
+    for attempt in range(2):
+        rd.status.zero_()
+        mfd.mfd_verify_withheld_test(td, 2, B, V, L, rd.parent, rd.token, rd.n_nodes, temp, seed, rd.accept_len,
+                                     rd.path_nodes, rd.out_tokens, rd.status, rd.ws, 200_000)
+        torch.cuda.synchronize()
+        assert status_of(rd) == mfd.MFD_ERR_TIMEOUT
+        rd.status.zero_()
+        rd.verify(td, temp, seed)
+        torch.cuda.synchronize()
+        assert status_of(rd) == 0
+        for q in range(2):
+            o = oracle.verify(t[q], tree["parent"][q], tree["token"][q], int(tree["n_nodes"][q]), L)
+            assert check_walk(int(np_(rd.accept_len)[q]), np_(rd.path_nodes)[q], np_(rd.out_tokens)[q], *o,
+                              sampled=False)
+    with pytest.raises(mfd.MfdError) as e:
+        mfd.mfd_verify_withheld_test(td, 2, B, V, L, rd.parent, rd.token, rd.n_nodes, temp, seed, rd.accept_len,
+                                     rd.path_nodes, rd.out_tokens, rd.status, rd.ws, 10)
+    assert e.value.code == mfd.MFD_ERR_INVALID_ARG

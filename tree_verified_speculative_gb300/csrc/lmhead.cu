@@ -23,12 +23,11 @@
 // writes, per row and range, (max, sum exp) and its T best (logit, id)
 // pairs; merge_topk (topk.cu) combines the P partials of a row.
 //
-// Many M tiles (R > 128, packed weight, when the host's plan says so): CTAs
-// run in clusters of two with M tiles 2m and 2m + 1 of the same vocabulary
-// range.  Each loads half of every weight block and multicasts it to both,
-// so a weight tile crosses L2 once per pair (the L2 bytes per MMA step fall
-// from 48 KB to 32 KB); a stage is free again when both CTAs' MMAs have read
-// it (two arrivals).
+// Many M tiles (R > 128): the work items of one vocabulary range are its M
+// tiles; the host orders items range-major, so the CTAs of a range stream the
+// same weight tiles at about the same time and each weight tile comes from
+// HBM about once and from L2 for the other M tiles.  Every CTA loads only
+// into its own shared memory.
 //
 // Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer (one
 // thread each), warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4)..).
@@ -63,22 +62,20 @@ constexpr int smem_bytes() {
 struct Params {
   int R, H, V;
   int n_mt;     // M tiles of 128 rows
-  int n_mg;     // M groups per range: n_mt, or M-tile pairs in the cluster form
   int n_vt;     // vocabulary tiles of 256 rows
   int P;        // vocabulary ranges
-  int n_items;  // n_mg * P
+  int n_items;  // n_mt * P
   float2 *part_ms;  // [R][P]      (running max, sum exp(z - max))
   int2 *part_cand;  // [R][P][T]   (logit bits, token id), best first
   int32_t *status;
   const uint8_t *w_packed;  // packed weight (see pack_w_kernel), or null
 };
 
-// rank: the CTA's rank in its cluster of two (0 without clusters)
-__device__ __forceinline__ void item_range(const Params &p, int item, int rank, bool mc, int &mt, int &t0, int &t1,
-                                           int &range) {
-  range = item / p.n_mg;
-  const int mg = item - range * p.n_mg;
-  mt = mc ? 2 * mg + rank : mg;
+// Work item -> (M tile, vocabulary tiles [t0, t1), range); items are
+// range-major.
+__device__ __forceinline__ void item_range(const Params &p, int item, int &mt, int &t0, int &t1, int &range) {
+  range = item / p.n_mt;
+  mt = item - range * p.n_mt;
   t0 = (int)(((long long)range * p.n_vt) / p.P);
   t1 = (int)(((long long)(range + 1) * p.n_vt) / p.P);
 }
@@ -131,7 +128,7 @@ __device__ __forceinline__ void sort32_best_first(float (&sv)[32], int (&si)[32]
 // PACKED: the weight comes as pack_w_kernel lays it out, so a stage's
 // weight bytes are one contiguous 1-D bulk copy instead of KSUB 2-D boxes of
 // 256 rows x 128 bytes (rows 2H bytes apart), which stream markedly slower.
-template <int T, bool PACKED, bool MC>
+template <int T, bool PACKED>
 __global__ void __launch_bounds__(THREADS, 1)
     lmhead_topk_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                        const Params p) {
@@ -152,15 +149,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  static_assert(!MC || (PACKED && KSUB == 1), "the cluster form streams the packed weight, one K atom a stage");
-  const int rank = MC ? (int)cluster_ctarank() : 0;
-  const int cta0 = MC ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // work-item stride unit
-  const int ncta = MC ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int cta0 = (int)blockIdx.x;
+  const int ncta = (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], MC ? 2 : 1);  // the MMAs of both CTAs of the pair read a stage
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -179,9 +174,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // the peer multicasts into this CTA's stages and arrives on its barriers
-  // only after they are initialised
-  if (MC) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int nk = p.H / BK;
@@ -202,7 +194,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int item = cta0; item < p.n_items && ok; item += ncta) {
         int mt, t0, t1, range;
-        item_range(p, item, rank, MC, mt, t0, t1, range);
+        item_range(p, item, mt, t0, t1, range);
         for (int t = t0; t < t1 && ok; ++t) {
           if (p.n_mt > 1) {
             // Every M tile of a range reads the same weight tiles at about
@@ -215,7 +207,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               tn = -1;
               if (item + ncta < p.n_items) {
                 int mt2, t2, t3, r2;
-                item_range(p, item + ncta, rank, MC, mt2, t2, t3, r2);
+                item_range(p, item + ncta, mt2, t2, t3, r2);
                 tn = t2 < t3 ? t2 : -1;
               }
             }
@@ -234,11 +226,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               break;
             }
             mbar_arrive_expect_tx(&full[stage], (uint32_t)(nsub * (A_SUB + B_SUB)));
-            if (MC)  // this CTA's half of the block, to both CTAs of the pair
-              bulk_load_1d_mc(sB + stage * B_BYTES + rank * (B_SUB / 2),
-                              p.w_packed + ((size_t)t * nk + kc) * B_SUB + rank * (B_SUB / 2), (uint32_t)(B_SUB / 2),
-                              &full[stage], (uint16_t)0x3, pol_w);
-            else if (PACKED)
+            if (PACKED)
               bulk_load_1d(sB + stage * B_BYTES, p.w_packed + ((size_t)t * nk + kc) * B_SUB, (uint32_t)(nsub * B_SUB),
                            &full[stage], pol_w);
             else
@@ -273,7 +261,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int item = cta0; item < p.n_items && ok; item += ncta) {
         int mt, t0, t1, range;
-        item_range(p, item, rank, MC, mt, t0, t1, range);
+        item_range(p, item, mt, t0, t1, range);
         for (int t = t0; t < t1 && ok; ++t) {
           if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
             ok = false;
@@ -295,10 +283,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               for (int kk = 0; kk < BK / 16; ++kk)
                 tc_mma_f16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kc | sub | kk) != 0);
             }
-            if (MC)
-              tc_commit_mc(&empty[stage], (uint16_t)0x3);
-            else
-              tc_commit(&empty[stage]);
+            tc_commit(&empty[stage]);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -329,7 +314,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int item = cta0; item < p.n_items && ok; item += ncta) {
       int mt, t0, t1, range;
-      item_range(p, item, rank, MC, mt, t0, t1, range);
+      item_range(p, item, mt, t0, t1, range);
       float m = -INFINITY, S = 0.f;
       float tv[T];
       int ti[T];
@@ -431,9 +416,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   __syncthreads();
-  // neither CTA of a pair leaves while the other's MMAs may still arrive on
-  // its barriers
-  if (MC) cluster_sync();
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
@@ -461,7 +443,7 @@ __global__ void pack_w_kernel(const uint4 *__restrict__ W, int V, int H, uint4 *
   }
 }
 
-template <int T, bool PACKED, bool MC>
+template <int T, bool PACKED>
 cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
   static_assert(smem_bytes() <= 232448, "shared memory budget");
   Params p;
@@ -469,34 +451,28 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
   p.H = L.H;
   p.V = L.V;
   p.n_mt = (L.R + BM - 1) / BM;
-  p.n_mg = MC ? (p.n_mt + 1) / 2 : p.n_mt;
   p.n_vt = (L.V + BN - 1) / BN;
   p.P = L.P;
-  p.n_items = p.n_mg * p.P;
+  p.n_items = p.n_mt * p.P;
   p.part_ms = reinterpret_cast<float2 *>(L.part_ms);
   p.part_cand = reinterpret_cast<int2 *>(L.part_cand);
   p.status = L.status;
   p.w_packed = static_cast<const uint8_t *>(L.w_packed);
-  cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<T, PACKED, MC>,
+  cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<T, PACKED>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
   if (e != cudaSuccess) return e;
-  const int units = MC ? L.n_sm / 2 : L.n_sm;  // CTAs, or CTA pairs
-  const int grid = (p.n_items < units ? p.n_items : units) * (MC ? 2 : 1);
+  const int grid = p.n_items < L.n_sm ? p.n_items : L.n_sm;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem_bytes();
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = MC ? 2 : 1;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = MC ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, lmhead_topk_kernel<T, PACKED, MC>, *L.tmap_h, PACKED ? *L.tmap_h : *L.tmap_w, p);
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, lmhead_topk_kernel<T, PACKED>, *L.tmap_h, PACKED ? *L.tmap_h : *L.tmap_w, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -508,14 +484,11 @@ int lmhead_m_rows() { return BM; }
 int lmhead_k_chunk() { return BK; }
 
 cudaError_t launch_lmhead_partials(const LmheadLaunch &L, cudaStream_t stream) {
-  const bool pk = L.w_packed != nullptr, mc = pk && L.pairs && L.R > BM && L.n_sm >= 2;
+  const bool pk = L.w_packed != nullptr;
   switch (L.T) {
-    case 8: return mc ? launch_t<8, true, true>(L, stream) : pk ? launch_t<8, true, false>(L, stream)
-                                                                : launch_t<8, false, false>(L, stream);
-    case 16: return mc ? launch_t<16, true, true>(L, stream) : pk ? launch_t<16, true, false>(L, stream)
-                                                                  : launch_t<16, false, false>(L, stream);
-    case 32: return mc ? launch_t<32, true, true>(L, stream) : pk ? launch_t<32, true, false>(L, stream)
-                                                                  : launch_t<32, false, false>(L, stream);
+    case 8: return pk ? launch_t<8, true>(L, stream) : launch_t<8, false>(L, stream);
+    case 16: return pk ? launch_t<16, true>(L, stream) : launch_t<16, false>(L, stream);
+    case 32: return pk ? launch_t<32, true>(L, stream) : launch_t<32, false>(L, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -12,7 +12,6 @@ struct LmheadLaunch {
   int R, H, V;
   int T;     // candidates kept per (row, range): 8, 16 or 32
   int P;     // vocabulary ranges (<= number of 256-row tiles)
-  bool pairs;  // packed weight, R > 128: clusters of two CTAs multicast each weight block
   int n_sm;  // persistent grid size
   void *part_ms;    // float2 [R][P]
   void *part_cand;  // int2 [R][P][T]
@@ -76,6 +75,8 @@ struct VerifyLaunch {
   int32_t *accept_len, *path_nodes, *out_tokens, *status;
   unsigned long long *ws;  // [grid][8] exchange words (generation-tagged, no zeroing needed)
   int grid;                   // largest cooperative grid
+  unsigned long long wait_ns = 0;  // bounded-wait limit (0: the library's default)
+  int withhold = 0;                // fault injection for tests of the bounded waits
 };
 int verify_max_grid(int n_sm);
 cudaError_t launch_verify(const VerifyLaunch &V, cudaStream_t stream);

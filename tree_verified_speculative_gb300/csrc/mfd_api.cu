@@ -69,8 +69,9 @@ using MapKey = std::tuple<int, const void *, int, int, int>;  // device, ptr, ro
 std::map<MapKey, CUtensorMap> g_maps;
 
 // bf16 [rows][cols] row-major, box = 64 columns x box_rows rows, 128B swizzle,
-// out-of-range rows read as zero.
-int tensor_map(const void *ptr, int rows, int cols, int box_rows, const CUtensorMap **out) {
+// out-of-range rows read as zero.  The descriptor is copied into *out while
+// the lock is held: another thread may clear the cache right after.
+int tensor_map(const void *ptr, int rows, int cols, int box_rows, CUtensorMap *out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MFD_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -92,19 +93,18 @@ int tensor_map(const void *ptr, int rows, int cols, int box_rows, const CUtensor
     if (g_maps.size() > 4096) g_maps.clear();
     it = g_maps.emplace(key, m).first;
   }
-  *out = &it->second;  // std::map nodes are stable
+  *out = it->second;
   return MFD_OK;
 }
 
 // ---------------------------------------------------------------- layouts
 struct TopkLayout {
   int P, T, chunk;
-  bool pairs;  // LM head: CTA pairs sharing each weight tile (packed weight only)
   size_t ms_bytes, cand_bytes, total;
 };
 
-// Fewest weight tiles for the busiest worker when n_groups M groups share
-// `workers` workers: over P vocabulary ranges, a worker takes
+// Fewest weight tiles for the busiest CTA when n_groups M tiles share
+// `workers` CTAs: over P vocabulary ranges, a CTA takes
 // ceil(n_groups * P / workers) items of ceil(tiles / P) tiles.  Among equal
 // costs the fewest ranges win: fewer partials to merge and fewer top-T
 // restarts per row.
@@ -128,18 +128,7 @@ TopkLayout lmhead_layout(int R, int V, int topk, int n_sm) {
   const int n_mt = (R + mfd::lmhead_m_rows() - 1) / mfd::lmhead_m_rows();
   y.P = tiles < n_sm ? tiles : n_sm;
   if (y.P > 256) y.P = 256;
-  y.pairs = false;
-  if (n_mt > 1) {
-    // Work items are (range, M tile) for single CTAs, or (range, pair of M
-    // tiles) for CTA pairs; pairs read each weight tile once from L2 between
-    // them, so they win ties.  The row-major weight path takes the same
-    // ranges with single CTAs.
-    int P1 = 1, P2 = 1;
-    const long long c1 = best_ranges(tiles, n_mt, n_sm, &P1);
-    const long long c2 = n_sm >= 2 ? best_ranges(tiles, (n_mt + 1) / 2, n_sm / 2, &P2) : c1 + 1;
-    y.pairs = c2 <= c1;
-    y.P = y.pairs ? P2 : P1;
-  }
+  if (n_mt > 1) best_ranges(tiles, n_mt, n_sm, &y.P);  // work items are (range, M tile)
   y.T = cand_width(topk);
   y.chunk = 0;
   y.ms_bytes = align256((size_t)R * y.P * 8);
@@ -154,7 +143,6 @@ TopkLayout logits_layout(int R, int V, int topk) {
   chunk = (chunk + 31) / 32 * 32;
   if (chunk < 1024) chunk = 1024;
   y.chunk = chunk;
-  y.pairs = false;
   y.P = (V + chunk - 1) / chunk;
   y.T = cand_width(topk);
   y.ms_bytes = align256((size_t)R * y.P * 8);
@@ -213,6 +201,11 @@ const char *mfd_status_string(int status) {
   }
 }
 
+int mfd_mfdd_modes(int n_req, int K) {
+  if (n_req < 1 || K < 1 || K > 16) return 0;
+  return n_req < MFD_MFDD_SWITCH_REQUESTS ? K : 1;
+}
+
 size_t mfd_workspace_size(int op, int n_req, int K, int L, int topk, int B, int R, int V) {
   (void)K;
   (void)L;
@@ -259,20 +252,19 @@ int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int 
   if (!is_sm103(d)) return MFD_ERR_UNSUPPORTED;
   const TopkLayout y = lmhead_layout(R, V, topk, d.n_sm);
   if (!ws || ws_bytes < y.total || !aligned(ws, 256)) return MFD_ERR_WORKSPACE;
-  const CUtensorMap *mh = nullptr, *mw = nullptr;
+  CUtensorMap mh, mw;
   if ((rc = tensor_map(h, R, H, mfd::lmhead_m_rows(), &mh)) != MFD_OK) return rc;
   if (W && (rc = tensor_map(W, V, H, mfd::lmhead_tile_rows(), &mw)) != MFD_OK) return rc;
   char *base = static_cast<char *>(ws);
   mfd::LmheadLaunch L;
-  L.tmap_h = mh;
-  L.tmap_w = mw;
+  L.tmap_h = &mh;
+  L.tmap_w = W ? &mw : nullptr;
   L.w_packed = W ? nullptr : Wp;
   L.R = R;
   L.H = H;
   L.V = V;
   L.T = y.T;
   L.P = y.P;
-  L.pairs = y.pairs && !W;
   L.n_sm = d.n_sm;
   L.part_ms = base;
   L.part_cand = base + y.ms_bytes;
@@ -447,10 +439,13 @@ int mfd_build_tree(const float *tk_logp, const int32_t *tk_tok, int n_req, int K
   return cuda_status(mfd::launch_build_tree(T, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int mfd_verify(const float *target_logits, int n_req, int B, int V, int L, const int32_t *parent,
-               const int32_t *token, const int32_t *n_nodes, const float *temperature, const uint64_t *seed,
-               int32_t *accept_len, int32_t *path_nodes, int32_t *out_tokens, int32_t *status, void *ws,
-               size_t ws_bytes, mfd_stream_t stream) {
+}  // extern "C"
+
+namespace {
+int verify_call(const float *target_logits, int n_req, int B, int V, int L, const int32_t *parent,
+                const int32_t *token, const int32_t *n_nodes, const float *temperature, const uint64_t *seed,
+                int32_t *accept_len, int32_t *path_nodes, int32_t *out_tokens, int32_t *status, void *ws,
+                size_t ws_bytes, mfd_stream_t stream, unsigned long long wait_ns, int withhold) {
   if (!target_logits || !parent || !token || !n_nodes || !temperature || !seed || !accept_len || !path_nodes ||
       !out_tokens || !status)
     return MFD_ERR_INVALID_ARG;
@@ -493,7 +488,30 @@ int mfd_verify(const float *target_logits, int n_req, int B, int V, int L, const
   Vl.status = status;
   Vl.ws = static_cast<unsigned long long *>(ws);
   Vl.grid = mfd::verify_max_grid(d.n_sm);
+  Vl.wait_ns = wait_ns;
+  Vl.withhold = withhold;
   return cuda_status(mfd::launch_verify(Vl, s));
+}
+}  // namespace
+
+extern "C" {
+
+int mfd_verify(const float *target_logits, int n_req, int B, int V, int L, const int32_t *parent,
+               const int32_t *token, const int32_t *n_nodes, const float *temperature, const uint64_t *seed,
+               int32_t *accept_len, int32_t *path_nodes, int32_t *out_tokens, int32_t *status, void *ws,
+               size_t ws_bytes, mfd_stream_t stream) {
+  return verify_call(target_logits, n_req, B, V, L, parent, token, n_nodes, temperature, seed, accept_len,
+                     path_nodes, out_tokens, status, ws, ws_bytes, stream, 0ull, 0);
+}
+
+int mfd_verify_withheld_test(const float *target_logits, int n_req, int B, int V, int L, const int32_t *parent,
+                             const int32_t *token, const int32_t *n_nodes, const float *temperature,
+                             const uint64_t *seed, int32_t *accept_len, int32_t *path_nodes, int32_t *out_tokens,
+                             int32_t *status, void *ws, size_t ws_bytes, uint64_t wait_limit_ns,
+                             mfd_stream_t stream) {
+  if (wait_limit_ns < 1000ull || wait_limit_ns > 100000000ull) return MFD_ERR_INVALID_ARG;
+  return verify_call(target_logits, n_req, B, V, L, parent, token, n_nodes, temperature, seed, accept_len,
+                     path_nodes, out_tokens, status, ws, ws_bytes, stream, wait_limit_ns, 1);
 }
 
 }  // extern "C"

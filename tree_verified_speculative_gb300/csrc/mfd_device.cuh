@@ -113,18 +113,6 @@ __device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_
       : "memory");
 }
 
-// As bulk_load_1d, into the shared memory of every CTA of the cluster in
-// cta_mask, at dst's offset in each; the bytes are counted on the mbarrier at
-// bar's offset in each destination CTA.
-__device__ __forceinline__ void bulk_load_1d_mc(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                                uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4, %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
-
 // L2 prefetch of `bytes` (a multiple of 16) at a 16-byte aligned address;
 // nothing tracks its completion.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
@@ -180,27 +168,6 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
-}
-
-// As tc_commit, arriving on the barrier at bar's offset in every CTA of the
-// cluster in cta_mask.
-__device__ __forceinline__ void tc_commit_mc(uint64_t *bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// ---------------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA in the cluster arrives, then waits for all.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives

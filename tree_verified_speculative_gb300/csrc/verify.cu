@@ -100,6 +100,8 @@ struct Params {
   int32_t *accept_len, *path_nodes, *out_tokens, *status;
   unsigned long long *ws;  // [grid][8] words: see Ws
   int cpr;                    // CTAs per request group
+  unsigned long long wait_ns;  // limit of every bounded wait
+  int withhold;                // fault injection: CTAs other than a group's first never publish their slot
 };
 
 // Workspace words, 7 per CTA of the grid: per group g its gen, its leader's
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(THREADS) verify_kernel(const Params p) {
 #pragma unroll
                 for (int j = 0; j < POLL_SLOTS; ++j) all &= 1 + lane + 32 * j >= cpr || rdy[j] == G;
                 if (all) break;
-                if (globaltimer() - t_start > kWaitLimitNs) {
+                if (globaltimer() - t_start > p.wait_ns) {
                   ok = 0;
                   break;
                 }
@@ -313,7 +315,7 @@ __global__ void __launch_bounds__(THREADS) verify_kernel(const Params p) {
 #pragma unroll
               for (int j = 0; j < POLL_SLOTS; ++j) all &= (unsigned)(w[j] & 3ull) == tag;
               if (all) break;
-              if (globaltimer() - t_start > kWaitLimitNs) {
+              if (globaltimer() - t_start > p.wait_ns) {
                 ok = 0;
                 break;
               }
@@ -343,11 +345,11 @@ __global__ void __launch_bounds__(THREADS) verify_kernel(const Params p) {
           } else {
             unsigned long long w = 0ull;
             if (lane == 0) {
-              st_relaxed(ws.slot(blockIdx.x, par), slot_pack(bv, bi, tag));
+              if (!p.withhold) st_relaxed(ws.slot(blockIdx.x, par), slot_pack(bv, bi, tag));
               if (!acquired) {
                 // the group's first CTA has cleared the result words
                 while (rdy[0] != G) {
-                  if (globaltimer() - t_start > kWaitLimitNs) {
+                  if (globaltimer() - t_start > p.wait_ns) {
                     ok = 0;
                     break;
                   }
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(THREADS) verify_kernel(const Params p) {
               }
               w = ld_relaxed(ws.res(grp, par));
               while (ok && (unsigned)(w & 3ull) != tag) {
-                if (globaltimer() - t_start > kWaitLimitNs) {
+                if (globaltimer() - t_start > p.wait_ns) {
                   ok = 0;
                   break;
                 }
@@ -444,6 +446,8 @@ cudaError_t launch_verify(const VerifyLaunch &V, cudaStream_t stream) {
   p.status = V.status;
   p.ws = V.ws;
   p.cpr = verify_cpr(V.grid, V.n_req, V.V);
+  p.wait_ns = V.wait_ns ? V.wait_ns : kWaitLimitNs;
+  p.withhold = V.withhold;
   const int n_groups = V.n_req < V.grid ? V.n_req : V.grid;
   const int grid = (n_groups < V.grid / p.cpr ? n_groups : V.grid / p.cpr) * p.cpr;
   cudaLaunchConfig_t cfg = {};

@@ -33,7 +33,7 @@ MFD_OP_VERIFY = 3
 EXPORTS = ("mfd_status_string", "mfd_workspace_size", "mfd_lmhead_topk", "mfd_lmhead_packed_bytes",
            "mfd_lmhead_pack", "mfd_lmhead_topk_packed", "mfd_lmhead_topk_subset", "mfd_logits_topk",
            "mfd_logits_topk_noalloc",
-           "mfd_build_tree", "mfd_verify")
+           "mfd_build_tree", "mfd_verify", "mfd_verify_withheld_test", "mfd_mfdd_modes")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _lock = threading.Lock()
@@ -79,6 +79,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.mfd_build_tree.restype = I
         lib.mfd_verify.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P]
         lib.mfd_verify.restype = I
+        lib.mfd_verify_withheld_test.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, P, P, SZ,
+                                                 ctypes.c_uint64, P]
+        lib.mfd_verify_withheld_test.restype = I
+        lib.mfd_mfdd_modes.argtypes = [I, I]
+        lib.mfd_mfdd_modes.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -114,6 +119,11 @@ def _s(stream) -> int | None:
 def _check(rc: int, where: str) -> None:
     if rc != MFD_OK:
         raise MfdError(rc, where)
+
+
+def mfd_mfdd_modes(n_req: int, K: int) -> int:
+    """Modes an MFD-D round drafts with: K below three requests, else 1."""
+    return int(load().mfd_mfdd_modes(int(n_req), int(K)))
 
 
 def mfd_workspace_size(op: int, n_req: int = 1, K: int = 1, L: int = 1, topk: int = 1, B: int = 1,
@@ -205,6 +215,18 @@ def mfd_verify(target_logits, n_req, B, V, L, parent, token, n_nodes, temperatur
                            _p(temperature), _p(seed), _p(accept_len), _p(path_nodes), _p(out_tokens),
                            _p(status), _p(ws), ws.numel() * ws.element_size(), _s(stream))
     _check(rc, "mfd_verify")
+
+
+def mfd_verify_withheld_test(target_logits, n_req, B, V, L, parent, token, n_nodes, temperature, seed,
+                             accept_len, path_nodes, out_tokens, status, ws, wait_limit_ns, stream=None) -> None:
+    """mfd_verify with the fault injection of its C entry point: the step
+    results of all but each group's first CTA are withheld and every wait is
+    limited to wait_limit_ns, so *status ends as MFD_ERR_TIMEOUT."""
+    rc = load().mfd_verify_withheld_test(_p_dev_or_pinned(target_logits), n_req, B, V, L, _p(parent), _p(token),
+                                         _p(n_nodes), _p(temperature), _p(seed), _p(accept_len), _p(path_nodes),
+                                         _p(out_tokens), _p(status), _p(ws), ws.numel() * ws.element_size(),
+                                         int(wait_limit_ns), _s(stream))
+    _check(rc, "mfd_verify_withheld_test")
 
 
 # ---------------------------------------------------------------------------

@@ -176,17 +176,3 @@ def round_inputs(W: torch.Tensor, K: int, L: int, n_shared: int, seed: int,
     m = int(rng.integers(0, K))
     s = int(rng.integers(0, 2**63 - 1))
     return Round(h=h, fut=fut, target_mode=m, seed=s)
-
-
-# Workloads of the five cases, named by what they are.
-WORKLOADS = {
-    "tiny_k2_l4_v32_b8": dict(K=2, L=4, V=32, topk=8, B=8, n_req=1),
-    "k8_l15_h2560_v151936_b64_greedy": dict(K=8, L=15, H=2560, V=151936, n_shared=11, topk=16, B=64,
-                                            n_req=1, temperature=0.0),
-    "k8_l15_h2560_v151936_b256_t1": dict(K=8, L=15, H=2560, V=151936, n_shared=11, topk=16, B=256,
-                                         n_req=1, temperature=1.0, rounds=1000),
-    "k8_l15_h5120_v248320_b256_greedy": dict(K=8, L=15, H=5120, V=248320, n_shared=13, topk=32, B=256,
-                                             n_req=1, temperature=0.0),
-    "batch32_k8_l15_h2560_v151936_b128": dict(K=8, L=15, H=2560, V=151936, n_shared=(8, 14), topk=16,
-                                              B=128, n_req=32, temperature="half0_half1"),
-}
