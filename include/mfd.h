@@ -56,7 +56,10 @@ typedef enum {
   MFD_ERR_WORKSPACE = 3,   /* ws NULL or smaller than mfd_workspace_size */
   MFD_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
   MFD_ERR_TIMEOUT = 5,     /* device: a bounded wait ran out (kernel exited early) */
-  MFD_ERR_INPUT = 6        /* device: input values break the contract (see each call) */
+  MFD_ERR_INPUT = 6,       /* device: input values break the contract (see each call) */
+  MFD_ERR_CHECK = 7        /* device, bounds-checked build (libmfd_checked) only: an index
+                              computed from data fell outside its array; the access was
+                              clamped into the array and the results are not to be trusted */
 } mfd_status;
 
 /* Static English text for a status code; never NULL. */

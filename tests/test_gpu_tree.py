@@ -166,3 +166,34 @@ def test_rejects_out_of_limits():
     with pytest.raises(mfd.MfdError) as e:
         rd.build_tree()
     assert e.value.code == mfd.MFD_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("value,shared", [(0.0, True), (0.0, False), (-1.0, True), (-1.0, False)])
+def test_all_equal_log_probs_at_the_limits(value, shared):
+    """Every log p equal, at the largest shape (K=16, L=16, top-32, B=128):
+    every prefix of a depth ties with all others, so the token order decides
+    everything (model card "MFD drafter for Qwen3.5-4B", first paragraph:
+    ties to the lexicographically smaller ids).  At log p = 0 the first B
+    prefixes in that order form a chain of depth L with siblings, the case
+    where the pruning bound is weakest; with shared rows every prefix is
+    held by all 16 modes.  The level search's pass count is bounded by
+    2 + K*B*topk / (pool - K*B) = 39 here, below its limit of 64."""
+    rng = np.random.default_rng(17 if shared else 18)
+    K, L, k, B = 16, 16, 32, 128
+    tk = np.empty((1, K, L, k), np.int32)
+    for i in range(L):
+        row = np.sort(rng.choice(1000, size=k, replace=False))
+        for m in range(K):
+            tk[0, m, i] = row if shared else np.sort(rng.choice(100000, size=k, replace=False))
+    lp = np.full((1, K, L, k), value, np.float32)
+    g = _compare(lp, tk, B)
+    if value == 0.0:
+        assert g["depth"].max() == L
+
+
+def test_two_value_ties_deep_at_the_limits():
+    """Log p drawn from {-0.001, -0.002} at K=16, L=16, top-32, B=128: deep
+    trees where many prefixes tie at the cut-off."""
+    rng = np.random.default_rng(19)
+    lp, tk = _random_tables(rng, 2, 16, 16, 32, 5000, values=np.array([-0.001, -0.002], np.float32))
+    _compare(lp, tk, 128)

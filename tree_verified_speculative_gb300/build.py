@@ -1,5 +1,8 @@
 """Build libmfd.so (sm_103a) in-tree with nvcc: one object per .cu file,
-compiled in parallel, linked with -shared.  Run: python -m tree_verified_speculative_gb300.build"""
+compiled in parallel, linked with -shared.  The same sources built with
+-DMFD_CHECKED give libmfd_checked.so, the bounds-checked build (an index out
+of range is clamped and reported as MFD_ERR_CHECK instead of being used).
+Run: python -m tree_verified_speculative_gb300.build"""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -12,6 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmfd.so")
+LIB_CHECKED = os.path.join(BUILD, "libmfd_checked.so")
 SOURCES = ["lmhead.cu", "topk.cu", "tree.cu", "verify.cu", "mfd_api.cu"]
 HEADERS = ["lmhead.h", "mfd_device.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -30,32 +34,41 @@ def _newest_input() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def _compile(src: str) -> tuple[str, str]:
-    obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(job: tuple[str, bool]) -> tuple[str, str]:
+    src, checked = job
+    obj = os.path.join(BUILD, src.replace(".cu", "_checked.o" if checked else ".o"))
+    cmd = [nvcc(), *ARCH, *FLAGS, *(["-DMFD_CHECKED"] if checked else []), "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
     return obj, r.stderr
 
 
+def _link(objs: list[str], out: str) -> None:
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, out)
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Both libraries; returns the path of libmfd.so."""
     os.makedirs(BUILD, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
+    newest = _newest_input()
+    if (not force and all(os.path.exists(p) and os.path.getmtime(p) >= newest for p in (LIB, LIB_CHECKED))):
         return LIB
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(_compile, SOURCES))
-    log = "\n".join(err for _, err in results)
+    jobs = [(s, False) for s in SOURCES] + [(s, True) for s in SOURCES]
+    with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        results = list(ex.map(_compile, jobs))
+    log = "\n".join(err for _, err in results[:len(SOURCES)])
     with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
         f.write(log)
     if verbose:
         print(log)
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    _link([o for o, _ in results[:len(SOURCES)]], LIB)
+    _link([o for o, _ in results[len(SOURCES):]], LIB_CHECKED)
     return LIB
 
 

@@ -197,6 +197,7 @@ const char *mfd_status_string(int status) {
     case MFD_ERR_CUDA: return "a CUDA runtime or driver call failed";
     case MFD_ERR_TIMEOUT: return "a bounded device wait ran out; the kernel stopped early";
     case MFD_ERR_INPUT: return "input values break the contract (see mfd.h)";
+    case MFD_ERR_CHECK: return "bounds-checked build: an index out of range was clamped";
     default: return "unknown status";
   }
 }

@@ -41,6 +41,38 @@ namespace {
 
 constexpr int THREADS = 512;
 constexpr int NWARPS = THREADS / 32;
+
+// Checked build (compiled with -DMFD_CHECKED): every shared-memory index the
+// kernel computes from data is tested against its array's extent.  An index
+// out of range is clamped into the array, so the access stays in bounds, and
+// the CTA ends with MFD_ERR_CHECK in *status.  The ordinary build compiles
+// CHK(i, n) to i.
+#ifdef MFD_CHECKED
+__shared__ int chk_bad_s;
+__device__ __forceinline__ int chk_index(int i, int n) {
+  if ((unsigned)i >= (unsigned)n) {
+    chk_bad_s = 1;
+    return i < 0 ? 0 : n - 1;
+  }
+  return i;
+}
+#define CHK(i, n) chk_index((int)(i), (int)(n))
+#define CHK_INIT() \
+  if (threadIdx.x == 0) chk_bad_s = 0
+#define CHK_REPORT()                                                    \
+  do {                                                                  \
+    __syncthreads();                                                    \
+    if (threadIdx.x == 0 && chk_bad_s) report(prm.status, MFD_ERR_CHECK); \
+  } while (0)
+#else
+#define CHK(i, n) (i)
+#define CHK_INIT() \
+  do {             \
+  } while (0)
+#define CHK_REPORT() \
+  do {               \
+  } while (0)
+#endif
 constexpr int MAX_PASSES = 64;
 constexpr int PLIST = 1024;     // parents listed for pair-parallel expansion
 constexpr int PAIR_MAX = 4096;  // (parent, rank) pairs expanded at once
@@ -199,7 +231,7 @@ struct Ctx {
 // token at position p (1-based) of an entry
 __device__ __forceinline__ uint32_t token_at(const Ctx &c, const PE &e, int p) {
   const int row = (pk_mode(e.k1) * c.L + p - 1) * c.topk;
-  return (uint32_t)c.tok[row + pk_get(e.k0, e.k1, p)];
+  return (uint32_t)c.tok[CHK(row + (int)pk_get(e.k0, e.k1, p), c.K * c.L * c.topk)];
 }
 
 // Token order of two prefixes of any modes (unsigned ids, a proper prefix
@@ -339,8 +371,8 @@ __device__ int compact_pool(Shared &sh, PE *ent, uint8_t *nxt, int n, KeepFn kee
       if (!__any_sync(0xffffffffu, kp[j])) continue;
       const int slot = warp_append(&sh.n_out, kp[j]);
       if (kp[j]) {
-        ent[slot] = e[j];
-        nxt[slot] = nx[j];
+        ent[CHK(slot, n)] = e[j];
+        nxt[CHK(slot, n)] = nx[j];
       }
     }
   }
@@ -480,6 +512,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
 
   const float *glp = prm.tk_logp + (size_t)q * KLT;
   const int32_t *gtk = prm.tk_tok + (size_t)q * KLT;
+  CHK_INIT();
   pdl_wait();  // the tables may come from the grid launched just before
   pdl_launch_dependents();
 
@@ -541,6 +574,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     for (int w = 0; w < NWARPS; ++w) any_bad |= sh.wbad[w];
     if (any_bad) {
       if (tid == 0) report(prm.status, MFD_ERR_INPUT);
+      CHK_REPORT();
       return;
     }
   }
@@ -665,8 +699,8 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
           while (x - off >= sh.f1[k]) off += sh.f1[k++];
           j = x - off;
         }
-        const bool own = sh.u1[k * topk + j];
-        en.score = lp_s[(k * L) * topk + j];
+        const bool own = sh.u1[CHK(k * topk + j, K * topk)];
+        en.score = lp_s[CHK((k * L) * topk + j, KLT)];
         en.k0 = 0;
         en.k1 = 1u | ((uint32_t)k << 25) | (own ? K1_OWNED : 0u);
         pk_set(en.k0, en.k1, 1, (uint32_t)j);
@@ -690,8 +724,8 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         a = r / f2;
         b2 = r - a * f2;
       }
-      const bool own = sh.u1[k * topk + a];
-      en.score = __fadd_rn(lp_s[(k * L) * topk + a], lp_s[(k * L + 1) * topk + b2]);
+      const bool own = sh.u1[CHK(k * topk + a, K * topk)];
+      en.score = __fadd_rn(lp_s[CHK((k * L) * topk + a, KLT)], lp_s[CHK((k * L + 1) * topk + b2, KLT)]);
       en.k0 = 0;
       en.k1 = 2u | ((uint32_t)k << 25) | (own ? K1_OWNED : 0u);
       pk_set(en.k0, en.k1, 1, (uint32_t)a);
@@ -756,16 +790,16 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
           }
           const int slot = warp_append(&sh.n_ent, want);
           if (want) {
-            ent[slot] = en;
-            nxt[slot] = x < N1 ? (uint8_t)topk : 0;
+            ent[CHK(slot, CAP)] = en;
+            nxt[CHK(slot, CAP)] = x < N1 ? (uint8_t)topk : 0;
           }
         }
       } else {
         for (int x = tid; x < N1; x += THREADS) {
           PE en;
           make(x, en);
-          ent[x] = en;
-          nxt[x] = 0;
+          ent[CHK(x, CAP)] = en;
+          nxt[CHK(x, CAP)] = 0;
         }
         if (tid == 0) sh.n_ent = N1;
       }
@@ -776,8 +810,8 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         if (x < N1 + N2) {
           PE en;
           const bool own = make(x, en);
-          ent[x] = en;
-          nxt[x] = x < N1 && two ? (uint8_t)topk : 0;
+          ent[CHK(x, CAP)] = en;
+          nxt[CHK(x, CAP)] = x < N1 && two ? (uint8_t)topk : 0;
           if (own) bin = bin_of(en.score);
         }
         if (bin >= 0) atomicAdd(&hist[bin], 1);  // bins here are mostly distinct within a warp
@@ -874,7 +908,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
           if (pk_depth(e.k1) == t && j < topk) {
             // the next rank is the best remaining child: if it misses the
             // bound, so do the others
-            const float lv = lp_s[(pk_mode(e.k1) * L + t) * topk + j];
+            const float lv = lp_s[CHK((pk_mode(e.k1) * L + t) * topk + j, KLT)];
             isp = lv > -INFINITY && (!ht || desc_key(__fadd_rn(e.score, lv)) <= tau);
           }
         }
@@ -890,10 +924,11 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
           bool want = false;
           PE ch;
           if (x < np * topk) {
-            const int i = plist[x / topk], j = x - (x / topk) * topk;
+            const int i = CHK(plist[CHK(x / topk, PLIST)], n0);
+            const int j = x - (x / topk) * topk;
             const PE par = ent[i];
             const int row = (pk_mode(par.k1) * L + t) * topk;
-            const float lv = lp_s[row + j];
+            const float lv = lp_s[CHK(row + j, KLT)];
             if (j >= nxt[i] && lv > -INFINITY) {
               ch.score = __fadd_rn(par.score, lv);
               if (!ht || desc_key(ch.score) <= tau) {
@@ -907,12 +942,12 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
           }
           const int slot = warp_append(&sh.n_ent, want);
           if (want) {
-            ent[slot] = ch;
-            nxt[slot] = 0;
+            ent[CHK(slot, CAP)] = ch;
+            nxt[CHK(slot, CAP)] = 0;
           }
         }
         __syncthreads();
-        for (int pi = tid; pi < np; pi += THREADS) nxt[plist[pi]] = (uint8_t)topk;
+        for (int pi = tid; pi < np; pi += THREADS) nxt[CHK(plist[pi], n0)] = (uint8_t)topk;
       } else {
         for (int base = warp * 32; base < n0; base += THREADS) {
           const int i = base + lane;
@@ -930,7 +965,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
             bool want = false;
             PE ch;
             if (act) {
-              const float lv = lp_s[row + j];
+              const float lv = lp_s[CHK(row + j, KLT)];
               if (!(lv > -INFINITY)) {
                 act = false;
                 j = topk;
@@ -979,6 +1014,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   }
   if (failed) {
     if (tid == 0) report(prm.status, MFD_ERR_UNSUPPORTED);
+    CHK_REPORT();
     return;
   }
 
@@ -996,6 +1032,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     prune_exact();
     if (sh.n_ent > NC) {
       if (tid == 0) report(prm.status, MFD_ERR_UNSUPPORTED);
+      CHK_REPORT();
       return;
     }
   }
@@ -1038,15 +1075,15 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         if (t0 == 0u) {
           const uint32_t prev = atomicCAS(&tag[s], 0u, tg);
           if (prev == 0u) {
-            rep[s] = (uint16_t)i;
+            rep[CHK(s, tsize)] = (uint16_t)i;
             break;
           }
           if (prev == tg) break;
         }
         s = (s + 1) & (uint32_t)(tsize - 1);
       }
-      hslot[i] = (uint16_t)s;
-      atomicMin(&bkey[s], desc_key(e.score));
+      hslot[CHK(i, NC)] = (uint16_t)s;
+      atomicMin(&bkey[CHK(s, tsize)], desc_key(e.score));
     }
     __syncthreads();
 #pragma unroll
@@ -1054,8 +1091,8 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       const int i = tid + jj * THREADS;
       if (i >= n) continue;
       const PE e = ent[i];
-      const int s = hslot[i];
-      const int r = rep[s];
+      const int s = CHK(hslot[i], tsize);
+      const int r = CHK(rep[s], n);
       if (r != i && seq_cmp(c, e, ent[r]) != 0) sh.coll = 1;
       if (desc_key(e.score) == bkey[s]) atomicMin(&bsub[s], ((uint32_t)pk_mode(e.k1) << 16) | (uint32_t)i);
       // the parent's slot: same tag, a representative one token shorter
@@ -1069,7 +1106,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
           const uint32_t t0 = tag[q];
           if (t0 == 0u) break;
           if (t0 == tg) {
-            const PE g = ent[rep[q]];
+            const PE g = ent[CHK(rep[q], n)];
             bool same = pk_depth(g.k1) == d - 1;
             for (int p = 1; p < d && same; ++p) same = token_at(c, g, p) == token_at(c, e, p);
             if (same) {
@@ -1080,7 +1117,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
           q = (q + 1) & (uint32_t)(tsize - 1);
         }
       }
-      pslot[i] = ps;
+      pslot[CHK(i, NC)] = ps;
     }
     __syncthreads();
     if (!sh.coll) break;
@@ -1089,6 +1126,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   }
   if (sh.coll) {
     if (tid == 0) report(prm.status, MFD_ERR_UNSUPPORTED);
+    CHK_REPORT();
     return;
   }
   // primaries; with few candidates every primary is selected right away
@@ -1097,15 +1135,15 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     const int i = base + lane;
     bool pr = false;
     if (i < n) {
-      pr = (int)(bsub[hslot[i]] & 0xFFFF) == i;
+      pr = (int)(bsub[CHK(hslot[i], tsize)] & 0xFFFF) == i;
       prim[i] = pr;
       nodeid[i] = -1;
     }
     if (n <= RANK_ALL) {
       const int k = warp_append(&sh.n_sel, pr);
       if (pr) {
-        sel[k] = (uint16_t)i;
-        skk[k] = desc_key(ent[i].score);
+        sel[CHK(k, NC)] = (uint16_t)i;
+        skk[CHK(k, NC)] = desc_key(ent[i].score);
       }
     }
   }
@@ -1125,8 +1163,8 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       const bool in = i < n && prim[i] && (!ht_sel || desc_key(ent[i].score) <= tau_sel);
       const int k = warp_append(&sh.n_sel, in);
       if (in) {
-        sel[k] = (uint16_t)i;
-        skk[k] = desc_key(ent[i].score);
+        sel[CHK(k, NC)] = (uint16_t)i;
+        skk[CHK(k, NC)] = desc_key(ent[i].score);
       }
     }
     __syncthreads();
@@ -1190,7 +1228,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       // keys below, then token order among the equal keys: per run, the
       // keys below its lower bound, then its block of equal keys
       lt = 0;
-      const PE ea = ent[sel[ia]];
+      const PE ea = ent[CHK(sel[CHK(ia, NC)], n)];
       for (int u = 0; u < nruns; ++u) {
         const uint32_t *run = skk + u * 32;
         int lo = 0;
@@ -1200,13 +1238,13 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         lt += lo;
         for (int p = lo; p < 32 && run[p] == key; ++p) {
           const int b = u * 32 + p;
-          if (ra[b] != ia && ra[b] < ns && seq_cmp(c, ent[sel[ra[b]]], ea) < 0) ++lt;
+          if (ra[b] != ia && ra[b] < ns && seq_cmp(c, ent[CHK(sel[ra[b]], n)], ea) < 0) ++lt;
         }
       }
     }
     if (real && lt < B) {
-      nslot[lt + 1] = sel[ia];
-      nodeid[sel[ia]] = (int16_t)(lt + 1);
+      nslot[CHK(lt + 1, B + 1)] = sel[CHK(ia, NC)];
+      nodeid[CHK(sel[CHK(ia, NC)], NC)] = (int16_t)(lt + 1);
     }
   }
   if (tid == 0) {
@@ -1218,11 +1256,11 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
 
   // ---------------------------------------------------- parents
   for (int nd = 1 + tid; nd <= nn; nd += THREADS) {
-    const int i = nslot[nd];
+    const int i = CHK(nslot[nd], n);
     int par = 0;
     if (pk_depth(ent[i].k1) > 1) {
       const int ps = pslot[i];
-      par = ps == 0xFFFF ? -1 : nodeid[bsub[ps] & 0xFFFF];
+      par = ps == 0xFFFF ? -1 : nodeid[CHK(bsub[CHK(ps, tsize)] & 0xFFFF, NC)];
       if (par < 1 || par >= nd) sh.bad = 1;
     }
     par_s[nd] = (int16_t)par;
@@ -1230,6 +1268,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
   __syncthreads();
   if (sh.bad) {
     if (tid == 0) report(prm.status, MFD_ERR_INPUT);
+    CHK_REPORT();
     return;
   }
 
@@ -1247,7 +1286,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       sc = 0.f;
       ps = bp;
     } else if (nd <= nn) {
-      const PE e = ent[nslot[nd]];
+      const PE e = ent[CHK(nslot[nd], n)];
       dp = pk_depth(e.k1);
       pa = par_s[nd];
       tk = (int)token_at(c, e, dp);
@@ -1269,11 +1308,12 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
 #pragma unroll
     for (int w = 0; w < MAX_MASK_WORDS; ++w) m[w] = 0u;
     if (i <= nn)
-      for (int a = i; a >= 0; a = (a == 0) ? -1 : par_s[a]) m[a >> 5] |= 1u << (a & 31);
+      for (int a = i; a >= 0; a = (a == 0) ? -1 : par_s[CHK(a, B + 1)]) m[CHK(a >> 5, MAX_MASK_WORDS)] |= 1u << (a & 31);
     uint32_t *row = prm.mask + ((size_t)q * N + i) * W32;
     for (int w = 0; w < W32; ++w) row[w] = m[w];
   }
   if (tid == 0) prm.n_nodes[q] = nn + 1;
+  CHK_REPORT();
 }
 
 int next_pow2(int x) {

@@ -16,6 +16,7 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libmfd.so")
+CHECKED_LIB_PATH = os.path.join(_HERE, "_build", "libmfd_checked.so")
 
 MFD_OK = 0
 MFD_ERR_INVALID_ARG = 1
@@ -24,6 +25,7 @@ MFD_ERR_WORKSPACE = 3
 MFD_ERR_CUDA = 4
 MFD_ERR_TIMEOUT = 5
 MFD_ERR_INPUT = 6
+MFD_ERR_CHECK = 7
 
 MFD_OP_LMHEAD_TOPK = 0
 MFD_OP_LOGITS_TOPK = 1
@@ -38,6 +40,7 @@ NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _lock = threading.Lock()
 _lib = None
+_libs: dict[str, ctypes.CDLL] = {}
 
 
 class MfdError(RuntimeError):
@@ -46,13 +49,28 @@ class MfdError(RuntimeError):
         self.code = code
 
 
+def use_library(path: str | None) -> None:
+    """Route every call of this module through the library at `path` (for
+    instance CHECKED_LIB_PATH, the bounds-checked build), or back to
+    libmfd.so with None."""
+    global _lib
+    lib = load(path or LIB_PATH)
+    with _lock:
+        _lib = lib
+
+
 def load(path: str | None = None) -> ctypes.CDLL:
-    """Load libmfd.so; raises if it is missing (no fallback)."""
+    """Load libmfd.so (or the library at `path`); raises if it is missing (no
+    fallback)."""
     global _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
         p = path or LIB_PATH
+        if p in _libs:
+            if path is None:
+                _lib = _libs[p]
+            return _libs[p]
         if not os.path.exists(p):
             raise RuntimeError(f"libmfd.so not built ({p}); run `python -m tree_verified_speculative_gb300.build`")
         lib = ctypes.CDLL(p)
@@ -84,6 +102,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.mfd_verify_withheld_test.restype = I
         lib.mfd_mfdd_modes.argtypes = [I, I]
         lib.mfd_mfdd_modes.restype = I
+        _libs[p] = lib
         if path is None:
             _lib = lib
         return lib
