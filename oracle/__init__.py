@@ -14,6 +14,9 @@ numpy arrays.  Each function cites the passage of the pages it follows:
   states; project page "Multi-Future Drafting", How it works, step 2: one
   distribution per (mode, position).
 * ``logits_topk`` -- the same log-softmax and top-k from given fp32 logits.
+* ``e4m3`` / ``e4m3_value`` / ``fp8_quantize`` / ``lmhead_fp8_topk`` -- the
+  FP8 drafter head: project page, In a serving engine, Figure 5 caption (the
+  drafter's linear layers in FP8, quantized online; acceptance unchanged).
 * ``build_tree`` -- project page, How it works, step 3: prefixes scored by
   their best mode, the B best kept as one tree, found by merging the K
   per-mode best-first searches into one heap.
@@ -68,6 +71,14 @@ def _load():
             lib.oracle_lmhead_logits.restype = None
             lib.oracle_lmhead_topk.argtypes = [P, i32, i32, P, i32, i32, P, P, P, i32]
             lib.oracle_lmhead_topk.restype = i32
+            lib.oracle_e4m3.argtypes = [f32]
+            lib.oracle_e4m3.restype = ctypes.c_uint8
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
+            lib.oracle_fp8_quantize.argtypes = [P, ctypes.c_size_t, P, P]
+            lib.oracle_fp8_quantize.restype = None
+            lib.oracle_lmhead_fp8_topk.argtypes = [P, i32, i32, P, i32, i32, P, P, P, P, P, i32]
+            lib.oracle_lmhead_fp8_topk.restype = i32
             lib.oracle_logits_topk.argtypes = [P, i32, i32, i32, P, P, P]
             lib.oracle_logits_topk.restype = i32
             lib.oracle_build_tree.argtypes = [P, P, i32, i32, i32, i32, ctypes.c_int32,
@@ -132,6 +143,50 @@ def lmhead_topk(h, W, topk: int, nthreads: int = 0):
     if rc:
         raise ValueError(f"oracle_lmhead_topk failed ({rc})")
     return lp, tk, lse
+
+
+def e4m3(x) -> np.ndarray:
+    """FP8 E4M3 bytes of fp32 values: round to nearest even, saturating at
+    +-448 (project page "Multi-Future Drafting", Figure 5 caption: the
+    drafter's linears in FP8; the format reading is in mfd_oracle.c)."""
+    a = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    lib = _load()
+    return np.array([lib.oracle_e4m3(float(v)) for v in a], np.uint8).reshape(np.shape(x))
+
+
+def e4m3_value(b) -> np.ndarray:
+    """Exact values of E4M3 bytes (NaN for 0x7F / 0xFF)."""
+    a = np.ascontiguousarray(b, dtype=np.uint8).reshape(-1)
+    lib = _load()
+    return np.array([lib.oracle_e4m3_value(int(v)) for v in a], np.float64).reshape(np.shape(b))
+
+
+def fp8_quantize(x) -> tuple[np.ndarray, float]:
+    """One scale for all of x (bf16): (E4M3 bytes, scale = max|x| / 448)."""
+    xb = _bf16_bits(x)
+    q = np.empty(xb.shape, np.uint8)
+    sc = ctypes.c_float()
+    _load().oracle_fp8_quantize(_ptr(xb), xb.size, _ptr(q), ctypes.byref(sc))
+    return q, float(sc.value)
+
+
+def lmhead_fp8_topk(h, W, topk: int, nthreads: int = 0):
+    """The FP8 LM head (weight one scale, each hidden row its own), then the
+    log-softmax and top-k as lmhead_topk.  Returns (tk_logp, tk_tok, lse,
+    weight scale, row scales [R])."""
+    hb, wb = _bf16_bits(h), _bf16_bits(W)
+    R, H = hb.shape
+    V = wb.shape[0]
+    lp = np.empty((R, topk), np.float32)
+    tk = np.empty((R, topk), np.int32)
+    lse = np.empty((R,), np.float64)
+    t = np.empty((R,), np.float32)
+    sW = ctypes.c_float()
+    rc = _load().oracle_lmhead_fp8_topk(_ptr(hb), R, H, _ptr(wb), V, topk, _ptr(lp), _ptr(tk), _ptr(lse),
+                                       ctypes.byref(sW), _ptr(t), nthreads)
+    if rc:
+        raise ValueError(f"oracle_lmhead_fp8_topk failed ({rc})")
+    return lp, tk, lse, float(sW.value), t
 
 
 def logits_topk(logits: np.ndarray, topk: int):

@@ -157,6 +157,126 @@ int oracle_lmhead_topk(const uint16_t *h, int R, int H, const uint16_t *W, int V
 }
 
 /* ------------------------------------------------------------------------ */
+/* [PP] "In a serving engine", Figure 5 caption: the drafter's linear layers
+ * run in FP8 with the serving engine's online option -- the weight quantized
+ * once when it is loaded, the activations quantized on the fly -- and the
+ * acceptance length does not change.  The pages name no format or scale
+ * granularity; the reading here: FP8 E4M3 (4 exponent bits, bias 7, 3
+ * mantissa bits, no infinities, largest finite 448), one scale for the whole
+ * weight, one scale per hidden-state row, each the row's (tensor's) largest
+ * magnitude over 448, values rounded to nearest-even and saturated at 448.
+ *
+ * Every fp32 step below is one IEEE-rounded float operation. */
+#define E4M3_MAX 448.0f
+
+/* float -> E4M3 byte, round to nearest even, saturating to +-448; NaN -> 0x7F.
+ * Written from the format: normal numbers (1 + m/8) 2^(e-7) for exponent
+ * fields e = 1..15 (0x7F and 0xFF are NaN), subnormals (m/8) 2^-6. */
+uint8_t oracle_e4m3(float x) {
+  uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  if (isnan(x)) return (uint8_t)(sign | 0x7F);
+  double a = fabs((double)x);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e);            /* a = f 2^e with f in [0.5, 1): a in [2^(e-1), 2^e) */
+  int ex = e - 1;          /* unbiased exponent of a */
+  if (ex < -6) ex = -6;    /* subnormal range shares the quantum of the smallest binade */
+  double quantum = ldexp(1.0, ex - 3);
+  double r = nearbyint(a / quantum) * quantum; /* exact scaling; ties to even (default mode) */
+  if (r > (double)E4M3_MAX) r = (double)E4M3_MAX;
+  if (r == 0.0) return sign;
+  int er;
+  double fr = frexp(r, &er);                  /* r = fr 2^er, fr in [0.5, 1) */
+  int unb = er - 1;
+  if (unb < -6) {                              /* subnormal: r = m 2^-9 */
+    int m = (int)ldexp(r, 9);
+    return (uint8_t)(sign | (uint8_t)m);
+  }
+  int mant = (int)ldexp(fr * 2.0 - 1.0, 3);    /* 3 mantissa bits */
+  return (uint8_t)(sign | (uint8_t)((unb + 7) << 3) | (uint8_t)mant);
+}
+
+/* E4M3 byte -> its exact value. */
+double oracle_e4m3_value(uint8_t b) {
+  int sign = b & 0x80, ef = (b >> 3) & 15, m = b & 7;
+  if (ef == 15 && m == 7) return NAN;
+  double v = ef == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, ef - 7);
+  return sign ? -v : v;
+}
+
+/* Quantize n bf16 values with one scale: amax = max |x|, inv = 448 / amax,
+ * q = e4m3(x * inv), scale = amax / 448 (an all-zero input gives inv = 0 and
+ * scale 0). */
+void oracle_fp8_quantize(const uint16_t *x, size_t n, uint8_t *q, float *scale) {
+  float amax = 0.0f;
+  for (size_t i = 0; i < n; ++i) {
+    float a = fabsf(bf16_to_float(x[i]));
+    if (a > amax) amax = a;
+  }
+  float inv = amax > 0.0f ? E4M3_MAX / amax : 0.0f;
+  for (size_t i = 0; i < n; ++i) q[i] = oracle_e4m3(bf16_to_float(x[i]) * inv);
+  *scale = amax / E4M3_MAX;
+}
+
+/* The FP8 LM head, log-softmax and top-k: W quantized with one scale sW, each
+ * hidden row r with its own scale t_r; z[r][v] = f_r * sum_h q_h[r][h] q_W[v][h]
+ * with f_r = t_r * sW (one fp32 product), the sum of exact E4M3 products in
+ * double; then the log-softmax and top-k of row_logsoftmax_topk.  Outputs as
+ * oracle_lmhead_topk, plus the quantized weight's scale (sW) and the rows'
+ * scales (t, [R]). */
+int oracle_lmhead_fp8_topk(const uint16_t *h, int R, int H, const uint16_t *W, int V, int topk,
+                           float *tk_logp, int32_t *tk_tok, double *lse, float *sW_out, float *t_out,
+                           int nthreads) {
+  if (topk < 1 || topk > V) return 1;
+  uint8_t *qW = (uint8_t *)malloc((size_t)V * H);
+  uint8_t *qh = (uint8_t *)malloc((size_t)R * H);
+  double *z = (double *)malloc(sizeof(double) * (size_t)R * V);
+  float *t = (float *)malloc(sizeof(float) * (size_t)R);
+  double lut[256];
+  if (!qW || !qh || !z || !t) { free(qW); free(qh); free(z); free(t); return 2; }
+  for (int b = 0; b < 256; ++b) lut[b] = oracle_e4m3_value((uint8_t)b);
+  float sW;
+  oracle_fp8_quantize(W, (size_t)V * H, qW, &sW);
+  for (int r = 0; r < R; ++r) oracle_fp8_quantize(h + (size_t)r * H, (size_t)H, qh + (size_t)r * H, &t[r]);
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+  for (int v = 0; v < V; ++v) {
+    const uint8_t *w = qW + (size_t)v * H;
+    for (int r = 0; r < R; ++r) {
+      const uint8_t *x = qh + (size_t)r * H;
+      double acc = 0.0;
+      for (int k = 0; k < H; ++k) acc += lut[x[k]] * lut[w[k]];
+      const float f = t[r] * sW;
+      z[(size_t)r * V + v] = (double)f * acc;
+    }
+  }
+  int err = 0;
+#ifdef _OPENMP
+#pragma omp parallel
+#endif
+  {
+    lp_tok *scr = (lp_tok *)malloc(sizeof(lp_tok) * (size_t)V);
+    if (!scr) {
+      err = 2;
+    } else {
+#ifdef _OPENMP
+#pragma omp for schedule(static)
+#endif
+      for (int r = 0; r < R; ++r)
+        row_logsoftmax_topk(z + (size_t)r * V, V, topk, tk_logp + (size_t)r * topk,
+                            tk_tok + (size_t)r * topk, lse ? lse + r : NULL, scr);
+      free(scr);
+    }
+  }
+  if (sW_out) *sW_out = sW;
+  if (t_out) memcpy(t_out, t, sizeof(float) * (size_t)R);
+  free(qW); free(qh); free(z); free(t);
+  return err;
+}
+
+/* ------------------------------------------------------------------------ */
 /* [PP] step 3: mixture DDTree.
  *
  * Mode k scores a prefix x = (x_1..x_d) by the fp32 left fold of its
