@@ -41,6 +41,10 @@ WORKLOADS = {
     # head covers a subset of the vocabulary, the walk verifies the full one
     "k8_l15_h2560_v151936_sub65536_b256_t1": dict(K=8, L=15, H=2560, V=151936, V_draft=65536, n_shared=11,
                                                   topk=16, B=256, T=1.0),
+    # the default workload with the drafter's head in FP8 (E4M3 weight packed
+    # once, hidden rows quantized per call): half the weight bytes
+    "k8_l15_h2560_v151936_b256_t1_fp8": dict(K=8, L=15, H=2560, V=151936, n_shared=11, topk=16, B=256, T=1.0,
+                                             fp8=True),
     # a small shape for quick host-side runs (the reference arm in CPU tests)
     "tiny": dict(K=2, L=4, H=64, V=512, n_shared=2, topk=8, B=16, T=1.0),
     # 32 requests in one round (3840 LM-head rows, one shared W): the
@@ -219,16 +223,24 @@ class DraftHead:
         from tree_verified_speculative_gb300 import mfd
 
         self.ids = draft_vocab(cfg)
+        self.fp8 = bool(cfg.get("fp8"))
         self.W_host = W if self.ids is None else W[torch.from_numpy(self.ids.astype(np.int64))].contiguous()
         self.V = self.W_host.shape[0]
+        self.H = self.W_host.shape[1]
         Wd = self.W_host.to(dev)
-        self.Wp = mfd.pack_lm_head(Wd)
+        self.Wp = mfd.pack_lm_head_fp8(Wd) if self.fp8 else mfd.pack_lm_head(Wd)
         del Wd
         self.ids_d = None if self.ids is None else torch.from_numpy(self.ids).to(dev)
-        self.name = "mfd_lmhead_topk_packed" if self.ids is None else "mfd_lmhead_topk_subset"
+        self.name = ("mfd_lmhead_topk_fp8" if self.fp8 else
+                     "mfd_lmhead_topk_packed" if self.ids is None else "mfd_lmhead_topk_subset")
+        # bytes the head must stream per call: the weight (1 byte a value in
+        # FP8, 2 in bf16) and the bf16 hidden rows
+        self.weight_bytes = self.V * self.H * (1 if self.fp8 else 2)
 
     def __call__(self, rd, h):
-        if self.ids_d is None:
+        if self.fp8:
+            rd.lmhead_topk_fp8(h, self.Wp)
+        elif self.ids_d is None:
             rd.lmhead_topk_packed(h, self.Wp)
         else:
             rd.lmhead_topk_subset(h, self.Wp, self.ids_d)
@@ -270,7 +282,7 @@ def run_gpu(args, ws, rank, local):
     t_dev = [torch.from_numpy(x).to(dev) for x in noise]
     temp = torch.tensor([T], dtype=torch.float32, device=dev)
     seeds = torch.tensor(np.array([r.seed for r in rounds], np.uint64).view(np.int64), device=dev)
-    rd = mfd.Round(1, K, L, topk, B, V, device=dev, V_draft=head.V)
+    rd = mfd.Round(1, K, L, topk, B, V, device=dev, V_draft=head.V, H=H)
     rd.status.zero_()
     N = B + 1
     acc_buf = torch.zeros((n_rounds,), dtype=torch.int32, device=dev)
@@ -389,18 +401,20 @@ def run_gpu(args, ws, rank, local):
     # ------------------------------------------------------------ roofline
     peak, peak_kind = peaks()
     lm_us = lm / steps * 1e3
-    algo_bytes = head.V * H * 2 + R * H * 2
+    algo_bytes = head.weight_bytes + R * H * 2
     achieved = algo_bytes / (lm_us * 1e-6) / 1e9
     traffic = profiled_traffic()
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "rounds/s", "n_gpus": ws, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / steps, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 (fp32 accumulate)" if head.fp8 else "bf16",
+        "data": "synthetic",
         "config": {"workload": args.workload, "K": K, "L": L, "H": H, "V": V, "topk": topk, "B": B,
                    "temperature": T, "n_req": 1, "parallelism": f"replicas{ws}" if ws > 1 else "single",
                    **({"V_draft": head.V} if head.ids is not None else {}),
-                   "lm_head_weight": f"packed once before timing (mfd_lmhead_pack), streamed by {head.name}",
-                   "l2": "inputs larger than L2 (W = %.0f MB streamed every round)" % (head.V * H * 2 / 1e6),
+                   "lm_head_weight": "packed once before timing (%s), streamed by %s"
+                                     % ("mfd_lmhead_pack_fp8" if head.fp8 else "mfd_lmhead_pack", head.name),
+                   "l2": "inputs larger than L2 (W = %.0f MB streamed every round)" % (head.weight_bytes / 1e6),
                    "timing": "sum over the timed rounds of two CUDA-event intervals per round, one around the LM head and the tree (back to back, as in a real round) and one around the verification, with the queue kept ahead of the GPU; the target plant (input generation that needs the round's tree) is untimed; the per-stage split comes from separate diagnostic rounds"},
         "stages_us": {"lmhead_topk_plus_build_tree": round(ab / steps * 1e3, 2), "verify": round(vf / steps * 1e3, 2),
                       "split_from_diagnostic_rounds": {"lmhead_topk": round(sum(lm_d) / len(diag) * 1e3, 2),
@@ -408,11 +422,13 @@ def run_gpu(args, ws, rank, local):
                                                        "rounds": len(diag)}},
         "stages_us_median": med,
         "mean_accept_len": round(float(acc.mean()), 4),
-        "roofline": {"kernel": f"{head.name} (lmhead_topk_kernel + merge_topk_kernel)", "bound": "hbm",
+        "roofline": {"kernel": f"{head.name} ({'quant_rows_kernel + ' if head.fp8 else ''}lmhead_topk_kernel + "
+                               "merge_topk_kernel)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": algo_bytes, "traffic": traffic},
-        "gpu_launches": 4 * steps,
+                     "algorithmic_bytes_per_launch": algo_bytes,
+                     "traffic": traffic if args.workload == DEFAULT else None},
+        "gpu_launches": (5 if head.fp8 else 4) * steps,
         "clocks": ck,
         "wall_s_timed_loop": round(wall1 - wall0, 3),
         "e2e": e2e,
@@ -664,7 +680,10 @@ def cpu_baseline(cfg, head, r, rd, noise, site):
     hb, wb = bits(r.h[:rows]), bits(head.W_host)
     oracle.build()
     t0 = time.perf_counter()
-    lp, tk, _ = oracle.lmhead_topk(hb, wb, topk)
+    if head.fp8:
+        lp, tk, _, _, _ = oracle.lmhead_fp8_topk(hb, wb, topk)
+    else:
+        lp, tk, _ = oracle.lmhead_topk(hb, wb, topk)
     t_lm = (time.perf_counter() - t0) * (R / rows)
     if head.ids is not None:
         tk = head.ids[tk]  # draft-vocabulary rows to vocabulary ids
@@ -788,7 +807,7 @@ def profile_rounds(args, local):
     head = DraftHead(cfg, W, dev)  # the packed copy is all the rounds read
     del W
     torch.cuda.empty_cache()
-    rd = mfd.Round(n_req, cfg["K"], cfg["L"], cfg["topk"], cfg["B"], cfg["V"], device=dev, V_draft=head.V)
+    rd = mfd.Round(n_req, cfg["K"], cfg["L"], cfg["topk"], cfg["B"], cfg["V"], device=dev, V_draft=head.V, H=cfg["H"])
     rd.status.zero_()
     for _ in range(args.profile_rounds):
         head(rd, h)

@@ -130,6 +130,45 @@ int mfd_lmhead_topk_packed(const void *h, int R, int H, const void *W_packed, in
                            float *tk_logp, int32_t *tk_tok, float *lse, int32_t *status, void *ws,
                            size_t ws_bytes, mfd_stream_t stream);
 
+/* FP8 drafter head (project page "Multi-Future Drafting", In a serving
+ * engine, Figure 5 caption: MFD runs its drafter's linear layers in FP8, the
+ * serving engine's online option, and the acceptance length is unchanged;
+ * decoding stays lossless because the walk verifies against the target's own
+ * logits).  The pages name no format or scale granularity; this library's
+ * reading: E4M3 values (round to nearest even, saturating at +-448), one
+ * scale for the whole weight, one scale per hidden row computed on the fly:
+ *   s_W = max|W| / 448,   Wq = e4m3(W * (448 / max|W|))        (once, at load)
+ *   t_r = max|h[r]| / 448, hq = e4m3(h[r] * (448 / max|h[r]|)) (every call)
+ *   z[r][v] = (t_r * s_W) * sum_h hq[r][h] Wq[v][h]   (exact E4M3 products,
+ *                                                       fp32 accumulation)
+ * then the log-softmax and top-k of mfd_lmhead_topk.  An all-zero row or
+ * weight has scale 0.  Every fp32 step is one IEEE-rounded operation.
+ *
+ * mfd_lmhead_packed_fp8_bytes: bytes of the E4M3 packed weight for (V, H):
+ *   per 256-row vocabulary tile and 128-element K slice one 32 KB block of
+ *   the 128-byte-swizzled shared-memory image (as mfd_lmhead_pack, 128 values
+ *   a row), rows past V zero, then a 256-byte trailer whose first word is
+ *   max|W| (fp32).  0 unless H % 128 == 0 and V within the limits.
+ * mfd_lmhead_pack_fp8: W bf16 [V][H] (16-byte aligned) -> W_packed (device,
+ *   256-byte aligned).  Errors as mfd_lmhead_pack.  Enqueued on `stream`.
+ * mfd_fp8_quantize_rows: x bf16 [R][H] (16-byte aligned, H % 8 == 0) ->
+ *   q uint8 [R][H] (E4M3, 8-byte aligned) and scale fp32 [R] = t_r.
+ *   Errors: INVALID_ARG, UNSUPPORTED (device), CUDA.
+ * mfd_lmhead_fp8_workspace_bytes: scratch of mfd_lmhead_topk_fp8 (the
+ *   LM head's partials plus the E4M3 hidden rows and their scales) on the
+ *   current device; 0 outside the limits (H % 128 != 0 included).
+ * mfd_lmhead_topk_fp8: mfd_lmhead_topk_packed with the E4M3 packed weight;
+ *   h stays bf16 (quantized inside the call); ws_bytes >=
+ *   mfd_lmhead_fp8_workspace_bytes(R, H, V, topk).  Outputs and errors as
+ *   mfd_lmhead_topk. */
+size_t mfd_lmhead_packed_fp8_bytes(int V, int H);
+int mfd_lmhead_pack_fp8(const void *W, int V, int H, void *W_packed, size_t packed_bytes, mfd_stream_t stream);
+int mfd_fp8_quantize_rows(const void *x, int R, int H, void *q, float *scale, mfd_stream_t stream);
+size_t mfd_lmhead_fp8_workspace_bytes(int R, int H, int V, int topk);
+int mfd_lmhead_topk_fp8(const void *h, int R, int H, const void *W_packed_fp8, int V, int topk,
+                        float *tk_logp, int32_t *tk_tok, float *lse, int32_t *status, void *ws,
+                        size_t ws_bytes, mfd_stream_t stream);
+
 /* Draft-vocabulary subset head (project page "Multi-Future Drafting", In a
  * serving engine: the serving build drafts only over the target's most
  * frequent tokens, about 64K of them, while the walk still checks against

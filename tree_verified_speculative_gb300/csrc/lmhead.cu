@@ -33,6 +33,17 @@
 // thread each), warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4)..).
 // TMEM holds two 256-column fp32 accumulators so that the epilogue of tile
 // n overlaps the MMAs of tile n+1.
+//
+// FP8 form (project page, In a serving engine, Figure 5 caption: the
+// drafter's linear layers in FP8, quantized online): the weight is packed
+// once as E4M3 with one scale for the whole tensor, the hidden rows are
+// quantized per call with one scale per row (quant_rows_kernel), and the MMA
+// is tcgen05 kind::f8f6f4 with an fp32 accumulator.  A stage then holds a
+// 128-element K slice (the same 128-byte swizzled rows, the same 48 KB), so
+// the weight stream is half the bytes; the epilogue scales the accumulator
+// by the row's factor f_r = t_r * s_W before the softmax and top-k.
+#include <cuda_fp8.h>
+
 #include "lmhead.h"
 #include "mfd_device.cuh"
 
@@ -42,6 +53,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;            // one 128-byte swizzle atom of bf16
+constexpr int BK8 = 128;          // one 128-byte swizzle atom of E4M3
 constexpr int KSUB = 1;           // K atoms per pipeline stage
 constexpr int STAGES = 4;
 constexpr int A_SUB = BM * BK * 2;  // one K atom of the hidden tile
@@ -69,6 +81,8 @@ struct Params {
   int2 *part_cand;  // [R][P][T]   (logit bits, token id), best first
   int32_t *status;
   const uint8_t *w_packed;  // packed weight (see pack_w_kernel), or null
+  const float *row_scale;   // FP8: t_r per hidden row [R]
+  const float *w_amax;      // FP8: the weight's largest magnitude (s_W = w_amax / 448)
 };
 
 // Work item -> (M tile, vocabulary tiles [t0, t1), range); items are
@@ -128,7 +142,7 @@ __device__ __forceinline__ void sort32_best_first(float (&sv)[32], int (&si)[32]
 // PACKED: the weight comes as pack_w_kernel lays it out, so a stage's
 // weight bytes are one contiguous 1-D bulk copy instead of KSUB 2-D boxes of
 // 256 rows x 128 bytes (rows 2H bytes apart), which stream markedly slower.
-template <int T, bool PACKED>
+template <int T, bool PACKED, bool FP8>
 __global__ void __launch_bounds__(THREADS, 1)
     lmhead_topk_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                        const Params p) {
@@ -176,7 +190,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int nk = p.H / BK;
+  static_assert(!FP8 || PACKED, "the FP8 weight is always packed");
+  constexpr int KEL = FP8 ? BK8 : BK;  // K elements per stage
+  const int nk = p.H / KEL;
   // The prologue above may overlap the previous grid; global memory is
   // touched only after it has finished.
   pdl_wait();
@@ -216,7 +232,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (PACKED)
                   bulk_prefetch_l2(p.w_packed + ((size_t)tn * nk + kb) * B_SUB, (uint32_t)B_SUB);
                 else
-                  tma_prefetch_2d(&tmap_w, kb * BK, tn * BN);
+                  tma_prefetch_2d(&tmap_w, kb * KEL, tn * BN);
               }
           }
           for (int kc = 0; kc < nk; kc += KSUB) {
@@ -231,10 +247,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                            &full[stage], pol_w);
             else
               for (int sub = 0; sub < nsub; ++sub)
-                tma_load_2d(sB + stage * B_BYTES + sub * B_SUB, &tmap_w, (kc + sub) * BK, t * BN, &full[stage],
+                tma_load_2d(sB + stage * B_BYTES + sub * B_SUB, &tmap_w, (kc + sub) * KEL, t * BN, &full[stage],
                             pol_w);
             for (int sub = 0; sub < nsub; ++sub)
-              tma_load_2d(sA + stage * A_BYTES + sub * A_SUB, &tmap_h, (kc + sub) * BK, mt * BM, &full[stage], pol_h);
+              tma_load_2d(sA + stage * A_BYTES + sub * A_SUB, &tmap_h, (kc + sub) * KEL, mt * BM, &full[stage], pol_h);
             issued |= 1u << stage;
             issued_par = phase ? (issued_par | (1u << stage)) : (issued_par & ~(1u << stage));
             if (++stage == STAGES) {
@@ -255,7 +271,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      constexpr uint32_t idesc = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -279,9 +295,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int sub = 0; sub < nsub; ++sub) {
               const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * A_BYTES + sub * A_SUB));
               const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * B_BYTES + sub * B_SUB));
+              // four MMAs of 32 bytes of K each (16 bf16 or 32 E4M3 elements):
+              // the descriptor's start address advances by 32 bytes (>> 4 = 2)
 #pragma unroll
-              for (int kk = 0; kk < BK / 16; ++kk)
-                tc_mma_f16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kc | sub | kk) != 0);
+              for (int kk = 0; kk < 4; ++kk) {
+                if (FP8)
+                  tc_mma_f8(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kc | sub | kk) != 0);
+                else
+                  tc_mma_f16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kc | sub | kk) != 0);
+              }
             }
             tc_commit(&empty[stage]);
             if (++stage == STAGES) {
@@ -312,9 +334,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
+    const float s_w = FP8 ? __fdiv_rn(__ldg(p.w_amax), 448.0f) : 1.f;
     for (int item = cta0; item < p.n_items && ok; item += ncta) {
       int mt, t0, t1, range;
       item_range(p, item, mt, t0, t1, range);
+      // FP8: z = f_r * acc with f_r = t_r * s_W, one fp32 product
+      const int my_row = mt * BM + row_in_tile;
+      const float f_r = FP8 ? (my_row < p.R ? __fmul_rn(__ldg(p.row_scale + my_row), s_w) : 0.f) : 1.f;
       float m = -INFINITY, S = 0.f;
       float tv[T];
       int ti[T];
@@ -334,6 +360,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < BN / 32; ++c) {
           float x[32];
           tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), x);
+          if (FP8) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = __fmul_rn(x[j], f_r);
+          }
           const int v0 = t * BN + c * 32;
           if (v0 + 32 > p.V) {
 #pragma unroll
@@ -443,7 +473,100 @@ __global__ void pack_w_kernel(const uint4 *__restrict__ W, int V, int H, uint4 *
   }
 }
 
-template <int T, bool PACKED>
+// FP8 weight, pass 1: the largest magnitude of W (bf16 [V][H], n16 chunks of
+// 8 values) into *amax (zeroed before; non-negative floats order as their
+// bit patterns, so an integer max suffices).
+__global__ void amax_bf16_kernel(const uint4 *__restrict__ W, size_t n16, unsigned int *amax_bits) {
+  float m = 0.f;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n16; q += stride) {
+    const uint4 v = __ldg(W + q);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      m = fmaxf(m, fabsf(__uint_as_float(w[j] << 16)));
+      m = fmaxf(m, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+    }
+  }
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));
+}
+
+// E4M3 of x, rounding to nearest even and saturating at +-448.
+__device__ __forceinline__ uint32_t to_e4m3(float x) {
+  return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+// FP8 weight, pass 2: for vocabulary tile t (256 rows) and K slice a (128
+// elements) a 32 KB block at ((t * H/128) + a) * 32 KB, row r at r * 128
+// bytes, its 16-byte chunk j (elements 16 j .. 16 j + 15 of the slice) at
+// chunk position j ^ (r % 8): the shared-memory image of the MMA's 128-byte
+// swizzle.  Each value is e4m3(w * (448 / amax)); rows past V are zero.
+__global__ void pack_w_fp8_kernel(const uint4 *__restrict__ W, int V, int H, const float *amax, uint4 *__restrict__ Wp,
+                                  size_t n16) {
+  const int nk = H / BK8;
+  const float a = __ldg(amax);
+  const float inv = a > 0.f ? __fdiv_rn(448.0f, a) : 0.f;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n16; q += stride) {
+    const size_t blk = q / (B_SUB / 16);
+    const int c = (int)(q - blk * (B_SUB / 16));
+    const int t = (int)(blk / nk), s = (int)(blk - (size_t)t * nk);
+    const int r = c >> 3, j = (c & 7) ^ (r & 7);
+    const int row = t * BN + r;
+    uint32_t o[4] = {0u, 0u, 0u, 0u};
+    if (row < V) {
+      const uint4 *src = W + ((size_t)row * H + (size_t)s * BK8 + (size_t)j * 16) / 8;
+      const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const uint32_t bits = (e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16);
+        o[e >> 2] |= to_e4m3(__fmul_rn(__uint_as_float(bits), inv)) << (8 * (e & 3));
+      }
+    }
+    Wp[q] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Online FP8 of the hidden rows: one warp per row of x (bf16 [R][H]):
+// amax = max |x|, q = e4m3(x * (448 / amax)), scale[r] = amax / 448 (0 and
+// zero bytes for an all-zero row).
+__global__ void __launch_bounds__(128) quant_rows_kernel(const uint16_t *__restrict__ x, int R, int H,
+                                                        uint8_t *__restrict__ q, float *__restrict__ scale) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 4 + warp;
+  if (r >= R) return;
+  const uint16_t *xr = x + (size_t)r * H;
+  float m = 0.f;
+  for (int k = lane * 8; k < H; k += 256) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + k));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      m = fmaxf(m, fabsf(__uint_as_float(w[j] << 16)));
+      m = fmaxf(m, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+    }
+  }
+  m = warp_max(m);
+  const float inv = m > 0.f ? __fdiv_rn(448.0f, m) : 0.f;
+  for (int k = lane * 8; k < H; k += 256) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + k));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t bits = (e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16);
+      o[e >> 2] |= to_e4m3(__fmul_rn(__uint_as_float(bits), inv)) << (8 * (e & 3));
+    }
+    *reinterpret_cast<uint2 *>(q + (size_t)r * H + k) = make_uint2(o[0], o[1]);
+  }
+  if (lane == 0) scale[r] = __fdiv_rn(m, 448.0f);
+}
+
+template <int T, bool PACKED, bool FP8>
 cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
   static_assert(smem_bytes() <= 232448, "shared memory budget");
   Params p;
@@ -458,7 +581,9 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
   p.part_cand = reinterpret_cast<int2 *>(L.part_cand);
   p.status = L.status;
   p.w_packed = static_cast<const uint8_t *>(L.w_packed);
-  cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<T, PACKED>,
+  p.row_scale = L.row_scale;
+  p.w_amax = L.w_amax;
+  cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<T, PACKED, FP8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
   if (e != cudaSuccess) return e;
   const int grid = p.n_items < L.n_sm ? p.n_items : L.n_sm;
@@ -472,7 +597,7 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, lmhead_topk_kernel<T, PACKED>, *L.tmap_h, PACKED ? *L.tmap_h : *L.tmap_w, p);
+  e = cudaLaunchKernelEx(&cfg, lmhead_topk_kernel<T, PACKED, FP8>, *L.tmap_h, PACKED ? *L.tmap_h : *L.tmap_w, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -485,15 +610,55 @@ int lmhead_k_chunk() { return BK; }
 
 cudaError_t launch_lmhead_partials(const LmheadLaunch &L, cudaStream_t stream) {
   const bool pk = L.w_packed != nullptr;
+  if (L.fp8) {
+    if (!pk || !L.row_scale || !L.w_amax) return cudaErrorInvalidValue;
+    switch (L.T) {
+      case 8: return launch_t<8, true, true>(L, stream);
+      case 16: return launch_t<16, true, true>(L, stream);
+      case 32: return launch_t<32, true, true>(L, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (L.T) {
-    case 8: return pk ? launch_t<8, true>(L, stream) : launch_t<8, false>(L, stream);
-    case 16: return pk ? launch_t<16, true>(L, stream) : launch_t<16, false>(L, stream);
-    case 32: return pk ? launch_t<32, true>(L, stream) : launch_t<32, false>(L, stream);
+    case 8: return pk ? launch_t<8, true, false>(L, stream) : launch_t<8, false, false>(L, stream);
+    case 16: return pk ? launch_t<16, true, false>(L, stream) : launch_t<16, false, false>(L, stream);
+    case 32: return pk ? launch_t<32, true, false>(L, stream) : launch_t<32, false, false>(L, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 size_t lmhead_packed_bytes(int V, int H) { return (size_t)((V + BN - 1) / BN) * BN * (size_t)H * 2; }
+
+size_t lmhead_packed_fp8_bytes(int V, int H) { return (size_t)((V + BN - 1) / BN) * BN * (size_t)H + 256; }
+
+cudaError_t launch_pack_w_fp8(const void *W, int V, int H, void *Wp, cudaStream_t stream) {
+  const size_t body = lmhead_packed_fp8_bytes(V, H) - 256;
+  unsigned int *amax = reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(Wp) + body);
+  cudaError_t e = cudaMemsetAsync(amax, 0, 256, stream);
+  if (e != cudaSuccess) return e;
+  amax_bf16_kernel<<<4 * 152, 256, 0, stream>>>(static_cast<const uint4 *>(W), (size_t)V * H / 8, amax);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  pack_w_fp8_kernel<<<4 * 152, 256, 0, stream>>>(static_cast<const uint4 *>(W), V, H,
+                                                 reinterpret_cast<const float *>(amax), static_cast<uint4 *>(Wp),
+                                                 body / 16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows(const void *x, int R, int H, void *q, float *scale, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((R + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, quant_rows_kernel, static_cast<const uint16_t *>(x), R, H,
+                                     static_cast<uint8_t *>(q), scale);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pack_w(const void *W, int V, int H, void *Wp, cudaStream_t stream) {
   const size_t n16 = lmhead_packed_bytes(V, H) / 16;

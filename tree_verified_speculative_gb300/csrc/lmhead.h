@@ -17,6 +17,9 @@ struct LmheadLaunch {
   void *part_cand;  // int2 [R][P][T]
   int32_t *status;
   const void *w_packed;  // packed weight (lmhead_packed_bytes), or null: use tmap_w
+  bool fp8 = false;                 // E4M3 packed weight (lmhead_packed_fp8_bytes), tmap_h over E4M3 rows
+  const float *row_scale = nullptr;  // FP8: t_r per hidden row
+  const float *w_amax = nullptr;     // FP8: the weight's largest magnitude (in the packed buffer's trailer)
 };
 
 int lmhead_tile_rows();  // vocabulary rows per tile (256)
@@ -25,6 +28,12 @@ int lmhead_k_chunk();    // K elements per pipeline stage (64)
 cudaError_t launch_lmhead_partials(const LmheadLaunch &L, cudaStream_t stream);
 size_t lmhead_packed_bytes(int V, int H);  // bytes of the packed weight
 cudaError_t launch_pack_w(const void *W, int V, int H, void *Wp, cudaStream_t stream);
+// E4M3 packed weight: 32 KB blocks of 256 rows x 128 K elements, then a
+// 256-byte trailer whose first word is the weight's largest magnitude
+size_t lmhead_packed_fp8_bytes(int V, int H);
+cudaError_t launch_pack_w_fp8(const void *W, int V, int H, void *Wp, cudaStream_t stream);
+// online E4M3 of bf16 rows x [R][H] (H % 8 == 0): q [R][H] bytes, scale [R]
+cudaError_t launch_quant_rows(const void *x, int R, int H, void *q, float *scale, cudaStream_t stream);
 
 // topk.cu
 struct MergeLaunch {

@@ -65,17 +65,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-using MapKey = std::tuple<int, const void *, int, int, int>;  // device, ptr, rows, cols, box rows
+using MapKey = std::tuple<int, const void *, int, int, int, int>;  // device, ptr, rows, cols, box rows, bytes/elem
 std::map<MapKey, CUtensorMap> g_maps;
 
-// bf16 [rows][cols] row-major, box = 64 columns x box_rows rows, 128B swizzle,
-// out-of-range rows read as zero.  The descriptor is copied into *out while
-// the lock is held: another thread may clear the cache right after.
-int tensor_map(const void *ptr, int rows, int cols, int box_rows, CUtensorMap *out) {
+// bf16 (elem = 2) or 8-bit (elem = 1) [rows][cols] row-major, box = 128
+// bytes of columns x box_rows rows, 128B swizzle, out-of-range rows read as
+// zero.  The descriptor is copied into *out while the lock is held: another
+// thread may clear the cache right after.
+int tensor_map(const void *ptr, int rows, int cols, int box_rows, CUtensorMap *out, int elem = 2) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MFD_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
-  const MapKey key{dev, ptr, rows, cols, box_rows};
+  const MapKey key{dev, ptr, rows, cols, box_rows, elem};
   auto it = g_maps.find(key);
   if (it == g_maps.end()) {
     EncodeTiledFn fn = encode_fn();
@@ -83,10 +84,11 @@ int tensor_map(const void *ptr, int rows, int cols, int box_rows, CUtensorMap *o
     CUtensorMap m;
     std::memset(&m, 0, sizeof m);
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * (cuuint64_t)elem};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1u, 1u};
-    const CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+    const CUresult r = fn(&m, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                          const_cast<void *>(ptr), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return MFD_ERR_CUDA;
@@ -135,6 +137,21 @@ TopkLayout lmhead_layout(int R, int V, int topk, int n_sm) {
   y.cand_bytes = align256((size_t)R * y.P * y.T * 8);
   y.total = y.ms_bytes + y.cand_bytes;
   return y;
+}
+
+// FP8 LM head scratch: the partials of lmhead_layout, then the E4M3 hidden
+// rows [R][H] and their scales [R].
+struct Fp8Layout {
+  TopkLayout y;
+  size_t hq_off, sc_off, total;
+};
+Fp8Layout fp8_layout(int R, int H, int V, int topk, int n_sm) {
+  Fp8Layout f;
+  f.y = lmhead_layout(R, V, topk, n_sm);
+  f.hq_off = f.y.total;
+  f.sc_off = f.hq_off + align256((size_t)R * H);
+  f.total = f.sc_off + align256((size_t)R * 4);
+  return f;
 }
 
 TopkLayout logits_layout(int R, int V, int topk) {
@@ -241,22 +258,32 @@ namespace {
 // vocabulary ids vocab_ids[0..V), increasing, below V_full)
 int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int V, int topk, float *tk_logp,
                 int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes, mfd_stream_t stream,
-                const int32_t *vocab_ids = nullptr, int V_full = 0) {
+                const int32_t *vocab_ids = nullptr, int V_full = 0, bool fp8 = false) {
   if (!h || (!W && !Wp) || !tk_logp || !tk_tok || !status || R < 1 || H < 1 || V < 1 || topk < 1)
     return MFD_ERR_INVALID_ARG;
   if (!aligned(h, 16) || (W && !aligned(W, 16)) || (Wp && !aligned(Wp, 256))) return MFD_ERR_INVALID_ARG;
-  if (H % mfd::lmhead_k_chunk() != 0 || topk > 32 || V < 16 || topk > V || V >= (1 << 30))
+  if (H % ((fp8 ? 2 : 1) * mfd::lmhead_k_chunk()) != 0 || topk > 32 || V < 16 || topk > V || V >= (1 << 30))
     return MFD_ERR_UNSUPPORTED;
   DeviceInfo d;
   int rc = current_device_info(&d);
   if (rc != MFD_OK) return rc;
   if (!is_sm103(d)) return MFD_ERR_UNSUPPORTED;
   const TopkLayout y = lmhead_layout(R, V, topk, d.n_sm);
-  if (!ws || ws_bytes < y.total || !aligned(ws, 256)) return MFD_ERR_WORKSPACE;
-  CUtensorMap mh, mw;
-  if ((rc = tensor_map(h, R, H, mfd::lmhead_m_rows(), &mh)) != MFD_OK) return rc;
-  if (W && (rc = tensor_map(W, V, H, mfd::lmhead_tile_rows(), &mw)) != MFD_OK) return rc;
+  const Fp8Layout f8 = fp8_layout(R, H, V, topk, d.n_sm);
+  if (!ws || ws_bytes < (fp8 ? f8.total : y.total) || !aligned(ws, 256)) return MFD_ERR_WORKSPACE;
   char *base = static_cast<char *>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  CUtensorMap mh, mw;
+  if (fp8) {
+    // the hidden rows in E4M3 with their scales, then the E4M3 head over them
+    if ((rc = cuda_status(mfd::launch_quant_rows(h, R, H, base + f8.hq_off, reinterpret_cast<float *>(base + f8.sc_off),
+                                                 s))) != MFD_OK)
+      return rc;
+    if ((rc = tensor_map(base + f8.hq_off, R, H, mfd::lmhead_m_rows(), &mh, 1)) != MFD_OK) return rc;
+  } else if ((rc = tensor_map(h, R, H, mfd::lmhead_m_rows(), &mh)) != MFD_OK) {
+    return rc;
+  }
+  if (W && (rc = tensor_map(W, V, H, mfd::lmhead_tile_rows(), &mw)) != MFD_OK) return rc;
   mfd::LmheadLaunch L;
   L.tmap_h = &mh;
   L.tmap_w = W ? &mw : nullptr;
@@ -270,7 +297,11 @@ int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int 
   L.part_ms = base;
   L.part_cand = base + y.ms_bytes;
   L.status = status;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fp8) {
+    L.fp8 = true;
+    L.row_scale = reinterpret_cast<const float *>(base + f8.sc_off);
+    L.w_amax = reinterpret_cast<const float *>(static_cast<const char *>(Wp) + mfd::lmhead_packed_fp8_bytes(V, H) - 256);
+  }
   if ((rc = cuda_status(mfd::launch_lmhead_partials(L, s))) != MFD_OK) return rc;
   mfd::MergeLaunch M;
   M.part_ms = L.part_ms;
@@ -322,6 +353,50 @@ int mfd_lmhead_topk_packed(const void *h, int R, int H, const void *W_packed, in
                            mfd_stream_t stream) {
   if (!W_packed) return MFD_ERR_INVALID_ARG;
   return lmhead_call(h, R, H, nullptr, W_packed, V, topk, tk_logp, tk_tok, lse, status, ws, ws_bytes, stream);
+}
+
+size_t mfd_lmhead_packed_fp8_bytes(int V, int H) {
+  if (V < 16 || V >= (1 << 30) || H < 1 || H % (2 * mfd::lmhead_k_chunk()) != 0) return 0;
+  return mfd::lmhead_packed_fp8_bytes(V, H);
+}
+
+int mfd_lmhead_pack_fp8(const void *W, int V, int H, void *W_packed, size_t packed_bytes, mfd_stream_t stream) {
+  if (!W || !W_packed || V < 1 || H < 1) return MFD_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(W_packed, 256)) return MFD_ERR_INVALID_ARG;
+  const size_t need = mfd_lmhead_packed_fp8_bytes(V, H);
+  if (need == 0) return MFD_ERR_UNSUPPORTED;
+  if (packed_bytes < need) return MFD_ERR_WORKSPACE;
+  DeviceInfo d;
+  int rc = current_device_info(&d);
+  if (rc != MFD_OK) return rc;
+  if (!is_sm103(d)) return MFD_ERR_UNSUPPORTED;
+  return cuda_status(mfd::launch_pack_w_fp8(W, V, H, W_packed, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mfd_fp8_quantize_rows(const void *x, int R, int H, void *q, float *scale, mfd_stream_t stream) {
+  if (!x || !q || !scale || R < 1 || H < 8 || H % 8 != 0) return MFD_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(q, 8) || !aligned(scale, 4)) return MFD_ERR_INVALID_ARG;
+  DeviceInfo d;
+  int rc = current_device_info(&d);
+  if (rc != MFD_OK) return rc;
+  if (!is_sm103(d)) return MFD_ERR_UNSUPPORTED;
+  return cuda_status(mfd::launch_quant_rows(x, R, H, q, scale, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t mfd_lmhead_fp8_workspace_bytes(int R, int H, int V, int topk) {
+  if (R < 1 || H < 1 || H % (2 * mfd::lmhead_k_chunk()) != 0 || V < 16 || topk < 1 || topk > 32 || topk > V)
+    return 0;
+  DeviceInfo d;
+  if (current_device_info(&d) != MFD_OK) return 0;
+  return fp8_layout(R, H, V, topk, d.n_sm).total;
+}
+
+int mfd_lmhead_topk_fp8(const void *h, int R, int H, const void *W_packed_fp8, int V, int topk, float *tk_logp,
+                        int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes,
+                        mfd_stream_t stream) {
+  if (!W_packed_fp8) return MFD_ERR_INVALID_ARG;
+  return lmhead_call(h, R, H, nullptr, W_packed_fp8, V, topk, tk_logp, tk_tok, lse, status, ws, ws_bytes, stream,
+                     nullptr, 0, true);
 }
 
 int mfd_lmhead_topk_subset(const void *h, int R, int H, const void *W_packed, int V_sub, const int32_t *vocab_ids,

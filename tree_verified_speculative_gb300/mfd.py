@@ -35,7 +35,9 @@ MFD_OP_VERIFY = 3
 EXPORTS = ("mfd_status_string", "mfd_workspace_size", "mfd_lmhead_topk", "mfd_lmhead_packed_bytes",
            "mfd_lmhead_pack", "mfd_lmhead_topk_packed", "mfd_lmhead_topk_subset", "mfd_logits_topk",
            "mfd_logits_topk_noalloc",
-           "mfd_build_tree", "mfd_verify", "mfd_verify_withheld_test", "mfd_mfdd_modes")
+           "mfd_build_tree", "mfd_verify", "mfd_verify_withheld_test", "mfd_mfdd_modes",
+           "mfd_lmhead_packed_fp8_bytes", "mfd_lmhead_pack_fp8", "mfd_fp8_quantize_rows",
+           "mfd_lmhead_fp8_workspace_bytes", "mfd_lmhead_topk_fp8")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _lock = threading.Lock()
@@ -102,6 +104,16 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.mfd_verify_withheld_test.restype = I
         lib.mfd_mfdd_modes.argtypes = [I, I]
         lib.mfd_mfdd_modes.restype = I
+        lib.mfd_lmhead_packed_fp8_bytes.argtypes = [I, I]
+        lib.mfd_lmhead_packed_fp8_bytes.restype = SZ
+        lib.mfd_lmhead_pack_fp8.argtypes = [P, I, I, P, SZ, P]
+        lib.mfd_lmhead_pack_fp8.restype = I
+        lib.mfd_fp8_quantize_rows.argtypes = [P, I, I, P, P, P]
+        lib.mfd_fp8_quantize_rows.restype = I
+        lib.mfd_lmhead_fp8_workspace_bytes.argtypes = [I, I, I, I]
+        lib.mfd_lmhead_fp8_workspace_bytes.restype = SZ
+        lib.mfd_lmhead_topk_fp8.argtypes = [P, I, I, P, I, I, P, P, P, P, P, SZ, P]
+        lib.mfd_lmhead_topk_fp8.restype = I
         _libs[p] = lib
         if path is None:
             _lib = lib
@@ -189,6 +201,49 @@ def mfd_lmhead_topk_packed(h, W_packed, V, topk, tk_logp, tk_tok, lse, status, w
     _check(rc, "mfd_lmhead_topk_packed")
 
 
+def mfd_lmhead_packed_fp8_bytes(V: int, H: int) -> int:
+    return int(load().mfd_lmhead_packed_fp8_bytes(V, H))
+
+
+def mfd_lmhead_pack_fp8(W, W_packed, stream=None) -> None:
+    V, H = W.shape
+    assert W.dtype == torch.bfloat16
+    rc = load().mfd_lmhead_pack_fp8(_p(W), V, H, _p(W_packed), W_packed.numel() * W_packed.element_size(),
+                                    _s(stream))
+    _check(rc, "mfd_lmhead_pack_fp8")
+
+
+def pack_lm_head_fp8(W, stream=None):
+    """The E4M3 packed copy of W with its scale trailer (a new device buffer,
+    allocated here, once)."""
+    V, H = W.shape
+    n = mfd_lmhead_packed_fp8_bytes(V, H)
+    if n == 0:
+        raise MfdError(MFD_ERR_UNSUPPORTED, "mfd_lmhead_packed_fp8_bytes")
+    Wp = torch.empty((n,), dtype=torch.uint8, device=W.device)
+    mfd_lmhead_pack_fp8(W, Wp, stream)
+    return Wp
+
+
+def mfd_fp8_quantize_rows(x, q, scale, stream=None) -> None:
+    R, H = x.shape
+    assert x.dtype == torch.bfloat16 and q.dtype == torch.uint8 and scale.dtype == torch.float32
+    rc = load().mfd_fp8_quantize_rows(_p(x), R, H, _p(q), _p(scale), _s(stream))
+    _check(rc, "mfd_fp8_quantize_rows")
+
+
+def mfd_lmhead_fp8_workspace_bytes(R: int, H: int, V: int, topk: int) -> int:
+    return int(load().mfd_lmhead_fp8_workspace_bytes(R, H, V, topk))
+
+
+def mfd_lmhead_topk_fp8(h, W_packed_fp8, V, topk, tk_logp, tk_tok, lse, status, ws, stream=None) -> None:
+    R, H = h.shape
+    assert h.dtype == torch.bfloat16
+    rc = load().mfd_lmhead_topk_fp8(_p(h), R, H, _p(W_packed_fp8), V, topk, _p(tk_logp), _p(tk_tok), _p(lse),
+                                    _p(status), _p(ws), ws.numel() * ws.element_size(), _s(stream))
+    _check(rc, "mfd_lmhead_topk_fp8")
+
+
 def mfd_lmhead_topk_subset(h, W_packed, vocab_ids, V_full, topk, tk_logp, tk_tok, lse, status, ws,
                            stream=None) -> None:
     """The LM head over a draft-vocabulary subset: W_packed holds the packed
@@ -253,9 +308,11 @@ class Round:
     """Device buffers for one drafting round of n_req requests, reused from
     call to call (allocation happens here, once, never inside the calls)."""
 
-    def __init__(self, n_req: int, K: int, L: int, topk: int, B: int, V: int, device="cuda", V_draft: int | None = None):
+    def __init__(self, n_req: int, K: int, L: int, topk: int, B: int, V: int, device="cuda", V_draft: int | None = None,
+                 H: int | None = None):
         """V: the target vocabulary (verification); V_draft: the draft
-        vocabulary of a subset head (lmhead_topk_subset), if any."""
+        vocabulary of a subset head (lmhead_topk_subset), if any; H: the
+        hidden width, needed only to size the FP8 head's scratch."""
         self.n_req, self.K, self.L, self.topk, self.B, self.V = n_req, K, L, topk, B, V
         R = n_req * K * L
         N = B + 1
@@ -284,7 +341,8 @@ class Round:
                  mfd_workspace_size(MFD_OP_LMHEAD_TOPK, n_req, K, L, topk, B, R, V_draft or V),
                  mfd_workspace_size(MFD_OP_LOGITS_TOPK, n_req, K, L, topk, B, R, V),
                  mfd_workspace_size(MFD_OP_BUILD_TREE, n_req, K, L, topk, B, R, V),
-                 mfd_workspace_size(MFD_OP_VERIFY, n_req, K, L, topk, B, R, V))
+                 mfd_workspace_size(MFD_OP_VERIFY, n_req, K, L, topk, B, R, V),
+                 mfd_lmhead_fp8_workspace_bytes(R, H, V, topk) if H else 0)
         self.ws = torch.empty((ws + 255) // 256 * 256, dtype=torch.uint8, device=dev)
 
     def lmhead_topk(self, h, W, stream=None):
@@ -293,6 +351,12 @@ class Round:
     def lmhead_topk_packed(self, h, W_packed, stream=None):
         mfd_lmhead_topk_packed(h, W_packed, self.V, self.topk, self.tk_logp, self.tk_tok, self.lse, self.status,
                                self.ws, stream)
+
+    def lmhead_topk_fp8(self, h, W_packed_fp8, stream=None):
+        """The FP8 drafter head (E4M3 packed weight); the Round must have
+        been made with H."""
+        mfd_lmhead_topk_fp8(h, W_packed_fp8, self.V, self.topk, self.tk_logp, self.tk_tok, self.lse, self.status,
+                            self.ws, stream)
 
     def lmhead_topk_subset(self, h, W_packed, vocab_ids, stream=None):
         """Draft over the subset whose packed rows are W_packed; tk_tok gets
