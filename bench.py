@@ -56,6 +56,11 @@ WORKLOADS = {
     # the single-mode path with batch-size sweeps (--n-req)
     "k1_l15_h2560_v151936_b64_greedy_batch": dict(K=1, L=15, H=2560, V=151936, n_shared=None, topk=16, B=64,
                                                   T=None, n_req=8, temps=[0.0]),
+    # MFD-D (project page, In a serving engine): all 8 modes below three
+    # requests in flight, the single-mode path from three on (the library's
+    # mfd_mfdd_modes); sweep with --n-req
+    "mfdd_l15_h2560_v151936_b64_greedy_batch": dict(K="mfdd", L=15, H=2560, V=151936, n_shared=None, topk=16, B=64,
+                                                    T=None, n_req=1, temps=[0.0]),
     # its small counterpart for host-side runs
     "r4_tiny_mixed": dict(K=2, L=4, H=64, V=512, n_shared=None, topk=8, B=16, T=None, n_req=4,
                           temps=[0.0, 0.0, 1.0, 1.0]),
@@ -84,15 +89,27 @@ def parse():
     return ap.parse_args()
 
 
+def batched(cfg) -> bool:
+    """A workload of independent requests per round (one LM head over all
+    their rows, one tree and one walk per request)."""
+    return cfg.get("temps") is not None
+
+
 def workload(args):
     """The workload's settings, with --n-req applied to a batched one (the
-    per-request temperatures cycle through the workload's list)."""
+    per-request temperatures cycle through the workload's list) and MFD-D's
+    mode count resolved by the library's switch rule."""
     cfg = dict(WORKLOADS[args.workload])
     n = getattr(args, "n_req", 0) or 0
-    if n > 0 and cfg.get("n_req", 1) > 1:
+    if n > 0 and batched(cfg):
         temps = cfg["temps"]
         cfg["n_req"] = n
         cfg["temps"] = [temps[i % len(temps)] for i in range(n)]
+    if cfg["K"] == "mfdd":
+        from tree_verified_speculative_gb300 import mfd
+
+        cfg["K"] = mfd.mfd_mfdd_modes(cfg["n_req"], 8)
+        cfg["mfdd"] = True
     return cfg
 
 
@@ -574,9 +591,11 @@ def run_gpu_batched(args, ws, rank, local):
     value = whole_job_rate(steps, ws, total_ms)
     lm_us = sum(lm_d) / len(diag) * 1e3
     flops = 2.0 * R * V * H
-    if R <= 128:  # one M tile: the weight stream bounds the LM head
-        algo = V * H * 2 + R * H * 2
-        peak, peak_kind = peaks("hbm")
+    algo = V * H * 2 + R * H * 2
+    hbm_peak, hbm_kind = peaks("hbm")
+    bf16_peak, _ = peaks("bf16")
+    if flops / algo < bf16_peak * 1e12 / (hbm_peak * 1e9):  # below the ridge: the weight stream bounds it
+        peak, peak_kind = hbm_peak, hbm_kind
         roof = {"bound": "hbm", "achieved": round(algo / (lm_us * 1e-6) / 1e9, 1), "unit": "GB/s",
                 "algorithmic_bytes_per_launch": algo}
     else:
@@ -595,6 +614,8 @@ def run_gpu_batched(args, ws, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "K": K, "L": L, "H": H, "V": V, "topk": topk, "B": B,
                    "n_req": n_req, "rows": R,
+                   **({"modes": "mfd_mfdd_modes(n_req, 8): 8 below three requests, 1 from three"}
+                      if cfg.get("mfdd") else {}),
                    "temperatures": f"{int(greedy.sum())} greedy, {int((~greedy).sum())} sampled (T={sorted(set(cfg['temps']))})",
                    "parallelism": f"replicas{ws}" if ws > 1 else "single",
                    "lm_head_weight": "packed once before timing (mfd_lmhead_pack), streamed by mfd_lmhead_topk_packed",
@@ -706,7 +727,12 @@ def cpu_baseline(cfg, head, r, rd, noise, site):
 
 # ---------------------------------------------------------------------------
 def run_reference(args, ws, rank):
-    """The CPU oracle on the same workload, a bounded sample per step."""
+    """The CPU oracle, as it stands, on the same workload: every step is one
+    full round of one request -- the LM head, log-softmax and top-k of all K*L
+    rows over the whole (draft) vocabulary, the tree from those tables, and
+    the verification walk over target rows planted along the round's future.
+    On a batched workload a round is n_req such requests, which the oracle
+    handles one after another, so a step's time is one request's times n_req."""
     import torch
 
     import oracle
@@ -716,65 +742,52 @@ def run_reference(args, ws, rank):
     K, L, H, V, topk, B = cfg["K"], cfg["L"], cfg["H"], cfg["V"], cfg["topk"], cfg["B"]
     n_req = cfg.get("n_req", 1)
     temps = cfg.get("temps") or [cfg["T"]]
-    n_shared = cfg["n_shared"] if cfg["n_shared"] is not None else min(11, L)
-    R = K * L
     oracle.build()
     bits = lambda x: x.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
     W = synth.lm_head(V, H, seed=W_SEED)
     ids = draft_vocab(cfg)
-    if ids is not None:  # the drafter's head covers the draft vocabulary only
-        W = W[torch.from_numpy(ids.astype(np.int64))].contiguous()
-    V_lm = W.shape[0]
-    wb = bits(W)
-    n_steps = args.warmup + args.steps
-    budget_s = 150.0 / max(1, n_steps)  # whole run within a few minutes
-    # the vocabulary slice the LM-head sample covers, sized from one calibration
-    r0 = synth.round_inputs(W, K, L, n_shared, seed=7)
-    t0 = time.perf_counter()
-    oracle.lmhead_logits(bits(r0.h), wb, 0, 4096)
-    per_vocab = (time.perf_counter() - t0) / 4096
-    n_v = int(max(256, min(V_lm, 0.5 * budget_s / max(per_vocab, 1e-9))))
-    z_row = np.random.default_rng(3).standard_normal((1, V_lm)).astype(np.float32)
+    W_lm = W if ids is None else W[torch.from_numpy(ids.astype(np.int64))].contiguous()
+    wb = bits(W_lm)
+    fp8 = bool(cfg.get("fp8"))
     noise = synth.target_noise(B + 1, V, np.random.default_rng(11))
+    rng = np.random.default_rng(13)
     times = []
-    for s in range(n_steps):
-        r = synth.round_inputs(W, K, L, n_shared, seed=2_000_000 + s)
+    for s in range(args.warmup + args.steps):
+        n_shared = cfg["n_shared"] if cfg["n_shared"] is not None else int(rng.integers(min(8, L), min(14, L) + 1))
+        r = synth.round_inputs(W, K, L, n_shared, seed=2_000_000 + s, vocab=ids)
         T = temps[s % len(temps)]
-        hb = bits(r.h)
-        v0 = (s * 9973) % max(1, V_lm - n_v)
         t0 = time.perf_counter()
-        oracle.lmhead_logits(hb, wb, v0, v0 + n_v)
-        t_lm = (time.perf_counter() - t0) * V_lm / n_v
+        if fp8:
+            lp, tk, _, _, _ = oracle.lmhead_fp8_topk(bits(r.h), wb, topk)
+        else:
+            lp, tk, _ = oracle.lmhead_topk(bits(r.h), wb, topk)
+        t_lm = time.perf_counter() - t0
+        if ids is not None:
+            tk = ids[tk]  # draft-vocabulary rows to vocabulary ids
         t0 = time.perf_counter()
-        oracle.logits_topk(z_row, topk)
-        t_sort = (time.perf_counter() - t0) * R
-        lp = np.sort(-np.abs(np.random.default_rng(s).normal(8, 1, size=(K, L, topk))).astype(np.float32),
-                     axis=2)[..., ::-1].copy()
-        tk = np.random.default_rng(s + 1).integers(0, V, size=(K, L, topk)).astype(np.int32)
-        for k in range(K):
-            for i in range(L):
-                tk[k, i] = np.random.default_rng(s * 1000 + k * 16 + i).choice(V, size=topk, replace=False)
-        t0 = time.perf_counter()
-        tr = oracle.build_tree(lp, tk, B)
+        tr = oracle.build_tree(lp.reshape(K, L, topk), tk.reshape(K, L, topk), B)
         t_tree = time.perf_counter() - t0
+        rows, cols = synth.plant_sites(tr["parent"], tr["token"], tr["depth"], int(tr["n_nodes"]),
+                                       r.fut[r.target_mode])
+        tl = synth.plant(noise, rows, cols)
         t0 = time.perf_counter()
-        oracle.verify(noise, tr["parent"], tr["token"], int(tr["n_nodes"]), L, T, r.seed)
+        oracle.verify(tl, tr["parent"], tr["token"], int(tr["n_nodes"]), L, T, r.seed)
         t_ver = time.perf_counter() - t0
         if s >= args.warmup:
-            # a round of n_req requests is n_req times one request's work
-            times.append((t_lm + t_sort + t_tree + t_ver) * n_req)
+            times.append((t_lm + t_tree + t_ver) * n_req)
     per_round = sum(times) / len(times)
     value = 1.0 / per_round
     cores = oracle.default_threads()
+    sample = (f"per step one full round of one request: {'FP8 ' if fp8 else ''}LM head + log-softmax + top-k of all "
+              f"{K * L} rows over {W_lm.shape[0]} vocabulary rows, tree, verification walk"
+              + (f"; a round of {n_req} requests is {n_req} such rounds" if n_req > 1 else ""))
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "rounds/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_round * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "K": K, "L": L, "H": H, "V": V, "topk": topk, "B": B,
                        "temperature": temps[0] if n_req == 1 else "per request", "n_req": n_req},
             "cpu_baseline": {"value": round(value, 4), "unit": "rounds/s", "cores": cores, "kind": "oracle",
-                             "sample": f"per step: LM head on {n_v} of {V_lm} draft-head rows for all {R} rows "
-                                       f"(scaled), one full-row log-softmax+top-k (scaled x{R}), full tree and "
-                                       "verification walk" + (f"; one request, scaled x{n_req}" if n_req > 1 else "")},
+                             "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -789,7 +802,7 @@ def profile_rounds(args, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     n_req = cfg.get("n_req", 1)
-    if n_req > 1:
+    if batched(cfg):
         W, rr = batched_inputs(cfg, 1, 0)
         rr = rr[0]
         h = torch.cat([r.h for r in rr], 0).to(dev)
@@ -830,7 +843,7 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args, ws, rank)))
         return
-    if workload(args).get("n_req", 1) > 1:
+    if batched(workload(args)):
         out = run_gpu_batched(args, ws, rank, local)
     else:
         out = run_gpu(args, ws, rank, local)

@@ -70,13 +70,15 @@ enum {
   MFD_OP_LMHEAD_TOPK = 0,
   MFD_OP_LOGITS_TOPK = 1,
   MFD_OP_BUILD_TREE = 2,
-  MFD_OP_VERIFY = 3
+  MFD_OP_VERIFY = 3,
+  MFD_OP_TREE_ANALYTICS = 4
 };
 
 /* Bytes of scratch that `op` needs for the given sizes on the CURRENT CUDA
  * device (the LM-head and verify splits follow its SM count).  Arguments an
  * op does not use are ignored: LMHEAD_TOPK uses (R, V, topk); LOGITS_TOPK
- * uses (R, V, topk); BUILD_TREE uses (n_req); VERIFY uses (n_req).
+ * uses (R, V, topk); BUILD_TREE uses (n_req); VERIFY uses (n_req);
+ * TREE_ANALYTICS uses (n_req, B).
  * Returns 0 for an unknown op or sizes outside the limits. */
 size_t mfd_workspace_size(int op, int n_req, int K, int L, int topk, int B, int R, int V);
 
@@ -286,6 +288,43 @@ int mfd_verify(const float *target_logits, int n_req, int B, int V, int L,
                const float *temperature, const uint64_t *seed, int32_t *accept_len,
                int32_t *path_nodes, int32_t *out_tokens, int32_t *status, void *ws,
                size_t ws_bytes, mfd_stream_t stream);
+
+/* Tree analytics: what a tree spends its budget on (project page "Multi-Future
+ * Drafting", TL;DR and Abstract: chimeras -- prefixes spliced from different
+ * futures that the target never produces; How it works, step 1, and "What the
+ * modes are", Figure 3: the expected number of accepted tokens is the
+ * probability mass the tree covers, read depth by depth).  Not part of a
+ * round: an analysis of trees against known futures and target logits.
+ *
+ *   parent, token, depth int32 [n_req][B + 1], n_nodes int32 [n_req]: trees
+ *                 in mfd_build_tree's format (parents before children)
+ *   futures       int32 [n_req][F][L]: the futures a chimera splices
+ *   target_logits fp32 [n_req][B + 1][V] (device memory); temperature fp32
+ *                 [n_req] (0 = greedy)
+ * Outputs:
+ *   node_class int32 [n_req][B + 1]: MFD_NODE_ON_FUTURE (the root, or a prefix
+ *              of some future), MFD_NODE_CHIMERA (every token is some future's
+ *              token at that position, yet the prefix is no future's),
+ *              MFD_NODE_OTHER; -1 past n_nodes
+ *   reach  double [n_req][B + 1]: probability that the verification walk
+ *              arrives at the node: the product, root first, of the target's
+ *              probability of each next token -- softmax(t[parent] / T)[token]
+ *              for T > 0, 1 or 0 for the greedy choice (argmax, smallest id on
+ *              ties) at T = 0; 0 past n_nodes
+ *   mass   double [n_req][L + 1]: sum of reach over the nodes at each depth
+ *              (mass[0] = 1); summed over depths >= 1 it is the expected
+ *              accepted length
+ * Probabilities are computed in double.  Limits: B <= 512, L <= 16, F >= 1.
+ * ws: mfd_workspace_size(MFD_OP_TREE_ANALYTICS, n_req, .., B, ..) bytes.
+ * Errors: INVALID_ARG, UNSUPPORTED (limits), WORKSPACE, CUDA; a tree that is
+ * not topological, a depth that is not its parent's plus one, a token outside
+ * [0, V) or a negative temperature set MFD_ERR_INPUT in *status. */
+enum { MFD_NODE_ON_FUTURE = 0, MFD_NODE_CHIMERA = 1, MFD_NODE_OTHER = 2 };
+int mfd_tree_analytics(const int32_t *parent, const int32_t *token, const int32_t *depth,
+                       const int32_t *n_nodes, int n_req, int B, int L, const int32_t *futures, int F,
+                       const float *target_logits, int V, const float *temperature, int32_t *node_class,
+                       double *reach, double *mass, int32_t *status, void *ws, size_t ws_bytes,
+                       mfd_stream_t stream);
 
 /* MFD-D, the single-mode default path (project page "Multi-Future Drafting",
  * In a serving engine, the MFD-D paragraph and Figure 5): the same drafter

@@ -81,8 +81,8 @@ def test_two_gloo_ranks():
 @pytest.mark.parametrize("n_req", [0, 6])
 def test_reference_arm_batched_workload(n_req):
     """The reference arm on a batched workload (4 requests, per-request
-    temperatures; --n-req overrides the batch): one line, the per-request work
-    scaled by the batch."""
+    temperatures; --n-req overrides the batch): one line; a step is one full
+    request's round and a round of the batch is that many of them."""
     import subprocess
 
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2", "--warmup", "0",
@@ -92,5 +92,6 @@ def test_reference_arm_batched_workload(n_req):
     line = json.loads(out.stdout.strip().splitlines()[-1])
     want = n_req or 4
     assert line["impl"] == "reference" and line["config"]["n_req"] == want and line["value"] > 0
-    assert f"scaled x{want}" in line["cpu_baseline"]["sample"]
+    assert f"a round of {want} requests is {want} such rounds" in line["cpu_baseline"]["sample"]
+    assert "one full round" in line["cpu_baseline"]["sample"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0

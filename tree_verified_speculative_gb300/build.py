@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmfd.so")
 LIB_CHECKED = os.path.join(BUILD, "libmfd_checked.so")
-SOURCES = ["lmhead.cu", "topk.cu", "tree.cu", "verify.cu", "mfd_api.cu"]
+SOURCES = ["lmhead.cu", "topk.cu", "tree.cu", "verify.cu", "analytics.cu", "mfd_api.cu"]
 HEADERS = ["lmhead.h", "mfd_device.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]

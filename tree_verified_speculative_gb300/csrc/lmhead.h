@@ -90,4 +90,20 @@ struct VerifyLaunch {
 int verify_max_grid(int n_sm);
 cudaError_t launch_verify(const VerifyLaunch &V, cudaStream_t stream);
 
+// analytics.cu
+struct AnalyticsLaunch {
+  const float *t;  // target logits [n_req][B + 1][V]
+  int n_req, B, V, L;
+  const int32_t *parent, *token, *depth, *n_nodes;
+  const int32_t *futures;  // [n_req][F][L]
+  int F;
+  const float *temperature;
+  double *lse;     // scratch [n_req][B + 1]
+  int32_t *amax;   // scratch [n_req][B + 1]
+  int32_t *node_class;
+  double *reach, *mass;
+  int32_t *status;
+};
+cudaError_t launch_tree_analytics(const AnalyticsLaunch &A, cudaStream_t stream);
+
 }  // namespace mfd

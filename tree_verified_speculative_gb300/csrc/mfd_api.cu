@@ -170,6 +170,8 @@ TopkLayout logits_layout(int R, int V, int topk) {
 
 size_t verify_bytes(int n_sm) { return align256((size_t)mfd::verify_max_grid(n_sm) * 8 * 8); }
 
+size_t analytics_bytes(int n_req, int B) { return align256((size_t)n_req * (B + 1) * 8) + align256((size_t)n_req * (B + 1) * 4); }
+
 size_t tree_bytes(int n_req) {
   (void)n_req;
   return 256;  // the tree is built in shared memory; the scratch is not used
@@ -219,6 +221,39 @@ const char *mfd_status_string(int status) {
   }
 }
 
+int mfd_tree_analytics(const int32_t *parent, const int32_t *token, const int32_t *depth, const int32_t *n_nodes,
+                       int n_req, int B, int L, const int32_t *futures, int F, const float *target_logits, int V,
+                       const float *temperature, int32_t *node_class, double *reach, double *mass, int32_t *status,
+                       void *ws, size_t ws_bytes, mfd_stream_t stream) {
+  if (!parent || !token || !depth || !n_nodes || !futures || !target_logits || !temperature || !node_class ||
+      !reach || !mass || !status)
+    return MFD_ERR_INVALID_ARG;
+  if (n_req < 1 || B < 1 || L < 1 || F < 1 || V < 1) return MFD_ERR_INVALID_ARG;
+  if (B > 512 || L > 16 || F > 64 || V >= (1 << 30)) return MFD_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < analytics_bytes(n_req, B) || !aligned(ws, 256)) return MFD_ERR_WORKSPACE;
+  char *base = static_cast<char *>(ws);
+  mfd::AnalyticsLaunch A;
+  A.t = target_logits;
+  A.n_req = n_req;
+  A.B = B;
+  A.V = V;
+  A.L = L;
+  A.parent = parent;
+  A.token = token;
+  A.depth = depth;
+  A.n_nodes = n_nodes;
+  A.futures = futures;
+  A.F = F;
+  A.temperature = temperature;
+  A.lse = reinterpret_cast<double *>(base);
+  A.amax = reinterpret_cast<int32_t *>(base + align256((size_t)n_req * (B + 1) * 8));
+  A.node_class = node_class;
+  A.reach = reach;
+  A.mass = mass;
+  A.status = status;
+  return cuda_status(mfd::launch_tree_analytics(A, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int mfd_mfdd_modes(int n_req, int K) {
   if (n_req < 1 || K < 1 || K > 16) return 0;
   return n_req < MFD_MFDD_SWITCH_REQUESTS ? K : 1;
@@ -244,6 +279,9 @@ size_t mfd_workspace_size(int op, int n_req, int K, int L, int topk, int B, int 
       if (n_req < 1) return 0;
       if (current_device_info(&d) != MFD_OK) return 0;
       return verify_bytes(d.n_sm);
+    case MFD_OP_TREE_ANALYTICS:
+      if (n_req < 1 || B < 1 || B > 512) return 0;
+      return analytics_bytes(n_req, B);
     default:
       return 0;
   }

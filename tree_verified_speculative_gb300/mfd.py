@@ -31,13 +31,15 @@ MFD_OP_LMHEAD_TOPK = 0
 MFD_OP_LOGITS_TOPK = 1
 MFD_OP_BUILD_TREE = 2
 MFD_OP_VERIFY = 3
+MFD_OP_TREE_ANALYTICS = 4
+MFD_NODE_ON_FUTURE, MFD_NODE_CHIMERA, MFD_NODE_OTHER = 0, 1, 2
 
 EXPORTS = ("mfd_status_string", "mfd_workspace_size", "mfd_lmhead_topk", "mfd_lmhead_packed_bytes",
            "mfd_lmhead_pack", "mfd_lmhead_topk_packed", "mfd_lmhead_topk_subset", "mfd_logits_topk",
            "mfd_logits_topk_noalloc",
            "mfd_build_tree", "mfd_verify", "mfd_verify_withheld_test", "mfd_mfdd_modes",
            "mfd_lmhead_packed_fp8_bytes", "mfd_lmhead_pack_fp8", "mfd_fp8_quantize_rows",
-           "mfd_lmhead_fp8_workspace_bytes", "mfd_lmhead_topk_fp8")
+           "mfd_lmhead_fp8_workspace_bytes", "mfd_lmhead_topk_fp8", "mfd_tree_analytics")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _lock = threading.Lock()
@@ -114,6 +116,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.mfd_lmhead_fp8_workspace_bytes.restype = SZ
         lib.mfd_lmhead_topk_fp8.argtypes = [P, I, I, P, I, I, P, P, P, P, P, SZ, P]
         lib.mfd_lmhead_topk_fp8.restype = I
+        lib.mfd_tree_analytics.argtypes = [P, P, P, P, I, I, I, P, I, P, I, P, P, P, P, P, P, SZ, P]
+        lib.mfd_tree_analytics.restype = I
         _libs[p] = lib
         if path is None:
             _lib = lib
@@ -150,6 +154,35 @@ def _s(stream) -> int | None:
 def _check(rc: int, where: str) -> None:
     if rc != MFD_OK:
         raise MfdError(rc, where)
+
+
+def mfd_tree_analytics(parent, token, depth, n_nodes, L, futures, target_logits, temperature, node_class, reach,
+                       mass, status, ws, stream=None) -> None:
+    """Chimera classes and covered mass of trees (see include/mfd.h):
+    futures int32 [n_req][F][L], target_logits fp32 [n_req][B+1][V]."""
+    n_req, N = parent.shape
+    F = futures.shape[1]
+    V = target_logits.shape[-1]
+    rc = load().mfd_tree_analytics(_p(parent), _p(token), _p(depth), _p(n_nodes), n_req, N - 1, L, _p(futures), F,
+                                   _p(target_logits), V, _p(temperature), _p(node_class), _p(reach), _p(mass),
+                                   _p(status), _p(ws), ws.numel() * ws.element_size(), _s(stream))
+    _check(rc, "mfd_tree_analytics")
+
+
+def tree_analytics(parent, token, depth, n_nodes, L, futures, target_logits, temperature, stream=None):
+    """mfd_tree_analytics with its outputs and scratch allocated here:
+    returns (node_class, reach, mass, status) device tensors."""
+    n_req, N = parent.shape
+    dev = parent.device
+    cls = torch.empty((n_req, N), dtype=torch.int32, device=dev)
+    reach = torch.empty((n_req, N), dtype=torch.float64, device=dev)
+    mass = torch.empty((n_req, L + 1), dtype=torch.float64, device=dev)
+    status = torch.zeros((1,), dtype=torch.int32, device=dev)
+    ws = torch.empty((mfd_workspace_size(MFD_OP_TREE_ANALYTICS, n_req, 1, 1, 1, N - 1),), dtype=torch.uint8,
+                     device=dev)
+    mfd_tree_analytics(parent, token, depth, n_nodes, L, futures, target_logits, temperature, cls, reach, mass,
+                       status, ws, stream)
+    return cls, reach, mass, status
 
 
 def mfd_mfdd_modes(n_req: int, K: int) -> int:

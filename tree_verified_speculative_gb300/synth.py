@@ -167,12 +167,13 @@ class Round:
 
 
 def round_inputs(W: torch.Tensor, K: int, L: int, n_shared: int, seed: int,
-                 vocab: np.ndarray | None = None) -> Round:
+                 vocab: np.ndarray | None = None, scale: float = 6.0) -> Round:
     """W is the full-vocabulary head; with `vocab`, the futures are drawn from
-    that draft vocabulary."""
+    that draft vocabulary.  `scale` sets how confident the drafter is in its
+    futures (the planted token's logit is about `scale`)."""
     rng = _rng(seed)
     fut = futures(K, L, W.shape[0], n_shared, rng, vocab)
-    h = hidden(W, fut, rng)
+    h = hidden(W, fut, rng, scale)
     m = int(rng.integers(0, K))
     s = int(rng.integers(0, 2**63 - 1))
     return Round(h=h, fut=fut, target_mode=m, seed=s)
