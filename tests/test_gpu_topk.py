@@ -224,12 +224,15 @@ def test_subset_head_rejects_ids_out_of_range():
     assert np.all(np_(a.tk_tok) == -1)
 
 
+TILE = 128  # vocabulary rows of one LM-head tile
+
+
 def _ranges(V: int) -> list[tuple[int, int]]:
-    """The LM head's vocabulary ranges at one M tile, as 256-row tile spans
-    [t0, t1): min(tiles, SMs) contiguous ranges (the split the library's
+    """The LM head's vocabulary ranges at one M tile, as spans [t0, t1) of
+    128-row tiles: min(tiles, SMs) contiguous ranges (the split the library's
     host code plans for R <= 128 rows)."""
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
-    n_vt = -(-V // 256)
+    n_vt = -(-V // TILE)
     P = min(n_vt, n_sm, 256)
     return [(r * n_vt // P, (r + 1) * n_vt // P) for r in range(P)]
 
@@ -241,7 +244,7 @@ def test_lmhead_ties_duplicate_rows(packed):
     Qwen3.5-4B", first paragraph: the B best prefixes, ties to the smaller
     ids; project page, How it works, step 3).  Groups of identical weight
     rows give exactly equal logits on both sides: (i) inside one range's
-    first 32 columns (the sorted first chunk), (ii) in different 256-row
+    first 32 columns (the sorted first chunk), (ii) in different 128-row
     tiles of one range, (iii) in different vocabulary ranges, and (iv) six
     copies across ranges with top-4, so the cut falls inside the tie.  Each
     hidden row points at one group, whose members are then its best
@@ -253,10 +256,10 @@ def test_lmhead_ties_duplicate_rows(packed):
     assert two, "expected a range with two tiles"
     t2 = two[len(two) // 2]
     groups = [
-        [ranges[5][0] * 256 + 3, ranges[5][0] * 256 + 17, ranges[5][0] * 256 + 30],
-        [t2[0] * 256 + 100, (t2[0] + 1) * 256 + 7],
-        [ranges[0][0] * 256 + 200, ranges[40][0] * 256 + 5, ranges[100][0] * 256 + 250, ranges[-1][0] * 256 + 1],
-        [ranges[i][0] * 256 + 11 * i % 256 for i in (2, 30, 31, 77, 120, 151 % len(ranges))],
+        [ranges[5][0] * TILE + 3, ranges[5][0] * TILE + 17, ranges[5][0] * TILE + 30],
+        [t2[0] * TILE + 100, (t2[0] + 1) * TILE + 7],
+        [ranges[0][0] * TILE + 120, ranges[40][0] * TILE + 5, ranges[100][0] * TILE + 127, ranges[-1][0] * TILE + 1],
+        [ranges[i][0] * TILE + 11 * i % TILE for i in (2, 30, 31, 77, 120, 151 % len(ranges))],
     ]
     members = [v for g in groups for v in g]
     assert len(set(members)) == len(members) and max(members) < V

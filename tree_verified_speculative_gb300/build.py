@@ -1,7 +1,8 @@
 """Build libmfd.so (sm_103a) in-tree with nvcc: one object per .cu file,
-compiled in parallel, linked with -shared.  The same sources built with
--DMFD_CHECKED give libmfd_checked.so, the bounds-checked build (an index out
-of range is clamped and reported as MFD_ERR_CHECK instead of being used).
+compiled in parallel, linked with -shared.  libmfd_checked.so is the same
+library with the tree builder compiled with -DMFD_CHECKED, the bounds-checked
+build (an index out of range is clamped and reported as MFD_ERR_CHECK instead
+of being used).
 Run: python -m tree_verified_speculative_gb300.build"""
 from __future__ import annotations
 
@@ -17,6 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmfd.so")
 LIB_CHECKED = os.path.join(BUILD, "libmfd_checked.so")
 SOURCES = ["lmhead.cu", "topk.cu", "tree.cu", "verify.cu", "analytics.cu", "mfd_api.cu"]
+CHECKED_SOURCES = ["tree.cu"]  # the sources with bounds checks under -DMFD_CHECKED
 HEADERS = ["lmhead.h", "mfd_device.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
@@ -59,7 +61,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     newest = _newest_input()
     if (not force and all(os.path.exists(p) and os.path.getmtime(p) >= newest for p in (LIB, LIB_CHECKED))):
         return LIB
-    jobs = [(s, False) for s in SOURCES] + [(s, True) for s in SOURCES]
+    # the checks live in tree.cu; the checked library shares every other object
+    jobs = [(s, False) for s in SOURCES] + [(s, True) for s in CHECKED_SOURCES]
     with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
         results = list(ex.map(_compile, jobs))
     log = "\n".join(err for _, err in results[:len(SOURCES)])
@@ -67,8 +70,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
         f.write(log)
     if verbose:
         print(log)
-    _link([o for o, _ in results[:len(SOURCES)]], LIB)
-    _link([o for o, _ in results[len(SOURCES):]], LIB_CHECKED)
+    plain = [o for o, _ in results[:len(SOURCES)]]
+    checked = {src: o for (src, _), (o, _) in zip(jobs[len(SOURCES):], results[len(SOURCES):])}
+    _link(plain, LIB)
+    _link([checked.get(src, o) for src, o in zip(SOURCES, plain)], LIB_CHECKED)
     return LIB
 
 

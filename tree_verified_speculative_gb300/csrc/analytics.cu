@@ -43,10 +43,10 @@ __global__ void __launch_bounds__(ROW_THREADS)
   const int nn = n_nodes[q];
   if (nn < 1 || nn > N || n >= nn) return;
   if (tid == 0) has_child = 0;
-  __syncthreads();
+  block_sync();
   for (int c = 1 + tid; c < nn; c += ROW_THREADS)
     if (parent[(size_t)q * N + c] == n) has_child = 1;
-  __syncthreads();
+  block_sync();
   if (!has_child) return;
   const float T = temperature[q];
   const float *row = t + ((size_t)q * N + n) * (size_t)V;
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(ROW_THREADS)
     red_f[warp] = bv;
     red_i[warp] = bi;
   }
-  __syncthreads();
+  block_sync();
   if (tid == 0) {
     for (int w = 1; w < ROW_THREADS / 32; ++w)
       if (vi_before(red_f[w], red_i[w], red_f[0], red_i[0])) {
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(ROW_THREADS)
         red_i[0] = red_i[w];
       }
   }
-  __syncthreads();
+  block_sync();
   if (!(T > 0.f)) {
     if (tid == 0) amax[(size_t)q * N + n] = red_i[0];
     return;
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(ROW_THREADS)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   if (lane == 0) red_d[warp] = s;
-  __syncthreads();
+  block_sync();
   if (tid == 0) {
     double tot = 0.0;
     for (int w = 0; w < ROW_THREADS / 32; ++w) tot += red_d[w];
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(NODE_THREADS)
   const int nn = n_nodes[q];
   const float T = temperature[q];
   if (tid == 0) bad = !(nn >= 1 && nn <= N) || !(T >= 0.f);
-  __syncthreads();
+  block_sync();
   if (bad) {
     if (tid == 0) report(status, MFD_ERR_INPUT);
     return;
@@ -126,14 +126,14 @@ __global__ void __launch_bounds__(NODE_THREADS)
     tok_s[n] = token[(size_t)q * N + n];
     dep_s[n] = depth[(size_t)q * N + n];
   }
-  __syncthreads();
+  block_sync();
   // the tree's own shape: parents first, depth one more than the parent's
   for (int n = tid; n < nn; n += NODE_THREADS) {
     const bool ok = n == 0 ? (dep_s[0] == 0) : (par_s[n] >= 0 && par_s[n] < n && dep_s[n] == dep_s[par_s[n]] + 1 &&
                                                   dep_s[n] <= L && tok_s[n] >= 0 && tok_s[n] < V);
     if (!ok) bad = 1;
   }
-  __syncthreads();
+  block_sync();
   if (bad) {
     if (tid == 0) report(status, MFD_ERR_INPUT);
     return;
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(NODE_THREADS)
     }
     edge_s[n] = e;
   }
-  __syncthreads();
+  block_sync();
   for (int n = tid; n < nn; n += NODE_THREADS) {
     // reach: the edges multiplied from the root down
     int path[MAX_L + 1];
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(NODE_THREADS)
     node_class[(size_t)q * N + n] = -1;
     reach[(size_t)q * N + n] = 0.0;
   }
-  __syncthreads();
+  block_sync();
   // mass by depth, summed in node order
   if (tid <= L) {
     double s = 0.0;

@@ -9,17 +9,17 @@
 // whole cost, so the kernel reads W exactly once, with TMA, and keeps the
 // logits in tensor memory: they never reach global memory.
 //
-//   D[128 x 256] (TMEM, fp32) = h_tile[128 x H] . W_tile[256 x H]^T
+//   D[128 x 128] (TMEM, fp32) = h_tile[128 x H] . W_tile[128 x H]^T
 //
-// A = 128 hidden rows (one M tile, zero-filled past R), B = 256 vocabulary
-// rows, K streamed through a 4-stage shared-memory ring of one 64-element
+// A = 128 hidden rows (one M tile, zero-filled past R), B = 128 vocabulary
+// rows, K streamed through a 6-stage shared-memory ring of one 64-element
 // (128-byte, swizzled) K atom each.  Each TMEM lane is one hidden row, so the
 // epilogue thread that owns lane r reads its row's logits column by column
 // and keeps the row's running max, running sum of exp and a sorted top-T in
 // registers -- no cross-thread reduction.
 //
 // Grid: persistent, one CTA per SM.  The vocabulary is split into P
-// contiguous ranges of 256-row tiles; work item = (range, M tile).  A CTA
+// contiguous ranges of 128-row tiles; work item = (range, M tile).  A CTA
 // writes, per row and range, (max, sum exp) and its T best (logit, id)
 // pairs; merge_topk (topk.cu) combines the P partials of a row.
 //
@@ -31,8 +31,12 @@
 //
 // Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer (one
 // thread each), warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4)..).
-// TMEM holds two 256-column fp32 accumulators so that the epilogue of tile
-// n overlaps the MMAs of tile n+1.
+// TMEM holds four 128-column fp32 accumulators, so that the MMAs can run up
+// to three tiles ahead of the epilogue: the epilogue of a range's first tile,
+// where the row's top-T fills and most columns enter it, takes longer than a
+// tile's stream, and with four accumulators the stream goes on meanwhile.
+// The exposed end, the last tile's epilogue after the last byte, is also
+// half of what a 256-row tile gave.
 //
 // FP8 form (project page, In a serving engine, Figure 5 caption: the
 // drafter's linear layers in FP8, quantized online): the weight is packed
@@ -51,24 +55,39 @@ namespace mfd {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int PK = 256;           // vocabulary rows of a packed weight block
 constexpr int BK = 64;            // one 128-byte swizzle atom of bf16
 constexpr int BK8 = 128;          // one 128-byte swizzle atom of E4M3
 constexpr int KSUB = 1;           // K atoms per pipeline stage
-constexpr int STAGES = 4;
 constexpr int A_SUB = BM * BK * 2;  // one K atom of the hidden tile
-constexpr int B_SUB = BN * BK * 2;  // one K atom of the weight tile
+constexpr int PK_SUB = PK * BK * 2;  // one K atom of a packed block
 constexpr int A_BYTES = KSUB * A_SUB;
-constexpr int B_BYTES = KSUB * B_SUB;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
-constexpr int TMEM_COLS = 2 * BN;
+constexpr int TMEM_COLS = 512;
+
+// Tile shape.  BN = 128 vocabulary rows (one M tile, the weight stream
+// bounds the head): four 128-column accumulators and a 6-stage ring of 32 KB
+// stages.  BN = 256 (several M tiles, tensor bound): two 256-column
+// accumulators, a 4-stage ring of 48 KB stages and half as many hidden-tile
+// loads per weight byte.
+template <int BN_>
+struct Tile {
+  static constexpr int BN = BN_;
+  static constexpr int NACC = TMEM_COLS / BN;
+  static constexpr int STAGES = BN == 128 ? 6 : 4;
+  static constexpr int B_SUB = BN * BK * 2;  // one K atom of the weight tile
+  static constexpr int B_BYTES = KSUB * B_SUB;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+};
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int STAGE_STRIDE = 36;  // floats per staged row (16-byte aligned rows)
 constexpr int STAGE_ROW_BYTES = 32 * STAGE_STRIDE * 4;  // one epilogue warp's 32 rows
 
+template <int BN>
 constexpr int smem_bytes() {
-  return 1024 /* alignment slack */ + STAGES * STAGE_BYTES + 4 * STAGE_ROW_BYTES + 8 * (2 * STAGES + 5) + 16;
+  using TL = Tile<BN>;
+  return 1024 /* alignment slack */ + TL::STAGES * TL::STAGE_BYTES + 4 * STAGE_ROW_BYTES +
+         8 * (2 * TL::STAGES + 2 * TL::NACC + 1) + 16;
 }
 
 struct Params {
@@ -94,24 +113,34 @@ __device__ __forceinline__ void item_range(const Params &p, int item, int &mt, i
   t1 = (int)(((long long)(range + 1) * p.n_vt) / p.P);
 }
 
+// The packed weight holds 256-row blocks (pack_w_kernel).  The K atom kc of
+// 256-row tile t is block (t, kc); that of 128-row tile t is half of block
+// (t / 2, kc): its first 16 KB for an even tile, its second for an odd one.
+// A half is self-contained: the swizzle repeats every 8 rows.
+template <int BN>
+__device__ __forceinline__ const uint8_t *packed_at(const uint8_t *w, int t, int kc, int nk) {
+  if (BN == PK) return w + ((size_t)t * nk + kc) * PK_SUB;
+  return w + ((size_t)(t >> 1) * nk + kc) * PK_SUB + (size_t)(t & 1) * Tile<BN>::B_SUB;
+}
+
 // Insert (x, v) into the sorted (value desc, id asc) list; the caller has
-// checked that x beats the last entry.  Its place is the number of entries
-// before it, and every entry from there on moves down one: T independent
-// compares and T independent selects, not a chain of T compare-swaps.
+// checked that x beats the last entry.  b[s] = entry s stays before (x, v);
+// the b's are true up to x's place and false after it, so entry s keeps its
+// place when b[s], takes (x, v) when b[s - 1] alone holds, and takes entry
+// s - 1 otherwise: T independent compares and two selects per entry, with no
+// position to count or compare.
 template <int T>
 __device__ __forceinline__ void topk_insert(float (&tv)[T], int (&ti)[T], float x, int v) {
-  int pos = 0;
+  bool b[T];
 #pragma unroll
-  for (int s = 0; s < T; ++s) pos += vi_before(tv[s], ti[s], x, v) ? 1 : 0;
+  for (int s = 0; s < T; ++s) b[s] = vi_before(tv[s], ti[s], x, v);
 #pragma unroll
   for (int s = T - 1; s > 0; --s) {  // tv[s - 1] is still the old entry here
-    tv[s] = s > pos ? tv[s - 1] : (s == pos ? x : tv[s]);
-    ti[s] = s > pos ? ti[s - 1] : (s == pos ? v : ti[s]);
+    tv[s] = b[s] ? tv[s] : (b[s - 1] ? x : tv[s - 1]);
+    ti[s] = b[s] ? ti[s] : (b[s - 1] ? v : ti[s - 1]);
   }
-  if (pos == 0) {
-    tv[0] = x;
-    ti[0] = v;
-  }
+  tv[0] = b[0] ? tv[0] : x;
+  ti[0] = b[0] ? ti[0] : v;
 }
 
 // Sort 32 (value, id) pairs best first (value desc, id asc) with a bitonic
@@ -142,10 +171,12 @@ __device__ __forceinline__ void sort32_best_first(float (&sv)[32], int (&si)[32]
 // PACKED: the weight comes as pack_w_kernel lays it out, so a stage's
 // weight bytes are one contiguous 1-D bulk copy instead of KSUB 2-D boxes of
 // 256 rows x 128 bytes (rows 2H bytes apart), which stream markedly slower.
-template <int T, bool PACKED, bool FP8>
+template <int T, bool PACKED, bool FP8, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     lmhead_topk_kernel(const __grid_constant__ CUtensorMap tmap_h, const __grid_constant__ CUtensorMap tmap_w,
                        const Params p) {
+  using TL = Tile<BN>;
+  constexpr int NACC = TL::NACC, STAGES = TL::STAGES, B_SUB = TL::B_SUB, B_BYTES = TL::B_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -155,8 +186,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES + 4 * STAGE_ROW_BYTES);
   uint64_t *empty = full + STAGES;
   uint64_t *tfull = empty + STAGES;
-  uint64_t *tempty = tfull + 2;
-  uint64_t *drain = tempty + 2;
+  uint64_t *tempty = tfull + NACC;
+  uint64_t *drain = tempty + NACC;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *never = abort_flag + 1;
@@ -171,7 +202,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NACC; ++a) {
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 4);
     }
@@ -187,7 +218,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  block_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   static_assert(!FP8 || PACKED, "the FP8 weight is always packed");
@@ -230,7 +261,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (tn >= 0)
               for (int kb = mt; kb < nk; kb += p.n_mt) {
                 if (PACKED)
-                  bulk_prefetch_l2(p.w_packed + ((size_t)tn * nk + kb) * B_SUB, (uint32_t)B_SUB);
+                  bulk_prefetch_l2(packed_at<BN>(p.w_packed, tn, kb, nk), (uint32_t)B_SUB);
                 else
                   tma_prefetch_2d(&tmap_w, kb * KEL, tn * BN);
               }
@@ -243,8 +274,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             mbar_arrive_expect_tx(&full[stage], (uint32_t)(nsub * (A_SUB + B_SUB)));
             if (PACKED)
-              bulk_load_1d(sB + stage * B_BYTES, p.w_packed + ((size_t)t * nk + kc) * B_SUB, (uint32_t)(nsub * B_SUB),
-                           &full[stage], pol_w);
+              bulk_load_1d(sB + stage * B_BYTES, packed_at<BN>(p.w_packed, t, kc, nk), (uint32_t)(nsub * B_SUB), &full[stage],
+                           pol_w);
             else
               for (int sub = 0; sub < nsub; ++sub)
                 tma_load_2d(sB + stage * B_BYTES + sub * B_SUB, &tmap_w, (kc + sub) * KEL, t * BN, &full[stage],
@@ -268,6 +299,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int s = 0; s < STAGES; ++s)
         if ((issued >> s) & 1u) mbar_wait(&full[s], (issued_par >> s) & 1u, never);
     }
+    // The block barrier below is an aligned one: the warp's idle lanes wait
+    // here for lane 0 so that all 32 reach it together.  Arriving there apart
+    // from lane 0 held the warp for 10-27 us at the end of the kernel.
+    __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------- MMA issuer
@@ -313,8 +348,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           if (!ok) break;
           tc_commit(&tfull[acc]);
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1u;
+          if (++acc == NACC) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
         }
       }
       if (!ok) {
@@ -325,6 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_commit(drain);
       mbar_wait(drain, 0, never);
     }
+    __syncwarp();  // as the producer warp: reconverge before the block barrier
   } else {
     // --------------------------------------------------------- epilogue
     const int quarter = warp & 3;
@@ -426,8 +464,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == NACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       if (!ok) break;
       const int row = mt * BM + row_in_tile;
@@ -445,7 +485,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
 
-  __syncthreads();
+  block_sync();
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
@@ -462,11 +502,11 @@ __global__ void pack_w_kernel(const uint4 *__restrict__ W, int V, int H, uint4 *
   const int nk = H / BK;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n16; q += stride) {
-    const size_t blk = q / (B_SUB / 16);
-    const int c = (int)(q - blk * (B_SUB / 16));
+    const size_t blk = q / (PK_SUB / 16);
+    const int c = (int)(q - blk * (PK_SUB / 16));
     const int t = (int)(blk / nk), a = (int)(blk - (size_t)t * nk);
     const int r = c >> 3, j = (c & 7) ^ (r & 7);
-    const int row = t * BN + r;
+    const int row = t * PK + r;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (row < V) v = __ldg(W + (size_t)row * (H / 8) + a * 8 + j);
     Wp[q] = v;
@@ -509,11 +549,11 @@ __global__ void pack_w_fp8_kernel(const uint4 *__restrict__ W, int V, int H, con
   const float inv = a > 0.f ? __fdiv_rn(448.0f, a) : 0.f;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n16; q += stride) {
-    const size_t blk = q / (B_SUB / 16);
-    const int c = (int)(q - blk * (B_SUB / 16));
+    const size_t blk = q / (PK_SUB / 16);
+    const int c = (int)(q - blk * (PK_SUB / 16));
     const int t = (int)(blk / nk), s = (int)(blk - (size_t)t * nk);
     const int r = c >> 3, j = (c & 7) ^ (r & 7);
-    const int row = t * BN + r;
+    const int row = t * PK + r;
     uint32_t o[4] = {0u, 0u, 0u, 0u};
     if (row < V) {
       const uint4 *src = W + ((size_t)row * H + (size_t)s * BK8 + (size_t)j * 16) / 8;
@@ -566,9 +606,9 @@ __global__ void __launch_bounds__(128) quant_rows_kernel(const uint16_t *__restr
   if (lane == 0) scale[r] = __fdiv_rn(m, 448.0f);
 }
 
-template <int T, bool PACKED, bool FP8>
+template <int T, bool PACKED, bool FP8, int BN>
 cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
-  static_assert(smem_bytes() <= 232448, "shared memory budget");
+  static_assert(smem_bytes<BN>() <= 232448, "shared memory budget");
   Params p;
   p.R = L.R;
   p.H = L.H;
@@ -583,53 +623,58 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
   p.w_packed = static_cast<const uint8_t *>(L.w_packed);
   p.row_scale = L.row_scale;
   p.w_amax = L.w_amax;
-  cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<T, PACKED, FP8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
+  cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<T, PACKED, FP8, BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<BN>());
   if (e != cudaSuccess) return e;
   const int grid = p.n_items < L.n_sm ? p.n_items : L.n_sm;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = smem_bytes();
+  cfg.dynamicSmemBytes = smem_bytes<BN>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, lmhead_topk_kernel<T, PACKED, FP8>, *L.tmap_h, PACKED ? *L.tmap_h : *L.tmap_w, p);
+  e = cudaLaunchKernelEx(&cfg, lmhead_topk_kernel<T, PACKED, FP8, BN>, *L.tmap_h, PACKED ? *L.tmap_h : *L.tmap_w, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int lmhead_tile_rows() { return BN; }
+int lmhead_tile_rows(int R) { return R <= BM ? 128 : 256; }
 int lmhead_m_rows() { return BM; }
 int lmhead_k_chunk() { return BK; }
 
-cudaError_t launch_lmhead_partials(const LmheadLaunch &L, cudaStream_t stream) {
+template <int BN>
+cudaError_t launch_bn(const LmheadLaunch &L, cudaStream_t stream) {
   const bool pk = L.w_packed != nullptr;
   if (L.fp8) {
     if (!pk || !L.row_scale || !L.w_amax) return cudaErrorInvalidValue;
     switch (L.T) {
-      case 8: return launch_t<8, true, true>(L, stream);
-      case 16: return launch_t<16, true, true>(L, stream);
-      case 32: return launch_t<32, true, true>(L, stream);
+      case 8: return launch_t<8, true, true, BN>(L, stream);
+      case 16: return launch_t<16, true, true, BN>(L, stream);
+      case 32: return launch_t<32, true, true, BN>(L, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (L.T) {
-    case 8: return pk ? launch_t<8, true, false>(L, stream) : launch_t<8, false, false>(L, stream);
-    case 16: return pk ? launch_t<16, true, false>(L, stream) : launch_t<16, false, false>(L, stream);
-    case 32: return pk ? launch_t<32, true, false>(L, stream) : launch_t<32, false, false>(L, stream);
+    case 8: return pk ? launch_t<8, true, false, BN>(L, stream) : launch_t<8, false, false, BN>(L, stream);
+    case 16: return pk ? launch_t<16, true, false, BN>(L, stream) : launch_t<16, false, false, BN>(L, stream);
+    case 32: return pk ? launch_t<32, true, false, BN>(L, stream) : launch_t<32, false, false, BN>(L, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-size_t lmhead_packed_bytes(int V, int H) { return (size_t)((V + BN - 1) / BN) * BN * (size_t)H * 2; }
+cudaError_t launch_lmhead_partials(const LmheadLaunch &L, cudaStream_t stream) {
+  return lmhead_tile_rows(L.R) == 128 ? launch_bn<128>(L, stream) : launch_bn<256>(L, stream);
+}
 
-size_t lmhead_packed_fp8_bytes(int V, int H) { return (size_t)((V + BN - 1) / BN) * BN * (size_t)H + 256; }
+size_t lmhead_packed_bytes(int V, int H) { return (size_t)((V + PK - 1) / PK) * PK * (size_t)H * 2; }
+
+size_t lmhead_packed_fp8_bytes(int V, int H) { return (size_t)((V + PK - 1) / PK) * PK * (size_t)H + 256; }
 
 cudaError_t launch_pack_w_fp8(const void *W, int V, int H, void *Wp, cudaStream_t stream) {
   const size_t body = lmhead_packed_fp8_bytes(V, H) - 256;

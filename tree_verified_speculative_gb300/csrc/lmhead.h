@@ -22,7 +22,7 @@ struct LmheadLaunch {
   const float *w_amax = nullptr;     // FP8: the weight's largest magnitude (in the packed buffer's trailer)
 };
 
-int lmhead_tile_rows();  // vocabulary rows per tile (256)
+int lmhead_tile_rows(int R);  // vocabulary rows per tile for R hidden rows (128 for one M tile, else 256)
 int lmhead_m_rows();     // hidden rows per M tile (128)
 int lmhead_k_chunk();    // K elements per pipeline stage (64)
 cudaError_t launch_lmhead_partials(const LmheadLaunch &L, cudaStream_t stream);

@@ -126,7 +126,7 @@ static long long best_ranges(int tiles, int n_groups, int workers, int *P_out) {
 
 TopkLayout lmhead_layout(int R, int V, int topk, int n_sm) {
   TopkLayout y;
-  const int tiles = (V + mfd::lmhead_tile_rows() - 1) / mfd::lmhead_tile_rows();
+  const int tiles = (V + mfd::lmhead_tile_rows(R) - 1) / mfd::lmhead_tile_rows(R);
   const int n_mt = (R + mfd::lmhead_m_rows() - 1) / mfd::lmhead_m_rows();
   y.P = tiles < n_sm ? tiles : n_sm;
   if (y.P > 256) y.P = 256;
@@ -321,7 +321,7 @@ int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int 
   } else if ((rc = tensor_map(h, R, H, mfd::lmhead_m_rows(), &mh)) != MFD_OK) {
     return rc;
   }
-  if (W && (rc = tensor_map(W, V, H, mfd::lmhead_tile_rows(), &mw)) != MFD_OK) return rc;
+  if (W && (rc = tensor_map(W, V, H, mfd::lmhead_tile_rows(R), &mw)) != MFD_OK) return rc;
   mfd::LmheadLaunch L;
   L.tmap_h = &mh;
   L.tmap_w = W ? &mw : nullptr;

@@ -238,6 +238,15 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------- misc
+// A block barrier that every warp reaches with all 32 lanes together.
+// __syncthreads is an aligned barrier; a warp whose lanes come to it apart
+// (after a loop of per-lane trip counts, or a branch taken by one lane) first
+// reconverges here.
+__device__ __forceinline__ void block_sync() {
+  __syncwarp();
+  __syncthreads();
+}
+
 // fp32 -> uint32 key whose ascending order is the float's DESCENDING order;
 // -0.0 is folded onto +0.0 so that equal floats get equal keys.
 __device__ __forceinline__ uint32_t desc_key(float f) {

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(MERGE_THREADS)
     red_s[warp] = ls;
   }
   if (lane < G) gbest[warp][lane] = g;
-  __syncthreads();
+  block_sync();
 
   float M = red_m[0];
 #pragma unroll
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(MERGE_THREADS)
       for (int k = 2; k < cnt[s]; ++k) surv[off++] = list_at(q, k);
     }
   }
-  __syncthreads();
+  block_sync();
   const int n_surv = n_surv_s;
 
   if (n_surv <= SURV_CAP) {
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(MERGE_THREADS)
       if (lane == 0) top[r] = w;
     }
   }
-  __syncthreads();
+  block_sync();
 
   // ---- log-probabilities, final order (log p desc, id asc)
   if (tid < topk) {

@@ -61,7 +61,7 @@ __device__ __forceinline__ int chk_index(int i, int n) {
   if (threadIdx.x == 0) chk_bad_s = 0
 #define CHK_REPORT()                                                    \
   do {                                                                  \
-    __syncthreads();                                                    \
+    block_sync();                                                    \
     if (threadIdx.x == 0 && chk_bad_s) report(prm.status, MFD_ERR_CHECK); \
   } while (0)
 #else
@@ -282,7 +282,7 @@ __device__ void radix_bound(Shared &sh, const PE *ent, int n, int G, int B, int 
     sh.has_tau = 0;
   }
   for (int i = tid; i < G * 256; i += THREADS) hA[i] = 0;
-  __syncthreads();
+  block_sync();
   for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
     int *hist = (pass & 1) ? hB : hA;
@@ -303,7 +303,7 @@ __device__ void radix_bound(Shared &sh, const PE *ent, int n, int G, int B, int 
     }
     if (pass + 1 < passes)
       for (int i = tid; i < G * 256; i += THREADS) next[i] = 0;
-    __syncthreads();
+    block_sync();
     for (int g = warp; g < G; g += NWARPS) {
       if (!sh.act[g]) continue;
       int c[8], sum = 0;
@@ -337,7 +337,7 @@ __device__ void radix_bound(Shared &sh, const PE *ent, int n, int G, int B, int 
         run += c[b];
       }
     }
-    __syncthreads();
+    block_sync();
   }
 }
 
@@ -365,7 +365,7 @@ __device__ int compact_pool(Shared &sh, PE *ent, uint8_t *nxt, int n, KeepFn kee
         kp[j] = keep(e[j], i);
       }
     }
-    __syncthreads();
+    block_sync();
 #pragma unroll
     for (int j = 0; j < STAGE; ++j) {
       if (!__any_sync(0xffffffffu, kp[j])) continue;
@@ -376,7 +376,7 @@ __device__ int compact_pool(Shared &sh, PE *ent, uint8_t *nxt, int n, KeepFn kee
       }
     }
   }
-  __syncthreads();
+  block_sync();
   return sh.n_out;
 }
 
@@ -410,12 +410,12 @@ __device__ __noinline__ void bound_owned(Shared &sh, const PE *ent, int *hist, i
       lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
       hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
     }
-    __syncthreads();
+    block_sync();
     if (lane == 0 && lo <= hi) {
       atomicMin(&sh.kmin, lo);
       atomicMax(&sh.kmax, hi);
     }
-    __syncthreads();
+    block_sync();
   }
   const uint32_t kmin = sh.kmin, kmax = sh.kmax;
   const int hb = (kmin ^ kmax) ? 31 - __clz((int)(kmin ^ kmax)) : 0;
@@ -437,7 +437,7 @@ __device__ __noinline__ void bound_owned(Shared &sh, const PE *ent, int *hist, i
       warp_hist_add(digit ? hist + 256 : hist, bin);
     }
     if (digit == 0 && tid < 256) hist[256 + tid] = 0;
-    __syncthreads();
+    block_sync();
     }
     if (warp == 0) {
       const int *h = digit ? hist + 256 : hist;
@@ -466,7 +466,7 @@ __device__ __noinline__ void bound_owned(Shared &sh, const PE *ent, int *hist, i
         }
       }
     }
-    __syncthreads();
+    block_sync();
     if (!sh.refine) break;
     prefix = sh.pre[0];
     shift = shift > 8 ? shift - 8 : 0;
@@ -567,7 +567,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) sh.wbad[warp] = bad;
   }
-  __syncthreads();
+  block_sync();
   {
     int any_bad = 0;
 #pragma unroll
@@ -649,7 +649,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       }
     }
   }
-  __syncthreads();
+  block_sync();
   {
     // fixed slots, mode-major: depth 1 first, then depth 2
     int N1 = 0, N2 = 0;
@@ -742,7 +742,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         if (own) atomicAdd(&hist[b], 1);
         atomicAdd(&hall[b], 1);
       }
-      __syncthreads();
+      block_sync();
       if (warp == 0) {
         // the first digit's boundary bin for the B-th owned entry (as in
         // bound_owned), and how many entries lie within it
@@ -775,7 +775,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
           sh.cut2 = 1;
         }
       }
-      __syncthreads();
+      block_sync();
       if (sh.cut2) {
         // every entry within that first bound; the others can neither be in
         // the tree nor lead to it
@@ -819,7 +819,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       if (tid == 0) sh.n_ent = N1 + N2;
     }
   }
-  __syncthreads();
+  block_sync();
   const bool cut2 = sh.cut2;
 
   // The bound: the B-th best score key among the owned entries (distinct
@@ -855,10 +855,10 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       }
       flg[i] = kp;
     }
-    __syncthreads();
+    block_sync();
     const int out = compact_by_flag(sh, ent, nxt, n, flg);
     if (tid == 0) sh.n_ent = out;
-    __syncthreads();
+    block_sync();
   };
 
   // ---------------------------------------------------- level expansion
@@ -894,7 +894,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         sh.overflow = 0;
         sh.n_par = 0;
       }
-      __syncthreads();
+      block_sync();
       const int n0 = sh.n_ent;
       const bool ht = sh.has_tau;
       const uint32_t tau = sh.tau;
@@ -915,7 +915,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         const int k = warp_append(&sh.n_par, isp);
         if (isp && k < PLIST) plist[k] = (uint16_t)i;
       }
-      __syncthreads();
+      block_sync();
       const int np = sh.n_par;
       if (np <= PLIST && np * topk <= PAIR_MAX && n0 + np * topk <= CAP) {
         // few parents and room for every child: all (parent, rank) pairs at once
@@ -946,7 +946,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
             nxt[CHK(slot, CAP)] = 0;
           }
         }
-        __syncthreads();
+        block_sync();
         for (int pi = tid; pi < np; pi += THREADS) nxt[CHK(plist[pi], n0)] = (uint8_t)topk;
       } else {
         for (int base = warp * 32; base < n0; base += THREADS) {
@@ -999,12 +999,12 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
           if (isp) nxt[i] = (uint8_t)j;
         }
       }
-      __syncthreads();
+      block_sync();
       if (tid == 0) {
         if (sh.n_ent > CAP) sh.n_ent = CAP;
         if (sh.n_ent > n0) sh.any = 1;
       }
-      __syncthreads();
+      block_sync();
       if (sh.any) tau_current = false;
       if (!sh.overflow) break;
       prune_exact();
@@ -1025,7 +1025,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       const uint32_t tau = sh.tau;
       const int n = compact_by_tau(sh, ent, nxt, sh.n_ent, tau);
       if (tid == 0) sh.n_ent = n;
-      __syncthreads();
+      block_sync();
     }
   }
   if (sh.n_ent > NC) {  // many ties within the bound: keep each mode's exact B best
@@ -1058,7 +1058,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       sh.coll = 0;
       sh.n_sel = 0;
     }
-    __syncthreads();
+    block_sync();
     uint64_t hpr[JH];
 #pragma unroll
     for (int jj = 0; jj < JH; ++jj) {
@@ -1085,7 +1085,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       hslot[CHK(i, NC)] = (uint16_t)s;
       atomicMin(&bkey[CHK(s, tsize)], desc_key(e.score));
     }
-    __syncthreads();
+    block_sync();
 #pragma unroll
     for (int jj = 0; jj < JH; ++jj) {
       const int i = tid + jj * THREADS;
@@ -1119,10 +1119,10 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       }
       pslot[CHK(i, NC)] = ps;
     }
-    __syncthreads();
+    block_sync();
     if (!sh.coll) break;
     seed = mix64(seed + 0x9E3779B97F4A7C15ull);
-    __syncthreads();
+    block_sync();
   }
   if (sh.coll) {
     if (tid == 0) report(prm.status, MFD_ERR_UNSUPPORTED);
@@ -1147,7 +1147,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
       }
     }
   }
-  __syncthreads();
+  block_sync();
 
   // ---------------------------------------------------- the B best prefixes
   // With few candidates every primary is ranked; otherwise a radix bound on
@@ -1157,7 +1157,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     const bool ht_sel = sh.act[0];
     const uint32_t tau_sel = sh.pre[0] | 0xFFFFu;
     if (tid == 0) sh.n_sel = 0;
-    __syncthreads();
+    block_sync();
     for (int base = warp * 32; base < n; base += THREADS) {
       const int i = base + lane;
       const bool in = i < n && prim[i] && (!ht_sel || desc_key(ent[i].score) <= tau_sel);
@@ -1167,7 +1167,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
         skk[CHK(k, NC)] = desc_key(ent[i].score);
       }
     }
-    __syncthreads();
+    block_sync();
   }
   const int ns = sh.n_sel;
   const int nruns = (ns + 31) >> 5;
@@ -1197,7 +1197,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     skk[a] = key;
     ra[a] = (uint16_t)ia;
   }
-  __syncthreads();
+  block_sync();
   for (int r = warp; r < nruns; r += NWARPS) {
     const int pos = r * 32 + lane;
     const uint32_t key = skk[pos];
@@ -1251,7 +1251,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     par_s[0] = -1;
     sh.bad = 0;
   }
-  __syncthreads();
+  block_sync();
   const int nn = ns < B ? ns : B;
 
   // ---------------------------------------------------- parents
@@ -1265,7 +1265,7 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     }
     par_s[nd] = (int16_t)par;
   }
-  __syncthreads();
+  block_sync();
   if (sh.bad) {
     if (tid == 0) report(prm.status, MFD_ERR_INPUT);
     CHK_REPORT();

@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(THREADS) verify_kernel(const Params p) {
         red_v[warp] = bv;
         red_i[warp] = bi;
       }
-      __syncthreads();
+      block_sync();
       if (warp == 0) {
         bv = lane < THREADS / 32 ? red_v[lane] : -INFINITY;
         bi = lane < THREADS / 32 ? red_i[lane] : 0x7FFFFFFF;
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(THREADS) verify_kernel(const Params p) {
           }
         }
       }
-      __syncthreads();
+      block_sync();
       if (!s_ok) {
         if (tid == 0) {
           report(p.status, MFD_ERR_TIMEOUT);
