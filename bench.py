@@ -82,6 +82,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the short runs of the other configurations that the default line carries")
     ap.add_argument("--n-req", type=int, default=0,
                     help="requests per round for a batched workload (0: the workload's own); temperatures cycle")
     ap.add_argument("--profile-rounds", type=int, default=0,
@@ -413,7 +415,7 @@ def run_gpu(args, ws, rank, local):
     sites = {**sites_t}
 
     # ------------------------------------------------------------ e2e
-    e2e = run_e2e(args, cfg, rounds, noise, sites, head, rd, dev)
+    e2e = None if getattr(args, "no_e2e", False) else run_e2e(args, cfg, rounds, noise, sites, head, rd, dev)
 
     # ------------------------------------------------------------ roofline
     peak, peak_kind = peaks()
@@ -833,6 +835,32 @@ def profile_rounds(args, local):
         raise SystemExit(1)
 
 
+# The other configurations of the method statement, run briefly after the
+# default one so that its line carries their figures too: the pages' 4B shape
+# at B=64 greedy, the wider shape, and 32 batched requests.
+SECONDARY = (("k8_l15_h2560_v151936_b64_greedy", 20), ("k8_l15_h5120_v248320_b256_greedy", 20),
+             ("r32_k8_l15_h2560_v151936_b128_mixed", 10))
+
+
+def run_secondary(args, ws, rank, local):
+    """Short runs of SECONDARY (no end-to-end or CPU-baseline legs): each
+    entry's rate, per-stage times and roofline."""
+    import copy
+
+    import torch
+
+    out = {}
+    for name, steps in SECONDARY:
+        a = copy.copy(args)
+        a.workload, a.steps, a.warmup, a.n_req, a.no_e2e, a.no_cpu_baseline = name, steps, 3, 0, True, True
+        r = run_gpu_batched(a, ws, rank, local) if batched(workload(a)) else run_gpu(a, ws, rank, local)
+        out[name] = {k: r[k] for k in ("value", "unit", "steps", "warmup", "ms_per_step", "stages_us", "roofline",
+                                       "mean_accept_len", "clocks") if k in r}
+        out[name]["config"] = {k: v for k, v in r["config"].items() if k not in ("timing",)}
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     ws, rank, local = dist_setup()
@@ -847,6 +875,8 @@ def main():
         out = run_gpu_batched(args, ws, rank, local)
     else:
         out = run_gpu(args, ws, rank, local)
+        if args.workload == DEFAULT and ws == 1 and not args.no_secondary:
+            out["secondary"] = run_secondary(args, ws, rank, local)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:

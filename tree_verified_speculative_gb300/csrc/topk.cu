@@ -73,22 +73,28 @@ __global__ void __launch_bounds__(MERGE_THREADS)
   };
   if (tid == 0) n_surv_s = 0;
 
-  // ---- (max, sum exp) and the first two candidates of each owned list
+  // ---- (max, sum exp) and the first four candidates of each owned list, in
+  // one round trip: a list rarely holds more than four of the row's top-k
+  constexpr int HEAD = 4;  // T >= 8
   float m[LISTS_PER_THREAD], sx[LISTS_PER_THREAD];
-  Cand h0[LISTS_PER_THREAD], h1[LISTS_PER_THREAD];
+  Cand hd[LISTS_PER_THREAD][HEAD];
 #pragma unroll
   for (int s = 0; s < LISTS_PER_THREAD; ++s) {
     const int q = tid + MERGE_THREADS * s;
     m[s] = -INFINITY;
     sx[s] = 0.f;
-    h0[s] = h1[s] = Cand{-INFINITY, 0x7FFFFFFF};
+#pragma unroll
+    for (int j = 0; j < HEAD; ++j) hd[s][j] = Cand{-INFINITY, 0x7FFFFFFF};
     if (q < P) {
       const float2 x = __ldcg(ms + q);
-      const int4 c = __ldcg(reinterpret_cast<const int4 *>(cand + (size_t)q * T));
+      const int4 c0 = __ldcg(reinterpret_cast<const int4 *>(cand + (size_t)q * T));
+      const int4 c1 = __ldcg(reinterpret_cast<const int4 *>(cand + (size_t)q * T) + 1);
       m[s] = x.x;
       sx[s] = x.y;
-      h0[s] = cand_of(c.x, c.y);
-      h1[s] = cand_of(c.z, c.w);
+      hd[s][0] = cand_of(c0.x, c0.y);
+      hd[s][1] = cand_of(c0.z, c0.w);
+      hd[s][2] = cand_of(c1.x, c1.y);
+      hd[s][3] = cand_of(c1.z, c1.w);
     }
   }
 
@@ -101,7 +107,7 @@ __global__ void __launch_bounds__(MERGE_THREADS)
   ls = warp_sum(ls);
   int G = 1;
   while (G < topk) G <<= 1;
-  Cand g = before(h0[1], h0[0]) ? h0[1] : h0[0];
+  Cand g = before(hd[1][0], hd[0][0]) ? hd[1][0] : hd[0][0];
   for (int o = 16; o >= G; o >>= 1) {
     const Cand d = shfl_cand(g, o);
     if (before(d, g)) g = d;
@@ -141,12 +147,11 @@ __global__ void __launch_bounds__(MERGE_THREADS)
   for (int s = 0; s < LISTS_PER_THREAD; ++s) {
     const int q = tid + MERGE_THREADS * s;
     int k = 0;
-    if (q < P && !before(tau, h0[s])) {
-      k = 1;
-      if (T > 1 && !before(tau, h1[s])) {
-        k = 2;
+    if (q < P) {
+#pragma unroll
+      for (int j = 0; j < HEAD; ++j) k += (k == j && !before(tau, hd[s][j])) ? 1 : 0;
+      if (k == HEAD)
         while (k < T && !before(tau, list_at(q, k))) ++k;
-      }
     }
     cnt[s] = k;
     c += k;
@@ -156,9 +161,10 @@ __global__ void __launch_bounds__(MERGE_THREADS)
 #pragma unroll
     for (int s = 0; s < LISTS_PER_THREAD; ++s) {
       const int q = tid + MERGE_THREADS * s;
-      if (cnt[s] > 0) surv[off++] = h0[s];
-      if (cnt[s] > 1) surv[off++] = h1[s];
-      for (int k = 2; k < cnt[s]; ++k) surv[off++] = list_at(q, k);
+#pragma unroll
+      for (int j = 0; j < HEAD; ++j)
+        if (j < cnt[s]) surv[off++] = hd[s][j];
+      for (int k = HEAD; k < cnt[s]; ++k) surv[off++] = list_at(q, k);
     }
   }
   block_sync();

@@ -547,10 +547,18 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     if (tid == 0) sh.n_ent = 0;
     if (tid < 512) hist[tid] = 0;  // the first bound's two digit histograms
     if (tid < 256) hist[512 + tid] = 0;  // and the count of every depth-1 and depth-2 entry
-    __syncwarp();
+  }
+  block_sync();
+  // The checks read only the warp's own rows; they run in the same interval
+  // as the ownership scan below, and their verdict is acted on after the next
+  // block barrier, before anything derived from the tables is used.
+  {
+    int SEG = 1;
+    while (SEG < topk) SEG <<= 1;
+    const int rows = K * L, spw = 32 / SEG;
+    const int seg = lane / SEG, j = lane - seg * SEG;
     bool bad = false;
-#pragma unroll 1
-    for (int r = 0; r < RMAX; ++r) {
+    for (int r = 0; (r * NWARPS + warp) * spw < rows; ++r) {
       const int row = (r * NWARPS + warp) * spw + seg;
       if (row < rows && j < topk) {
         const float *lr = lp_s + row * topk;
@@ -566,17 +574,6 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     }
     bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) sh.wbad[warp] = bad;
-  }
-  block_sync();
-  {
-    int any_bad = 0;
-#pragma unroll
-    for (int w = 0; w < NWARPS; ++w) any_bad |= sh.wbad[w];
-    if (any_bad) {
-      if (tid == 0) report(prm.status, MFD_ERR_INPUT);
-      CHK_REPORT();
-      return;
-    }
   }
   const Ctx c{lp_s, tok_s, K, L, topk};
   auto mode_of = [&](int i) { return pk_mode(ent[i].k1); };
@@ -650,6 +647,16 @@ __global__ void __launch_bounds__(THREADS, 1) build_tree_kernel(const Params prm
     }
   }
   block_sync();
+  {
+    int any_bad = 0;
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) any_bad |= sh.wbad[w];
+    if (any_bad) {
+      if (tid == 0) report(prm.status, MFD_ERR_INPUT);
+      CHK_REPORT();
+      return;
+    }
+  }
   {
     // fixed slots, mode-major: depth 1 first, then depth 2
     int N1 = 0, N2 = 0;
