@@ -103,8 +103,11 @@ size_t mfd_workspace_size(int op, int n_req, int K, int L, int topk, int B, int 
  *                                bounded pipeline wait running out)
  * Requires an sm_103a device.  TMA descriptors for (h, W, R, H, V) are
  * encoded on the first call and cached by (pointer, shape); the cache is
- * thread-safe.  Errors: INVALID_ARG (NULL, R < 1, misaligned h/W),
- * UNSUPPORTED (limits, device), WORKSPACE, CUDA. */
+ * thread-safe.  Hidden rows that span 144 KB or less (R * H * 2 bytes) are
+ * first copied into ws, padded with zero rows: every CTA reads them, and on
+ * GB300 rows within so few bytes of address space are served by few L2
+ * slices.  The copy changes no result.  Errors: INVALID_ARG (NULL, R < 1,
+ * misaligned h/W), UNSUPPORTED (limits, device), WORKSPACE, CUDA. */
 int mfd_lmhead_topk(const void *h, int R, int H, const void *W, int V, int topk,
                     float *tk_logp, int32_t *tk_tok, float *lse, int32_t *status, void *ws,
                     size_t ws_bytes, mfd_stream_t stream);

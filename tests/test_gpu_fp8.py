@@ -111,6 +111,25 @@ def head():
     return W, mfd.pack_lm_head_fp8(W.cuda())
 
 
+@pytest.mark.parametrize("R", [1, 15])
+def test_fp8_staged_hidden_rows_match_unstaged(head, R):
+    """E4M3 hidden rows that span 144 KB or less are quantized into a
+    zero-padded copy; 60 rows (150 KB) are not padded.  The same rows give
+    bit-identical tables either way."""
+    W, Wp = head
+    h = synth.round_inputs(W, 8, 15, 11, seed=71).h[:60]
+    out = []
+    for rows in (R, 60):
+        rd = mfd.Round(1, 1, rows, 16, 1, 151936, H=2560)
+        rd.status.zero_()
+        rd.lmhead_topk_fp8(h[:rows].contiguous().cuda(), Wp)
+        torch.cuda.synchronize()
+        assert status_of(rd) == 0
+        out.append((np_(rd.tk_tok)[:R], np_(rd.tk_logp)[:R].view(np.uint32), np_(rd.lse)[:R].view(np.uint32)))
+    for a, b in zip(*out):
+        np.testing.assert_array_equal(a, b)
+
+
 def test_lmhead_fp8_pages_shape_sampled_rows(head):
     """K=8, L=15, H=2560, V=151,936, top-16: all 120 rows through the FP8
     head, 12 of them against the oracle's FP8 head over the full vocabulary;

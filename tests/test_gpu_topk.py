@@ -87,6 +87,32 @@ def head_2560():
     return W, W.cuda()
 
 
+@pytest.mark.parametrize("R", [1, 15, 25])
+def test_staged_hidden_rows_match_unstaged(head_2560, R):
+    """Hidden rows that span 144 KB or less (here 1, 15 and 25 rows of 5 KB)
+    are read from a zero-padded copy in the workspace; 40 rows (200 KB) are
+    read in place.  The same rows give bit-identical tables either way, on
+    the row-major and the packed weight: each MMA row is independent."""
+    W, Wd = head_2560
+    h = synth.round_inputs(W, 8, 15, 11, seed=70).h[:40]
+    Wp = mfd.pack_lm_head(Wd)
+    for packed in (False, True):
+        out = []
+        for rows in (R, 40):
+            rd = mfd.Round(1, 1, rows, 16, 1, 151936)
+            rd.status.zero_()
+            hd = h[:rows].contiguous().cuda()
+            if packed:
+                rd.lmhead_topk_packed(hd, Wp)
+            else:
+                rd.lmhead_topk(hd, Wd)
+            torch.cuda.synchronize()
+            assert status_of(rd) == 0
+            out.append((np_(rd.tk_tok)[:R], np_(rd.tk_logp)[:R].view(np.uint32), np_(rd.lse)[:R].view(np.uint32)))
+        for a, b in zip(*out):
+            np.testing.assert_array_equal(a, b)
+
+
 def test_lmhead_pages_shape_sampled_rows(head_2560):
     """K=8, L=15, H=2560, V=151936, top-k 16, planted futures (11 of 15
     shared): all 120 rows through the kernel, 24 of them checked against the

@@ -571,14 +571,20 @@ __global__ void pack_w_fp8_kernel(const uint4 *__restrict__ W, int V, int H, con
 
 // Online FP8 of the hidden rows: one warp per row of x (bf16 [R][H]):
 // amax = max |x|, q = e4m3(x * (448 / amax)), scale[r] = amax / 448 (0 and
-// zero bytes for an all-zero row).
+// zero bytes for an all-zero row).  q has `rows` rows `stride` bytes apart;
+// rows R..rows-1 are written as zero bytes.
 __global__ void __launch_bounds__(128) quant_rows_kernel(const uint16_t *__restrict__ x, int R, int H,
-                                                        uint8_t *__restrict__ q, float *__restrict__ scale) {
+                                                        uint8_t *__restrict__ q, float *__restrict__ scale,
+                                                        int rows, size_t stride) {
   pdl_wait();
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 4 + warp;
-  if (r >= R) return;
+  if (r >= rows) return;
+  if (r >= R) {
+    for (int k = lane * 8; k < H; k += 256) *reinterpret_cast<uint2 *>(q + (size_t)r * stride + k) = make_uint2(0u, 0u);
+    return;
+  }
   const uint16_t *xr = x + (size_t)r * H;
   float m = 0.f;
   for (int k = lane * 8; k < H; k += 256) {
@@ -601,9 +607,25 @@ __global__ void __launch_bounds__(128) quant_rows_kernel(const uint16_t *__restr
       const uint32_t bits = (e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16);
       o[e >> 2] |= to_e4m3(__fmul_rn(__uint_as_float(bits), inv)) << (8 * (e & 3));
     }
-    *reinterpret_cast<uint2 *>(q + (size_t)r * H + k) = make_uint2(o[0], o[1]);
+    *reinterpret_cast<uint2 *>(q + (size_t)r * stride + k) = make_uint2(o[0], o[1]);
   }
   if (lane == 0) scale[r] = __fdiv_rn(m, 448.0f);
+}
+
+// Staged hidden rows: row r of x (row16 16-byte words) to row r of dst
+// (stride16 words apart), zeros for rows R..rows-1.  One CTA per row.
+__global__ void __launch_bounds__(128) stage_rows_kernel(const uint4 *__restrict__ x, int R, int row16,
+                                                        uint4 *__restrict__ dst, int stride16) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int r = blockIdx.x;
+  uint4 *d = dst + (size_t)r * stride16;
+  if (r < R) {
+    const uint4 *s = x + (size_t)r * row16;
+    for (int i = threadIdx.x; i < row16; i += 128) d[i] = __ldg(s + i);
+  } else {
+    for (int i = threadIdx.x; i < row16; i += 128) d[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 template <int T, bool PACKED, bool FP8, int BN>
@@ -689,9 +711,12 @@ cudaError_t launch_pack_w_fp8(const void *W, int V, int H, void *Wp, cudaStream_
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_rows(const void *x, int R, int H, void *q, float *scale, cudaStream_t stream) {
+cudaError_t launch_quant_rows(const void *x, int R, int H, void *q, float *scale, cudaStream_t stream, int rows,
+                              size_t stride) {
+  if (rows < R) rows = R;
+  if (stride == 0) stride = (size_t)H;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((R + 3) / 4);
+  cfg.gridDim = dim3((rows + 3) / 4);
   cfg.blockDim = dim3(128);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -700,7 +725,57 @@ cudaError_t launch_quant_rows(const void *x, int R, int H, void *q, float *scale
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, quant_rows_kernel, static_cast<const uint16_t *>(x), R, H,
-                                     static_cast<uint8_t *>(q), scale);
+                                     static_cast<uint8_t *>(q), scale, rows, stride);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// Every CTA of the LM head reads the same hidden rows at about the same
+// time.  Measured on GB300: while those rows span 128 KB of addresses or
+// less, wherever they sit, their L2 requests gather on a few L2 slices (the
+// busiest slice serves about 5x the mean instead of 2x) and one M tile's
+// kernel takes 1.45x as long (172-182 us instead of 120 us at V = 151,936,
+// H = 2560, for 1 to 25 rows).  Such rows are copied into scratch first:
+// zero rows are appended until they span more than kHiddenSpread bytes, and
+// when even a full M tile of rows would not, the rows are spaced further
+// apart.  The zero rows change no result: each MMA row is independent and
+// rows past R are never written out.
+constexpr size_t kHiddenSpread = 144 * 1024;
+
+HiddenStage lmhead_hidden_stage(int R, size_t row_bytes) {
+  HiddenStage s{false, R, row_bytes, 0};
+  if (R > BM || (size_t)R * row_bytes > kHiddenSpread) return s;
+  const size_t need = kHiddenSpread + 1;
+  size_t rows = (need + row_bytes - 1) / row_bytes;
+  if (rows > (size_t)BM) rows = BM;
+  if (rows < (size_t)R) rows = R;
+  size_t stride = ((need + rows - 1) / rows + 127) / 128 * 128;
+  if (stride < row_bytes) stride = row_bytes;
+  s.staged = true;
+  s.rows = (int)rows;
+  s.stride = stride;
+  s.bytes = rows * stride;
+  return s;
+}
+
+// Staged only when R * row_bytes <= kHiddenSpread: either rows * row_bytes
+// <= kHiddenSpread + row_bytes (stride = row_bytes), or rows = BM and stride
+// <= (kHiddenSpread + 1) / BM + 128.
+size_t lmhead_stage_max_bytes() { return 2 * kHiddenSpread + 1 + (size_t)BM * 128 + 256; }
+
+cudaError_t launch_stage_rows(const void *x, int R, size_t row_bytes, void *dst, const HiddenStage &s,
+                              cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s.rows);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, stage_rows_kernel, static_cast<const uint4 *>(x), R, (int)(row_bytes / 16),
+                                     static_cast<uint4 *>(dst), (int)(s.stride / 16));
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

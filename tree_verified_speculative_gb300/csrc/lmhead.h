@@ -32,8 +32,26 @@ cudaError_t launch_pack_w(const void *W, int V, int H, void *Wp, cudaStream_t st
 // 256-byte trailer whose first word is the weight's largest magnitude
 size_t lmhead_packed_fp8_bytes(int V, int H);
 cudaError_t launch_pack_w_fp8(const void *W, int V, int H, void *Wp, cudaStream_t stream);
-// online E4M3 of bf16 rows x [R][H] (H % 8 == 0): q [R][H] bytes, scale [R]
-cudaError_t launch_quant_rows(const void *x, int R, int H, void *q, float *scale, cudaStream_t stream);
+// online E4M3 of bf16 rows x [R][H] (H % 8 == 0): q [rows][stride] bytes
+// (rows >= R; rows past R zero; 0 = R rows of H bytes), scale [R]
+cudaError_t launch_quant_rows(const void *x, int R, int H, void *q, float *scale, cudaStream_t stream,
+                              int rows = 0, size_t stride = 0);
+
+// Hidden rows as the LM head reads them.  Every CTA reads the same hidden
+// rows at about the same time; rows that span too few bytes of address
+// space are staged into scratch first, padded with zero rows (and, for
+// narrow rows, spaced further apart), so that they span more.
+struct HiddenStage {
+  bool staged;    // copied into scratch before the LM head
+  int rows;       // rows the hidden operand spans (>= R; rows past R are zero)
+  size_t stride;  // bytes from one row to the next
+  size_t bytes;   // scratch bytes of the staged copy (0 unless staged)
+};
+HiddenStage lmhead_hidden_stage(int R, size_t row_bytes);
+size_t lmhead_stage_max_bytes();  // bound on HiddenStage::bytes over every R and row size
+// bf16 rows x [R][row_bytes] -> dst [s.rows][s.stride] (rows past R zero)
+cudaError_t launch_stage_rows(const void *x, int R, size_t row_bytes, void *dst, const HiddenStage &s,
+                              cudaStream_t stream);
 
 // topk.cu
 struct MergeLaunch {

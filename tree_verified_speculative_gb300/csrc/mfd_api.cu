@@ -65,18 +65,20 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-using MapKey = std::tuple<int, const void *, int, int, int, int>;  // device, ptr, rows, cols, box rows, bytes/elem
+using MapKey = std::tuple<int, const void *, int, int, int, int, size_t>;  // device, ptr, rows, cols, box rows, bytes/elem, row stride
 std::map<MapKey, CUtensorMap> g_maps;
 
-// bf16 (elem = 2) or 8-bit (elem = 1) [rows][cols] row-major, box = 128
-// bytes of columns x box_rows rows, 128B swizzle, out-of-range rows read as
-// zero.  The descriptor is copied into *out while the lock is held: another
-// thread may clear the cache right after.
-int tensor_map(const void *ptr, int rows, int cols, int box_rows, CUtensorMap *out, int elem = 2) {
+// bf16 (elem = 2) or 8-bit (elem = 1) [rows][cols] row-major, rows `stride`
+// bytes apart (0: cols * elem), box = 128 bytes of columns x box_rows rows,
+// 128B swizzle, out-of-range rows read as zero.  The descriptor is copied
+// into *out while the lock is held: another thread may clear the cache right
+// after.
+int tensor_map(const void *ptr, int rows, int cols, int box_rows, CUtensorMap *out, int elem = 2, size_t stride = 0) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MFD_ERR_CUDA;
+  if (stride == 0) stride = (size_t)cols * (size_t)elem;
   std::lock_guard<std::mutex> lk(g_mu);
-  const MapKey key{dev, ptr, rows, cols, box_rows, elem};
+  const MapKey key{dev, ptr, rows, cols, box_rows, elem, stride};
   auto it = g_maps.find(key);
   if (it == g_maps.end()) {
     EncodeTiledFn fn = encode_fn();
@@ -84,7 +86,7 @@ int tensor_map(const void *ptr, int rows, int cols, int box_rows, CUtensorMap *o
     CUtensorMap m;
     std::memset(&m, 0, sizeof m);
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * (cuuint64_t)elem};
+    const cuuint64_t strides[1] = {(cuuint64_t)stride};
     const cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1u, 1u};
     const CUresult r = fn(&m, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
@@ -103,6 +105,7 @@ int tensor_map(const void *ptr, int rows, int cols, int box_rows, CUtensorMap *o
 struct TopkLayout {
   int P, T, chunk;
   size_t ms_bytes, cand_bytes, total;
+  size_t stage_off = 0;  // LM head: room for the staged hidden rows (lmhead_hidden_stage)
 };
 
 // Fewest weight tiles for the busiest CTA when n_groups M tiles share
@@ -136,11 +139,15 @@ TopkLayout lmhead_layout(int R, int V, int topk, int n_sm) {
   y.ms_bytes = align256((size_t)R * y.P * 8);
   y.cand_bytes = align256((size_t)R * y.P * y.T * 8);
   y.total = y.ms_bytes + y.cand_bytes;
+  // one M tile: room for the hidden rows staged when they span few bytes
+  y.stage_off = y.total;
+  if (R <= mfd::lmhead_m_rows()) y.total += align256(mfd::lmhead_stage_max_bytes());
   return y;
 }
 
 // FP8 LM head scratch: the partials of lmhead_layout, then the E4M3 hidden
-// rows [R][H] and their scales [R].
+// rows (R rows of H bytes, or the padded rows of lmhead_hidden_stage) and
+// their scales [R].
 struct Fp8Layout {
   TopkLayout y;
   size_t hq_off, sc_off, total;
@@ -149,7 +156,8 @@ Fp8Layout fp8_layout(int R, int H, int V, int topk, int n_sm) {
   Fp8Layout f;
   f.y = lmhead_layout(R, V, topk, n_sm);
   f.hq_off = f.y.total;
-  f.sc_off = f.hq_off + align256((size_t)R * H);
+  const mfd::HiddenStage hs = mfd::lmhead_hidden_stage(R, (size_t)H);
+  f.sc_off = f.hq_off + align256(hs.staged ? hs.bytes : (size_t)R * H);
   f.total = f.sc_off + align256((size_t)R * 4);
   return f;
 }
@@ -312,12 +320,18 @@ int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int 
   char *base = static_cast<char *>(ws);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   CUtensorMap mh, mw;
+  // hidden rows that span few bytes are read from a padded copy
+  const mfd::HiddenStage hs = mfd::lmhead_hidden_stage(R, (size_t)H * (fp8 ? 1 : 2));
   if (fp8) {
     // the hidden rows in E4M3 with their scales, then the E4M3 head over them
     if ((rc = cuda_status(mfd::launch_quant_rows(h, R, H, base + f8.hq_off, reinterpret_cast<float *>(base + f8.sc_off),
-                                                 s))) != MFD_OK)
+                                                 s, hs.rows, hs.stride))) != MFD_OK)
       return rc;
-    if ((rc = tensor_map(base + f8.hq_off, R, H, mfd::lmhead_m_rows(), &mh, 1)) != MFD_OK) return rc;
+    if ((rc = tensor_map(base + f8.hq_off, hs.rows, H, mfd::lmhead_m_rows(), &mh, 1, hs.stride)) != MFD_OK) return rc;
+  } else if (hs.staged) {
+    char *hstage = base + y.stage_off;
+    if ((rc = cuda_status(mfd::launch_stage_rows(h, R, (size_t)H * 2, hstage, hs, s))) != MFD_OK) return rc;
+    if ((rc = tensor_map(hstage, hs.rows, H, mfd::lmhead_m_rows(), &mh, 2, hs.stride)) != MFD_OK) return rc;
   } else if ((rc = tensor_map(h, R, H, mfd::lmhead_m_rows(), &mh)) != MFD_OK) {
     return rc;
   }
