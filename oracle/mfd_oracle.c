@@ -492,16 +492,17 @@ void oracle_philox_batch(const uint32_t *ctr, const uint32_t *key, int n, uint32
   for (int i = 0; i < n; ++i) oracle_philox4x32_10(ctr + 4 * i, key + 2 * i, out + 4 * i);
 }
 
-/* Gumbel noise for (seed, node, vocab id): word 0 of Philox4x32-10 with
- * counter (v, node, 0, 0) and key (seed low 32 bits, seed high 32 bits);
+/* Gumbel noise for (seed, node, vocab id): word v mod 4 of the Philox4x32-10
+ * block with counter (v div 4, node, 0, 0) and key (seed low 32 bits, seed
+ * high 32 bits), so one block serves four consecutive vocabulary ids;
  * u = (2 * (x >> 9) + 1) * 2^-24, exact in fp32 and strictly inside (0, 1);
  * G = -log(-log(u)) with fp32 logarithms. */
 float oracle_gumbel(uint64_t seed, int32_t node, int32_t v) {
-  uint32_t ctr[4] = {(uint32_t)v, (uint32_t)node, 0u, 0u};
+  uint32_t ctr[4] = {(uint32_t)v / 4u, (uint32_t)node, 0u, 0u};
   uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
   uint32_t o[4];
   oracle_philox4x32_10(ctr, key, o);
-  float u = (float)(2u * (o[0] >> 9) + 1u) * 0x1p-24f;
+  float u = (float)(2u * (o[(uint32_t)v % 4u] >> 9) + 1u) * 0x1p-24f;
   return -logf(-logf(u));
 }
 

@@ -109,6 +109,25 @@ def test_philox_against_independent_implementation():
         np.testing.assert_array_equal(oracle.philox4x32_10(ctr, key), got)
 
 
+def test_gumbel_layout_from_the_block_function():
+    """G(seed, node, v) uses word v mod 4 of the Philox block at counter
+    (v div 4, node, 0, 0), key (seed low, seed high): recomputed here from
+    the block function (pinned to Triton's above) with numpy's logarithms."""
+    V = 67
+    for seed, node in ((0, 0), (987654321123, 5), (2 ** 63 + 11, 300)):
+        g = oracle.gumbel(seed, node, V).astype(np.float64)
+        v = np.arange(V)
+        ctr = np.zeros((V, 4), np.uint32)
+        ctr[:, 0] = v // 4
+        ctr[:, 1] = node
+        key = np.zeros((V, 2), np.uint32)
+        key[:, 0] = seed & 0xFFFFFFFF
+        key[:, 1] = (seed >> 32) & 0xFFFFFFFF
+        x = oracle.philox4x32_10(ctr, key)[v, v % 4].astype(np.uint64)
+        u = (2 * (x >> 9) + 1).astype(np.float64) * 2.0 ** -24
+        np.testing.assert_allclose(g, -np.log(-np.log(u)), rtol=0, atol=2e-5)
+
+
 def test_gumbel_moments():
     """G = -log(-log u) is standard Gumbel: mean = Euler-Mascheroni gamma,
     variance = pi^2 / 6."""
