@@ -262,9 +262,9 @@ int mfd_build_tree(const float *tk_logp, const int32_t *tk_tok, int n_req, int K
  * node -- greedy (temperature 0): y = argmax_v t[cur][v]; sampled
  * (temperature T > 0): y = argmax_v (t[cur][v] / T + G(seed, cur, v)), a
  * Gumbel-max draw from softmax(t / T), where G = -log(-log(u)),
- * u = (2 * (x >> 9) + 1) * 2^-24 and x is word 0 of Philox4x32-10 (Salmon et
- * al., SC'11) at counter (v, cur, 0, 0), key (seed low, seed high).  Ties go
- * to the smaller v.  If a child of cur carries y the walk moves there,
+ * u = (2 * (x >> 9) + 1) * 2^-24 and x is word v mod 4 of the Philox4x32-10
+ * block (Salmon et al., SC'11) at counter (v div 4, cur, 0, 0), key (seed
+ * low, seed high).  Ties go to the smaller v.  If a child of cur carries y the walk moves there,
  * otherwise y is the bonus token and the walk stops.
  *
  *   target_logits fp32 [n_req][B + 1][V]; only the rows on the walk are read.
@@ -280,12 +280,16 @@ int mfd_build_tree(const float *tk_logp, const int32_t *tk_tok, int n_req, int K
  *   accept_len    int32 [n_req]         drafted tokens accepted (0..L)
  *   path_nodes    int32 [n_req][L + 1]  node read at step j (path_nodes[0] = 0)
  *   out_tokens    int32 [n_req][L + 1]  y at step j: accepted tokens, bonus last
- * Entries past accept_len hold -1.  The walk is one cooperative grid with a
- * bounded grid-wide wait per step (MFD_ERR_TIMEOUT if it runs out).  The
- * CTAs exchange step results through ws, which needs no zeroing: its words
- * carry a generation counter that each call advances, so ws may be shared
- * with other calls and replayed in CUDA graphs (only calls overlapping on the
- * GPU must not share it). */
+ * Entries past accept_len hold -1.  Below 8 requests the walk is one
+ * cooperative grid with a bounded grid-wide wait per step (MFD_ERR_TIMEOUT if
+ * it runs out); its CTAs exchange step results through ws, which needs no
+ * zeroing: its words carry a generation counter that each call advances, so
+ * ws may be shared with other calls and replayed in CUDA graphs (only calls
+ * overlapping on the GPU must not share it).  From 8 requests on, each
+ * request is walked by one thread-block cluster (up to 16 CTAs) whose CTAs
+ * exchange each step's result in their shared memory behind a hardware
+ * cluster barrier; ws is then not written.  Both forms give the same
+ * results. */
 int mfd_verify(const float *target_logits, int n_req, int B, int V, int L,
                const int32_t *parent, const int32_t *token, const int32_t *n_nodes,
                const float *temperature, const uint64_t *seed, int32_t *accept_len,
@@ -344,7 +348,8 @@ int mfd_mfdd_modes(int n_req, int K);
 
 /* Fault injection for the walk's bounded waits, for tests (the pages have no
  * counterpart: it exists so that the timeout path can be exercised without
- * faulting or hanging a GPU).  Arguments and outputs as mfd_verify, plus
+ * faulting or hanging a GPU).  Arguments and outputs as mfd_verify, always
+ * walked by the cooperative grid (the form with waits), plus
  * wait_limit_ns in [1e3, 1e8]: every bounded wait of this call gives up after
  * that long.  In every request group of more than one CTA (V >= 2048), the
  * CTAs other than the group's first never publish their step result, so the

@@ -121,6 +121,33 @@ def test_mixed_batch_32():
     assert exact >= 30
 
 
+@pytest.mark.parametrize("V", [151936, 20000, 1000])
+def test_cluster_walk_equals_grid_walk(V):
+    """From 8 requests a round is walked by one thread-block cluster per
+    request, below that by the cooperative grid.  Eight requests walked in one
+    call (clusters) and each walked alone (grid) give the same walks, bit for
+    bit, greedy and sampled (T = 1 and 0.7), and the oracle's on the greedy
+    ones."""
+    rng = np.random.default_rng(V)
+    n = 8
+    tree, futs = _trees(rng, n, 4, 15, 8, V, 96)
+    t = _targets(rng, tree, futs, V, rng.integers(0, 4, size=n))
+    temps = [0.0, 1.0, 0.7, 0.0, 1.0, 0.0, 0.7, 1.0]
+    seeds = [int(x) for x in rng.integers(0, 2**63 - 1, size=n)]
+    b_acc, b_path, b_out, st = _gpu_verify(t, tree["parent"], tree["token"], tree["n_nodes"], 15, temps, seeds)
+    assert st == 0
+    for q in range(n):
+        a_acc, a_path, a_out, st = _gpu_verify(t[q:q + 1], tree["parent"][q:q + 1], tree["token"][q:q + 1],
+                                               tree["n_nodes"][q:q + 1], 15, temps[q:q + 1], seeds[q:q + 1])
+        assert st == 0
+        assert int(a_acc[0]) == int(b_acc[q])
+        np.testing.assert_array_equal(a_path[0], b_path[q])
+        np.testing.assert_array_equal(a_out[0], b_out[q])
+        if temps[q] == 0.0:
+            o = oracle.verify(t[q], tree["parent"][q], tree["token"][q], int(tree["n_nodes"][q]), 15, 0.0, seeds[q])
+            assert check_walk(int(b_acc[q]), b_path[q], b_out[q], *o, sampled=False)
+
+
 def test_rejects_bad_temperature():
     parent = np.array([[-1, 0]], np.int32)
     token = np.array([[0, 1]], np.int32)

@@ -100,12 +100,17 @@ struct VerifyLaunch {
   const float *temperature;
   const uint64_t *seed;
   int32_t *accept_len, *path_nodes, *out_tokens, *status;
+  // the grid walk (n_req < VERIFY_CLUSTER_REQUESTS) only:
   unsigned long long *ws;  // [grid][8] exchange words (generation-tagged, no zeroing needed)
   int grid;                   // largest cooperative grid
   unsigned long long wait_ns = 0;  // bounded-wait limit (0: the library's default)
   int withhold = 0;                // fault injection for tests of the bounded waits
 };
+// requests from which a round is walked by clusters (one per request)
+// instead of the cooperative grid
+constexpr int VERIFY_CLUSTER_REQUESTS = 8;
 int verify_max_grid(int n_sm);
+int verify_cluster_size(int V);  // CTAs of the cluster that walks one request
 cudaError_t launch_verify(const VerifyLaunch &V, cudaStream_t stream);
 
 // analytics.cu
