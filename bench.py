@@ -367,20 +367,48 @@ def run_gpu(args, ws, rank, local):
                 tb[ri, ci] = torch.from_numpy(base).to(dev, non_blocking=True)
                 acc_buf[i:i + 1].copy_(rd.accept_len)
 
+    # the timed rounds: the LM head, the tree and the walk back to back in one
+    # interval, as a round runs; the target rows are planted beforehand from
+    # the same round's tree out of an untimed pass (the tree is deterministic,
+    # checked below against the tree each timed round builds)
+    ev_r = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_rounds)]
+    trees_r = {k: torch.empty_like(v) for k, v in trees.items()}
+
+    def phase_round(rounds_idx, sites):
+        for c0 in range(0, len(rounds_idx), CHUNK):
+            ahead(len(rounds_idx[c0:c0 + CHUNK]))
+            for i in rounds_idx[c0:c0 + CHUNK]:
+                rows, cols = sites[i]
+                tb = t_dev[i % N_NOISE]
+                ri = torch.from_numpy(rows).to(dev, non_blocking=True)
+                ci = torch.from_numpy(cols).to(dev, non_blocking=True)
+                base = noise[i % N_NOISE][rows, cols]
+                tb[ri, ci] = torch.from_numpy(base + np.float32(10.0)).to(dev, non_blocking=True)
+                h_cur.copy_(h_all[i])
+                r0, r1 = ev_r[i]
+                r0.record(stream)
+                head(rd, h_cur)
+                rd.build_tree()
+                rd.verify(tb[None], temp, seeds[i:i + 1])
+                r1.record(stream)
+                tb[ri, ci] = torch.from_numpy(base).to(dev, non_blocking=True)
+                acc_buf[i:i + 1].copy_(rd.accept_len)
+                for k in trees_r:
+                    trees_r[k][i].copy_(getattr(rd, k))
+
     warm = list(range(args.warmup))
     timed = list(range(args.warmup, n_rounds))
     phase_a(warm)
     phase_b(warm, plant_sites_of(warm))
+    phase_a(timed)  # untimed: the trees the plant needs
     torch.cuda.synchronize()
+    sites_t = plant_sites_of(timed)
     barrier(ws)
     torch.cuda.synchronize()
     clocks = Clocks(local)
     time.sleep(0.2)
     wall0 = time.perf_counter()
-    phase_a(timed)
-    torch.cuda.synchronize()
-    sites_t = plant_sites_of(timed)
-    phase_b(timed, sites_t)
+    phase_round(timed, sites_t)
     torch.cuda.synchronize()
     wall1 = time.perf_counter()
     barrier(ws)
@@ -389,26 +417,30 @@ def run_gpu(args, ws, rank, local):
     st = int(rd.status.item())
     if st != 0:
         raise RuntimeError(f"device status {st}: {mfd.status_string(st)}")
-    ab = vf = 0.0
-    ab_all = []
-    for i in timed:
-        e0, _, e1, s2, e3 = ev[i]
-        ab_all.append(e0.elapsed_time(e1))
-        ab += ab_all[-1]
-        vf += s2.elapsed_time(e3)
-    total_ms = reduce_max(ab + vf, ws)
+    for k in trees:
+        if not torch.equal(trees[k][timed], trees_r[k][timed]):
+            raise RuntimeError(f"the timed rounds built other trees ({k}) than the untimed pass")
+    round_all = [ev_r[i][0].elapsed_time(ev_r[i][1]) for i in timed]
+    total_ms = reduce_max(sum(round_all), ws)
+    ab_all = [ev[i][0].elapsed_time(ev[i][2]) for i in timed]  # untimed pass: LM head + tree
+    ab = sum(ab_all)
     # diagnostic rounds, after the timed ones and not in the value: the same
-    # rounds again with an event between the LM head and the tree
+    # rounds again with an event between the LM head and the tree, and the
+    # walk alone in its own interval
     diag = timed[:min(len(timed), 200)]
     phase_a(diag, split=True)
+    phase_b(diag, sites_t)
     torch.cuda.synchronize()
     lm_d = [ev[i][0].elapsed_time(ev[i][1]) for i in diag]
     bd_d = [ev[i][1].elapsed_time(ev[i][2]) for i in diag]
-    vf_all = [ev[i][3].elapsed_time(ev[i][4]) for i in timed]
+    vf_all = [ev[i][3].elapsed_time(ev[i][4]) for i in diag]
+    vf = sum(vf_all) * len(timed) / len(diag)
     lm = sum(lm_d) * len(timed) / len(diag)
-    med = {"lmhead_topk_plus_build_tree": round(float(np.median(ab_all)) * 1e3, 2),
+    med = {"round": round(float(np.median(round_all)) * 1e3, 2),
+           "lmhead_topk_plus_build_tree": round(float(np.median(ab_all)) * 1e3, 2),
            "lmhead_topk": round(float(np.median(lm_d)) * 1e3, 2), "build_tree": round(float(np.median(bd_d)) * 1e3, 2),
            "verify": round(float(np.median(vf_all)) * 1e3, 2)}
+    med["tree_and_verify_on_top_of_lmhead"] = round(med["round"] - med["lmhead_topk"], 2)
     steps = args.steps
     value = whole_job_rate(steps, ws, total_ms)
     acc = acc_buf[args.warmup:].float().cpu().numpy()
@@ -434,8 +466,9 @@ def run_gpu(args, ws, rank, local):
                    "lm_head_weight": "packed once before timing (%s), streamed by %s"
                                      % ("mfd_lmhead_pack_fp8" if head.fp8 else "mfd_lmhead_pack", head.name),
                    "l2": "inputs larger than L2 (W = %.0f MB streamed every round)" % (head.weight_bytes / 1e6),
-                   "timing": "sum over the timed rounds of two CUDA-event intervals per round, one around the LM head and the tree (back to back, as in a real round) and one around the verification, with the queue kept ahead of the GPU; the target plant (input generation that needs the round's tree) is untimed; the per-stage split comes from separate diagnostic rounds"},
-        "stages_us": {"lmhead_topk_plus_build_tree": round(ab / steps * 1e3, 2), "verify": round(vf / steps * 1e3, 2),
+                   "timing": "sum over the timed rounds of one CUDA-event interval per round around the LM head, the tree and the walk, back to back as a round runs, with the queue kept ahead of the GPU; the target rows are planted beforehand (untimed) from an untimed pass's trees, which the timed rounds are checked to rebuild exactly; the per-stage split (LM head, tree, walk alone) comes from separate diagnostic rounds"},
+        "stages_us": {"round": round(sum(round_all) / steps * 1e3, 2),
+                      "lmhead_topk_plus_build_tree": round(ab / steps * 1e3, 2), "verify": round(vf / steps * 1e3, 2),
                       "split_from_diagnostic_rounds": {"lmhead_topk": round(sum(lm_d) / len(diag) * 1e3, 2),
                                                        "build_tree": round(sum(bd_d) / len(diag) * 1e3, 2),
                                                        "rounds": len(diag)}},
@@ -561,19 +594,43 @@ def run_gpu_batched(args, ws, rank, local):
                 flat[sites[i]] = base
                 acc_buf[i].copy_(rd.accept_len)
 
+    # timed rounds: LM head, trees and walks back to back in one interval,
+    # the target rows planted beforehand from an untimed pass's trees
+    ev_r = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_rounds)]
+    trees_r = {k: torch.empty_like(v) for k, v in trees.items()}
+
+    def phase_round(idx, sites):
+        for c0 in range(0, len(idx), CHUNK):
+            ahead(len(idx[c0:c0 + CHUNK]))
+            for i in idx[c0:c0 + CHUNK]:
+                tb = noise[i % 2]
+                flat = tb.view(-1)
+                base = flat[sites[i]]
+                flat[sites[i]] = base + 10.0
+                h_cur.copy_(h_all[i % n_distinct])
+                r0, r1 = ev_r[i]
+                r0.record(stream)
+                rd.lmhead_topk_packed(h_cur, Wp)
+                rd.build_tree()
+                rd.verify(tb, temp, seeds[i % n_distinct])
+                r1.record(stream)
+                flat[sites[i]] = base
+                acc_buf[i].copy_(rd.accept_len)
+                for k in trees_r:
+                    trees_r[k][i].copy_(getattr(rd, k))
+
     warm = list(range(args.warmup))
     timed = list(range(args.warmup, n_rounds))
     phase_a(warm)
     phase_b(warm, plant_sites_of(warm))
+    phase_a(timed)  # untimed: the trees the plant needs
     torch.cuda.synchronize()
+    sites_t = plant_sites_of(timed)
     barrier(ws)
     torch.cuda.synchronize()
     clocks = Clocks(local)
     time.sleep(0.2)
-    phase_a(timed)
-    torch.cuda.synchronize()
-    sites_t = plant_sites_of(timed)
-    phase_b(timed, sites_t)
+    phase_round(timed, sites_t)
     torch.cuda.synchronize()
     barrier(ws)
     torch.cuda.synchronize()
@@ -581,12 +638,17 @@ def run_gpu_batched(args, ws, rank, local):
     st = int(rd.status.item())
     if st != 0:
         raise RuntimeError(f"device status {st}: {mfd.status_string(st)}")
-    ab = sum(ev[i][0].elapsed_time(ev[i][2]) for i in timed)
-    vf = sum(ev[i][3].elapsed_time(ev[i][4]) for i in timed)
-    total_ms = reduce_max(ab + vf, ws)
+    for k in trees:
+        if not torch.equal(trees[k][timed], trees_r[k][timed]):
+            raise RuntimeError(f"the timed rounds built other trees ({k}) than the untimed pass")
+    round_all = [ev_r[i][0].elapsed_time(ev_r[i][1]) for i in timed]
+    total_ms = reduce_max(sum(round_all), ws)
+    ab = sum(ev[i][0].elapsed_time(ev[i][2]) for i in timed)  # untimed pass: LM head + trees
     diag = timed[:min(len(timed), 50)]
     phase_a(diag, split=True)
+    phase_b(diag, sites_t)
     torch.cuda.synchronize()
+    vf = sum(ev[i][3].elapsed_time(ev[i][4]) for i in diag) * len(timed) / len(diag)
     lm_d = [ev[i][0].elapsed_time(ev[i][1]) for i in diag]
     bd_d = [ev[i][1].elapsed_time(ev[i][2]) for i in diag]
     steps = args.steps
@@ -623,16 +685,17 @@ def run_gpu_batched(args, ws, rank, local):
                    "lm_head_weight": "packed once before timing (mfd_lmhead_pack), streamed by mfd_lmhead_topk_packed",
                    "l2": "inputs larger than L2 (W = %.0f MB; %d distinct hidden-state batches of %.1f MB cycled)"
                          % (V * H * 2 / 1e6, n_distinct, R * H * 2 / 1e6),
-                   "timing": "as the single-request workload: one CUDA-event interval around the LM head and the "
-                             "trees, one around the walks, summed over the timed rounds; split from diagnostic rounds"},
+                   "timing": "as the single-request workload: one CUDA-event interval per round around the LM "
+                             "head, the trees and the walks, summed over the timed rounds; split from diagnostic rounds"},
         "requests_per_s": round(value * n_req, 1),
-        "stages_us": {"lmhead_topk_plus_build_tree": round(ab / steps * 1e3, 2), "verify": round(vf / steps * 1e3, 2),
+        "stages_us": {"round": round(sum(round_all) / steps * 1e3, 2),
+                      "lmhead_topk_plus_build_tree": round(ab / steps * 1e3, 2), "verify": round(vf / steps * 1e3, 2),
                       "split_from_diagnostic_rounds": {"lmhead_topk": round(lm_us, 2),
                                                        "build_tree": round(sum(bd_d) / len(diag) * 1e3, 2),
                                                        "rounds": len(diag)}},
         "mean_accept_len": accept,
         "roofline": roof,
-        "gpu_launches": 4 * steps,
+        "gpu_launches": (5 if R <= 128 and R * H * 2 <= 144 * 1024 else 4) * steps,  # + the staged hidden rows
         "clocks": ck,
         "e2e": None,
         "e2e_note": "measured on the single-request workload only",
