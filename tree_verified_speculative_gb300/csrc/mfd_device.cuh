@@ -238,13 +238,15 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------- misc
-// A block barrier that every warp reaches with all 32 lanes together.
-// __syncthreads is an aligned barrier; a warp whose lanes come to it apart
-// (after a loop of per-lane trip counts, or a branch taken by one lane) first
-// reconverges here.
+// A block barrier that counts every thread by itself: the non-aligned
+// barrier.sync, which lanes of one warp may reach apart.  (Measured with the
+// aligned form, __syncthreads after a __syncwarp: a lane that had just taken
+// a branch of its own left the barrier when its warp's first lanes arrived,
+// before the other warps did.)  The __syncwarp still orders the warp's own
+// shared-memory accesses.
 __device__ __forceinline__ void block_sync() {
   __syncwarp();
-  __syncthreads();
+  asm volatile("barrier.sync 0;" ::: "memory");
 }
 
 // fp32 -> uint32 key whose ascending order is the float's DESCENDING order;
