@@ -346,6 +346,20 @@ int mfd_tree_analytics(const int32_t *parent, const int32_t *token, const int32_
 #define MFD_MFDD_SWITCH_REQUESTS 3
 int mfd_mfdd_modes(int n_req, int K);
 
+/* Fault injection for the LM head's bounded waits, for tests (the pages have
+ * no counterpart: it exists so that the kernel's timeout path can be
+ * exercised without faulting or hanging a GPU).  Arguments and outputs as
+ * mfd_lmhead_topk_packed; every CTA's producer stops after the CTA's first
+ * weight tile, so the MMA warp's next wait gives up after the kernel's wait
+ * limit (1 s): it stores MFD_ERR_TIMEOUT in *status and raises the CTA's
+ * abort flag, the epilogue warps leave their waits, the MMAs already issued
+ * drain, tensor memory is released and every CTA returns.  The outputs are
+ * then not meaningful; the next call on the same buffers is exact.  Errors:
+ * those of mfd_lmhead_topk_packed. */
+int mfd_lmhead_withheld_test(const void *h, int R, int H, const void *W_packed, int V, int topk,
+                             float *tk_logp, int32_t *tk_tok, float *lse, int32_t *status, void *ws,
+                             size_t ws_bytes, mfd_stream_t stream);
+
 /* Fault injection for the walk's bounded waits, for tests (the pages have no
  * counterpart: it exists so that the timeout path can be exercised without
  * faulting or hanging a GPU).  Arguments and outputs as mfd_verify, always

@@ -113,6 +113,35 @@ def test_staged_hidden_rows_match_unstaged(head_2560, R):
             np.testing.assert_array_equal(a, b)
 
 
+def test_lmhead_bounded_wait_runs_out_and_next_call_is_exact(head_2560):
+    """The LM head's pipeline waits are bounded: with the producers stopped
+    after each CTA's first tile (the library's fault-injection entry point),
+    the MMA warp's wait runs out, the call ends with MFD_ERR_TIMEOUT instead
+    of hanging, every CTA returns (the stream synchronises), and the next
+    ordinary call on the same buffers gives the earlier results bit for bit."""
+    W, Wd = head_2560
+    Wp = mfd.pack_lm_head(Wd)
+    h = synth.round_inputs(W, 8, 15, 11, seed=72).h.cuda()
+    rd = mfd.Round(1, 8, 15, 16, 1, 151936)
+    rd.status.zero_()
+    rd.lmhead_topk_packed(h, Wp)
+    torch.cuda.synchronize()
+    assert status_of(rd) == 0
+    ref = (np_(rd.tk_tok).copy(), np_(rd.tk_logp).view(np.uint32).copy(), np_(rd.lse).view(np.uint32).copy())
+    for attempt in range(2):
+        rd.status.zero_()
+        mfd.mfd_lmhead_withheld_test(h, Wp, 151936, 16, rd.tk_logp, rd.tk_tok, rd.lse, rd.status, rd.ws)
+        torch.cuda.synchronize()
+        assert status_of(rd) == mfd.MFD_ERR_TIMEOUT
+        rd.status.zero_()
+        rd.lmhead_topk_packed(h, Wp)
+        torch.cuda.synchronize()
+        assert status_of(rd) == 0
+        np.testing.assert_array_equal(np_(rd.tk_tok), ref[0])
+        np.testing.assert_array_equal(np_(rd.tk_logp).view(np.uint32), ref[1])
+        np.testing.assert_array_equal(np_(rd.lse).view(np.uint32), ref[2])
+
+
 def test_lmhead_pages_shape_sampled_rows(head_2560):
     """K=8, L=15, H=2560, V=151936, top-k 16, planted futures (11 of 15
     shared): all 120 rows through the kernel, 24 of them checked against the

@@ -102,6 +102,7 @@ struct Params {
   const uint8_t *w_packed;  // packed weight (see pack_w_kernel), or null
   const float *row_scale;   // FP8: t_r per hidden row [R]
   const float *w_amax;      // FP8: the weight's largest magnitude (s_W = w_amax / 448)
+  int withhold;             // fault injection for tests: the producer stops after each CTA's first tile
 };
 
 // Work item -> (M tile, vocabulary tiles [t0, t1), range); items are
@@ -238,11 +239,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t pol_h = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_par = 0;
-      bool ok = true;
-      for (int item = cta0; item < p.n_items && ok; item += ncta) {
+      bool ok = true, stop = false;
+      for (int item = cta0; item < p.n_items && ok && !stop; item += ncta) {
         int mt, t0, t1, range;
         item_range(p, item, mt, t0, t1, range);
         for (int t = t0; t < t1 && ok; ++t) {
+          if (p.withhold && (t > t0 || item != cta0)) {
+            // fault injection: nothing more is loaded, so the MMA warp's next
+            // wait runs out and the CTA takes its timeout path
+            stop = true;
+            break;
+          }
           if (p.n_mt > 1) {
             // Every M tile of a range reads the same weight tiles at about
             // the same time, so a weight tile missing in L2 stalls them all.
@@ -645,6 +652,7 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
   p.w_packed = static_cast<const uint8_t *>(L.w_packed);
   p.row_scale = L.row_scale;
   p.w_amax = L.w_amax;
+  p.withhold = L.withhold ? 1 : 0;
   cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<T, PACKED, FP8, BN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<BN>());
   if (e != cudaSuccess) return e;

@@ -20,6 +20,7 @@ struct LmheadLaunch {
   bool fp8 = false;                 // E4M3 packed weight (lmhead_packed_fp8_bytes), tmap_h over E4M3 rows
   const float *row_scale = nullptr;  // FP8: t_r per hidden row
   const float *w_amax = nullptr;     // FP8: the weight's largest magnitude (in the packed buffer's trailer)
+  bool withhold = false;             // fault injection for tests of the bounded waits
 };
 
 int lmhead_tile_rows(int R);  // vocabulary rows per tile for R hidden rows (128 for one M tile, else 256)

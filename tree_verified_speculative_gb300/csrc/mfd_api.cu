@@ -304,7 +304,7 @@ namespace {
 // vocabulary ids vocab_ids[0..V), increasing, below V_full)
 int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int V, int topk, float *tk_logp,
                 int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes, mfd_stream_t stream,
-                const int32_t *vocab_ids = nullptr, int V_full = 0, bool fp8 = false) {
+                const int32_t *vocab_ids = nullptr, int V_full = 0, bool fp8 = false, bool withhold = false) {
   if (!h || (!W && !Wp) || !tk_logp || !tk_tok || !status || R < 1 || H < 1 || V < 1 || topk < 1)
     return MFD_ERR_INVALID_ARG;
   if (!aligned(h, 16) || (W && !aligned(W, 16)) || (Wp && !aligned(Wp, 256))) return MFD_ERR_INVALID_ARG;
@@ -349,6 +349,7 @@ int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int 
   L.part_ms = base;
   L.part_cand = base + y.ms_bytes;
   L.status = status;
+  L.withhold = withhold;
   if (fp8) {
     L.fp8 = true;
     L.row_scale = reinterpret_cast<const float *>(base + f8.sc_off);
@@ -405,6 +406,14 @@ int mfd_lmhead_topk_packed(const void *h, int R, int H, const void *W_packed, in
                            mfd_stream_t stream) {
   if (!W_packed) return MFD_ERR_INVALID_ARG;
   return lmhead_call(h, R, H, nullptr, W_packed, V, topk, tk_logp, tk_tok, lse, status, ws, ws_bytes, stream);
+}
+
+int mfd_lmhead_withheld_test(const void *h, int R, int H, const void *W_packed, int V, int topk, float *tk_logp,
+                             int32_t *tk_tok, float *lse, int32_t *status, void *ws, size_t ws_bytes,
+                             mfd_stream_t stream) {
+  if (!W_packed) return MFD_ERR_INVALID_ARG;
+  return lmhead_call(h, R, H, nullptr, W_packed, V, topk, tk_logp, tk_tok, lse, status, ws, ws_bytes, stream,
+                     nullptr, 0, false, true);
 }
 
 size_t mfd_lmhead_packed_fp8_bytes(int V, int H) {

@@ -37,7 +37,7 @@ MFD_NODE_ON_FUTURE, MFD_NODE_CHIMERA, MFD_NODE_OTHER = 0, 1, 2
 EXPORTS = ("mfd_status_string", "mfd_workspace_size", "mfd_lmhead_topk", "mfd_lmhead_packed_bytes",
            "mfd_lmhead_pack", "mfd_lmhead_topk_packed", "mfd_lmhead_topk_subset", "mfd_logits_topk",
            "mfd_logits_topk_noalloc",
-           "mfd_build_tree", "mfd_verify", "mfd_verify_withheld_test", "mfd_mfdd_modes",
+           "mfd_build_tree", "mfd_verify", "mfd_verify_withheld_test", "mfd_lmhead_withheld_test", "mfd_mfdd_modes",
            "mfd_lmhead_packed_fp8_bytes", "mfd_lmhead_pack_fp8", "mfd_fp8_quantize_rows",
            "mfd_lmhead_fp8_workspace_bytes", "mfd_lmhead_topk_fp8", "mfd_tree_analytics")
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -91,6 +91,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.mfd_lmhead_pack.restype = I
         lib.mfd_lmhead_topk_packed.argtypes = [P, I, I, P, I, I, P, P, P, P, P, SZ, P]
         lib.mfd_lmhead_topk_packed.restype = I
+        lib.mfd_lmhead_withheld_test.argtypes = [P, I, I, P, I, I, P, P, P, P, P, SZ, P]
+        lib.mfd_lmhead_withheld_test.restype = I
         lib.mfd_lmhead_topk_subset.argtypes = [P, I, I, P, I, P, I, I, P, P, P, P, P, SZ, P]
         lib.mfd_lmhead_topk_subset.restype = I
         lib.mfd_logits_topk.argtypes = [P, I, I, I, P, P, P, P, P, SZ, P]
@@ -232,6 +234,17 @@ def mfd_lmhead_topk_packed(h, W_packed, V, topk, tk_logp, tk_tok, lse, status, w
     rc = load().mfd_lmhead_topk_packed(_p(h), R, H, _p(W_packed), V, topk, _p(tk_logp), _p(tk_tok), _p(lse),
                                        _p(status), _p(ws), ws.numel() * ws.element_size(), _s(stream))
     _check(rc, "mfd_lmhead_topk_packed")
+
+
+def mfd_lmhead_withheld_test(h, W_packed, V, topk, tk_logp, tk_tok, lse, status, ws, stream=None) -> None:
+    """mfd_lmhead_topk_packed with the fault injection of its C entry point:
+    the producers stop after the first tile, so the kernel's bounded wait
+    runs out (*status = MFD_ERR_TIMEOUT after about a second)."""
+    R, H = h.shape
+    assert h.dtype == torch.bfloat16
+    rc = load().mfd_lmhead_withheld_test(_p(h), R, H, _p(W_packed), V, topk, _p(tk_logp), _p(tk_tok), _p(lse),
+                                         _p(status), _p(ws), ws.numel() * ws.element_size(), _s(stream))
+    _check(rc, "mfd_lmhead_withheld_test")
 
 
 def mfd_lmhead_packed_fp8_bytes(V: int, H: int) -> int:
