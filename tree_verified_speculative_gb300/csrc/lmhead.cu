@@ -129,12 +129,15 @@ __device__ __forceinline__ const uint8_t *packed_at(const uint8_t *w, int t, int
 // the b's are true up to x's place and false after it, so entry s keeps its
 // place when b[s], takes (x, v) when b[s - 1] alone holds, and takes entry
 // s - 1 otherwise: T independent compares and two selects per entry, with no
-// position to count or compare.
+// position to count or compare.  A row's columns come in increasing id
+// order, so every listed id is below v (the empty list's entries are -inf,
+// which x beats): entry s stays before (x, v) exactly when its value is at
+// least x, one compare.
 template <int T>
 __device__ __forceinline__ void topk_insert(float (&tv)[T], int (&ti)[T], float x, int v) {
   bool b[T];
 #pragma unroll
-  for (int s = 0; s < T; ++s) b[s] = vi_before(tv[s], ti[s], x, v);
+  for (int s = 0; s < T; ++s) b[s] = tv[s] >= x;
 #pragma unroll
   for (int s = T - 1; s > 0; --s) {  // tv[s - 1] is still the old entry here
     tv[s] = b[s] ? tv[s] : (b[s - 1] ? x : tv[s - 1]);
