@@ -106,8 +106,19 @@ size_t mfd_workspace_size(int op, int n_req, int K, int L, int topk, int B, int 
  * thread-safe.  Hidden rows that span 144 KB or less (R * H * 2 bytes) are
  * first copied into ws, padded with zero rows: every CTA reads them, and on
  * GB300 rows within so few bytes of address space are served by few L2
- * slices.  The copy changes no result.  Errors: INVALID_ARG (NULL, R < 1,
- * misaligned h/W), UNSUPPORTED (limits, device), WORKSPACE, CUDA. */
+ * slices.  The copy changes no result.  With R <= 128 the vocabulary
+ * ranges also share, through ws, a lower bound on each row's topk-th best
+ * logit (the smallest of topk per-residue-class maxima of published
+ * candidates, token id mod topk), and a range skips a column below it; the
+ * bound changes no result.  ws needs no zeroing for it: its first 16 bytes
+ * hold a generation word and a ready word, each call advances the
+ * generation, clears the bound and only then stores ready = the splitmix64
+ * finalizer of the new generation, and the CTAs trust the bound only after
+ * they read that value.  Contents left by other calls are mistaken for a
+ * cleared bound only if the ready word already equals that value, which
+ * fresh, zeroed or pattern-filled memory does not hold.  Errors: INVALID_ARG
+ * (NULL, R < 1, misaligned h/W), UNSUPPORTED (limits, device), WORKSPACE,
+ * CUDA. */
 int mfd_lmhead_topk(const void *h, int R, int H, const void *W, int V, int topk,
                     float *tk_logp, int32_t *tk_tok, float *lse, int32_t *status, void *ws,
                     size_t ws_bytes, mfd_stream_t stream);

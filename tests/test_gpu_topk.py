@@ -349,3 +349,76 @@ def test_lmhead_ties_duplicate_rows(packed):
             assert list(o_tok[r, :len(want)]) == want, (gi, r, o_tok[r])
             assert list(g_tok[r, :len(want)]) == want, (gi, r, g_tok[r])
             assert len(set(g_lp[r, :len(want)].view(np.uint32).tolist())) == 1
+
+
+def _splitmix64_finalizer(z: int) -> int:
+    """The published splitmix64 finalizer (Steele, Lea, Flood, OOPSLA'14)."""
+    m = (1 << 64) - 1
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & m
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & m
+    return z ^ (z >> 31)
+
+
+def test_row_bound_stale_and_foreign_scratch(head_2560):
+    """At one M tile the ranges share a per-row bound on the row's k-th best
+    logit through the workspace (a column below it cannot reach the top-k).
+    The bound must never outlive its call: scratch filled with a large
+    pattern before the first call, and a call with logits 16x larger before
+    an ordinary one on the same scratch, leave the ordinary call's tables
+    bit-identical to those of a fresh workspace.  Each call advances the
+    generation word at the start of the scratch by one and leaves the ready
+    word at the splitmix64 finalizer of the new generation."""
+    W, Wd = head_2560
+    Wp = mfd.pack_lm_head(Wd)
+    h = synth.round_inputs(W, 8, 15, 11, seed=73).h.cuda()
+
+    def run(rd, x):
+        rd.status.zero_()
+        rd.lmhead_topk_packed(x, Wp)
+        torch.cuda.synchronize()
+        assert status_of(rd) == 0
+        return np_(rd.tk_tok).copy(), np_(rd.tk_logp).view(np.uint32).copy(), np_(rd.lse).view(np.uint32).copy()
+
+    fresh = mfd.Round(1, 8, 15, 16, 1, 151936)
+    fresh.ws.zero_()
+    ref = run(fresh, h)
+    rd = mfd.Round(1, 8, 15, 16, 1, 151936)
+    rd.ws.view(torch.uint8).fill_(0x7F)
+    for got in (run(rd, h), (run(rd, (h.float() * 16).to(torch.bfloat16)), run(rd, h))[1]):
+        for a, b in zip(got, ref):
+            np.testing.assert_array_equal(a, b)
+    words = rd.ws.view(torch.uint8)[:16].cpu().numpy().view(np.uint64)
+    gen, ready = int(words[0]), int(words[1])
+    run(rd, h)
+    words = rd.ws.view(torch.uint8)[:16].cpu().numpy().view(np.uint64)
+    assert int(words[0]) == (gen + 1) % (1 << 64)
+    assert int(words[1]) == _splitmix64_finalizer(int(words[0]))
+    assert ready == _splitmix64_finalizer(gen)
+
+
+@pytest.mark.parametrize("packed,topk", [(False, 2), (True, 2), (True, 8)])
+def test_row_bound_every_logit_tied(packed, topk):
+    """A weight of one repeated row gives every column of a hidden row the
+    same logit.  Range heads never change then (a later column never beats
+    an equal one), so with top-2 both residue classes of the row bound get
+    that value and the bound equals every value it gates; with top-8 classes
+    stay empty and the bound stays -inf.  Either way the top-k must be token
+    ids 0..k-1 in order, each with log p = -log V."""
+    V, H = 20000, 128
+    rng = np.random.default_rng(5)
+    row = (rng.standard_normal(H) / np.sqrt(H)).astype(np.float32)
+    W = synth.bf16_round(np.tile(row, (V, 1)))
+    h = synth.bf16_round(rng.standard_normal((37, H)).astype(np.float32))
+    rd = mfd.Round(1, 1, 37, topk, 1, V)
+    rd.status.zero_()
+    if packed:
+        rd.lmhead_topk_packed(h.cuda(), mfd.pack_lm_head(W.cuda()))
+    else:
+        rd.lmhead_topk(h.cuda(), W.cuda())
+    torch.cuda.synchronize()
+    assert status_of(rd) == 0
+    tok, lp = np_(rd.tk_tok), np_(rd.tk_logp)
+    assert (tok == np.arange(topk)[None, :]).all()
+    np.testing.assert_allclose(lp, -np.log(V), atol=1e-4)
+    o_lp, o_tok, _ = oracle.lmhead_topk(_bits(h), _bits(W), topk)
+    assert (o_tok == np.arange(topk)[None, :]).all()

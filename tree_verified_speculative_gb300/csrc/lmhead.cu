@@ -29,8 +29,9 @@
 // HBM about once and from L2 for the other M tiles.  Every CTA loads only
 // into its own shared memory.
 //
-// Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer (one
-// thread each), warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4)..).
+// Roles (224 threads): warp 0 = TMA producer, warp 1 = MMA issuer (one
+// thread each), warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4)..),
+// warp 6 = the row bound's upkeep (one M tile; see the row bound below).
 // TMEM holds four 128-column fp32 accumulators, so that the MMAs can run up
 // to three tiles ahead of the epilogue: the epilogue of a range's first tile,
 // where the row's top-T fills and most columns enter it, takes longer than a
@@ -62,7 +63,7 @@ constexpr int KSUB = 1;           // K atoms per pipeline stage
 constexpr int A_SUB = BM * BK * 2;  // one K atom of the hidden tile
 constexpr int PK_SUB = PK * BK * 2;  // one K atom of a packed block
 constexpr int A_BYTES = KSUB * A_SUB;
-constexpr int THREADS = 192;
+constexpr int THREADS = 224;
 constexpr int TMEM_COLS = 512;
 
 // Tile shape.  BN = 128 vocabulary rows (one M tile, the weight stream
@@ -87,7 +88,75 @@ template <int BN>
 constexpr int smem_bytes() {
   using TL = Tile<BN>;
   return 1024 /* alignment slack */ + TL::STAGES * TL::STAGE_BYTES + 4 * STAGE_ROW_BYTES +
-         8 * (2 * TL::STAGES + 2 * TL::NACC + 1) + 16;
+         8 * (2 * TL::STAGES + 2 * TL::NACC + 1) + 16 + 4 * BM + 16;
+}
+
+// Row bound (one M tile).  A column below the row's k-th best logit over the
+// whole vocabulary cannot reach the row's top-k, so a range need not insert
+// it.  Such a bound: split the vocabulary ids into G = k residue classes
+// (id mod k) and let every range publish its list's first two entries into
+// their classes' slots (an integer max of the value's order key); the
+// smallest of the k class maxima is then the value of k distinct columns at
+// least, so at most the k-th best.  A range inserts a column only if it
+// beats both its own T-th entry and that bound; every column of the final
+// top-k still enters its range's list, and the lists stay real, sorted
+// candidates, which is all the merge needs.  The slots live in the
+// workspace, cleared per call by CTA 0 behind a generation handshake (the
+// same scheme as the verify walk's): every CTA reads gen, expects
+// ready == mix(gen + 1), and trusts the slots only after seeing that;
+// CTA 0 clears them, stores ready with release semantics, and writes
+// gen + 1 into gen when it leaves.  A seventh warp keeps this CTA's copy of
+// the bounds (shared memory) current; publications need no handshake, since
+// a clear can only lose one, never make one wrong.
+constexpr int KEY_NEG_INF = (int)0x807FFFFF;  // ord_key(-inf)
+constexpr int RB_READY_POLLS = 1 << 16;       // x ~128 ns before a CTA gives up on the bound
+constexpr int RB_PASSES = 1 << 22;
+constexpr unsigned RB_SLEEP_NS = 256;
+constexpr int RB_BATCH = 8;  // 16-byte slot loads a lane has in flight at once
+
+// float -> int whose signed order is the float's order (-0.0 just below +0.0)
+__device__ __forceinline__ int ord_key(float f) {
+  const int b = __float_as_int(f);
+  return b >= 0 ? b : b ^ 0x7FFFFFFF;
+}
+__device__ __forceinline__ float ord_val(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7FFFFFFF); }
+// the largest float below g (-inf for -inf), so that x >= g is x > below(g)
+// for every non-NaN x; denormals are compared as they are (no flush to zero)
+__device__ __forceinline__ float below(float g) {
+  if (!(g > -INFINITY)) return -INFINITY;
+  if (g == 0.f) return __int_as_float((int)0x80000001);
+  const int b = __float_as_int(g);
+  return __int_as_float(g > 0.f ? b - 1 : b + 1);
+}
+
+// splitmix64's finalizer (Steele, Lea, Flood, OOPSLA'14): a bijection, so
+// distinct generations give distinct ready words
+__device__ __forceinline__ unsigned long long mix64(unsigned long long z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ int4 ld_relaxed_v4(const int *p) {
+  int4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_max(int *p, int v) {
+  asm volatile("red.relaxed.gpu.global.max.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 struct Params {
@@ -103,6 +172,9 @@ struct Params {
   const float *row_scale;   // FP8: t_r per hidden row [R]
   const float *w_amax;      // FP8: the weight's largest magnitude (s_W = w_amax / 448)
   int withhold;             // fault injection for tests: the producer stops after each CTA's first tile
+  int *rb;                  // row bound (one M tile): int [R][T] class maxima (order keys), or null
+  unsigned long long *rb_gen, *rb_ready;
+  int G;                    // residue classes of the row bound (the top-k)
 };
 
 // Work item -> (M tile, vocabulary tiles [t0, t1), range); items are
@@ -195,6 +267,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *never = abort_flag + 1;
+  volatile int *epi_left = never + 1;  // epilogue warps still running
+  volatile float *bnd_s = reinterpret_cast<volatile float *>(epi_left + 1);  // row bounds [BM]
+  volatile int *rb_stop = reinterpret_cast<volatile int *>(bnd_s + BM);     // upkeep may stop
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -213,6 +288,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
     *never = 0;
+    *epi_left = 4;
+    *rb_stop = 0;
     fence_mbar_init();
     prefetch_tmap(&tmap_h);
     if (!PACKED) prefetch_tmap(&tmap_w);
@@ -221,6 +298,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
+  if (warp == 6)
+    for (int i = lane; i < BM; i += 32) bnd_s[i] = -INFINITY;
   tc_fence_before();
   block_sync();
   tc_fence_after();
@@ -373,6 +452,69 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(drain, 0, never);
     }
     __syncwarp();  // as the producer warp: reconverge before the block barrier
+  } else if (warp == 6) {
+    // ------------------------------------------------------ row bound
+    if (p.rb) {
+      const unsigned long long G = __shfl_sync(0xffffffffu, ld_relaxed_u64(p.rb_gen), 0) + 1ull;
+      const unsigned long long want = mix64(G);
+      if (cta0 == 0) {
+        for (int i = lane; i < p.R * T; i += 32) p.rb[i] = KEY_NEG_INF;
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          st_release_u64(p.rb_ready, want);
+        }
+        __syncwarp();
+      }
+      // loop conditions are taken by lane 0 for the whole warp (the loops
+      // hold full-warp shuffles)
+      auto running = [&]() { return __shfl_sync(0xffffffffu, (int)(!*abort_flag && !*rb_stop && *epi_left > 0), 0) != 0; };
+      bool trusted = false;
+      for (int it = 0; it < RB_READY_POLLS && running(); ++it) {
+        trusted = __all_sync(0xffffffffu, ld_relaxed_u64(p.rb_ready) == want);
+        if (trusted) break;
+        __nanosleep(128);
+      }
+      if (trusted) {
+        __threadfence();  // every lane saw the ready word: its later loads see the clear
+        // A pass reads the slots as 16-byte words, RB_BATCH of them in flight
+        // per lane: word i holds classes 4 (i mod T/4) .. + 3 of row
+        // i div (T/4), so the T/4 lanes of one row reduce by shuffles.
+        constexpr int QR = T / 4;
+        const int nq = p.R * QR;
+        const int c4 = 4 * (lane % QR);
+        for (int pass = 0; pass < RB_PASSES && running(); ++pass) {
+          for (int i0 = 0; i0 < nq && running(); i0 += 32 * RB_BATCH) {
+            int4 q[RB_BATCH];
+#pragma unroll
+            for (int k = 0; k < RB_BATCH; ++k) {
+              const int i = i0 + 32 * k + lane;
+              q[k] = i < nq ? ld_relaxed_v4(p.rb + 4 * (size_t)i) : make_int4(0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF);
+            }
+#pragma unroll
+            for (int k = 0; k < RB_BATCH; ++k) {
+              int m = 0x7FFFFFFF;
+              m = c4 + 0 < p.G ? min(m, q[k].x) : m;
+              m = c4 + 1 < p.G ? min(m, q[k].y) : m;
+              m = c4 + 2 < p.G ? min(m, q[k].z) : m;
+              m = c4 + 3 < p.G ? min(m, q[k].w) : m;
+#pragma unroll
+              for (int o = 1; o < QR; o <<= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+              const int i = i0 + 32 * k + lane;
+              if (c4 == 0 && i < nq) {
+                const float b = ord_val(m);
+                if (b > bnd_s[i / QR]) bnd_s[i / QR] = b;
+              }
+            }
+          }
+          __nanosleep(RB_SLEEP_NS);
+        }
+      }
+      __syncwarp();
+      // every CTA read gen when it started; the next call takes G + 1
+      if (cta0 == 0 && lane == 0) st_relaxed_u64(p.rb_gen, G);
+    }
+    __syncwarp();
   } else {
     // --------------------------------------------------------- epilogue
     const int quarter = warp & 3;
@@ -397,7 +539,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         tv[s] = -INFINITY;
         ti[s] = 0x7FFFFFFF;
       }
+      int pub0 = -1, pub1 = -1;  // ids of entries 0 and 1 when last published
+      const bool pub_row = p.rb != nullptr && my_row < p.R;
+      int *rb_row = pub_row ? p.rb + (size_t)my_row * T : nullptr;
+      // publishes the list's first two entries when they have changed and
+      // beat the bound in use (a slot already holds at least the bound)
+      auto publish = [&]() {
+        if (!pub_row) return;
+        const float gb = bnd_s[row_in_tile];
+        if (ti[0] != pub0 && ti[0] != 0x7FFFFFFF && tv[0] > gb) red_max(rb_row + ti[0] % p.G, ord_key(tv[0]));
+        if (ti[1] != pub1 && ti[1] != 0x7FFFFFFF && tv[1] > gb) red_max(rb_row + ti[1] % p.G, ord_key(tv[1]));
+        pub0 = ti[0];
+        pub1 = ti[1];
+      };
       for (int t = t0; t < t1; ++t) {
+        // the bound changes little from here on: its upkeep ends now rather
+        // than hold up the CTA's exit with a pass in flight
+        if (t == t1 - 1 && item + ncta >= p.n_items) *rb_stop = 1;
         if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
           ok = false;
           break;
@@ -447,13 +605,15 @@ __global__ void __launch_bounds__(THREADS, 1)
               tv[s] = sv[s];
               ti[s] = si[s];
             }
+            publish();
             continue;
           }
           // Top-T: one bit per column that beats this row's current T-th
           // entry (a later column never ties its way in: its id is larger).
           // Only the set bits are visited, so the warp pays for the largest
           // candidate count among its 32 rows, not for every column.
-          const float thr = tv[T - 1];
+          // ... and is not below the row bound (x >= bound: x > below(bound))
+          const float thr = fmaxf(tv[T - 1], below(bnd_s[row_in_tile]));
           uint32_t cm = 0;
 #pragma unroll
           for (int j = 0; j < 32; ++j) cm |= (x[j] > thr ? 1u : 0u) << j;
@@ -469,6 +629,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (xv > tv[T - 1]) topk_insert<T>(tv, ti, xv, v0 + j);
               }
             }
+            publish();
           }
         }
         tc_fence_before();
@@ -493,6 +654,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!*abort_flag) report(p.status, MFD_ERR_TIMEOUT);
       *abort_flag = 1;
     }
+    __syncwarp();
+    if (lane == 0) atomicAdd(const_cast<int *>(epi_left), -1);
   }
 
   block_sync();
@@ -656,6 +819,11 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
   p.row_scale = L.row_scale;
   p.w_amax = L.w_amax;
   p.withhold = L.withhold ? 1 : 0;
+  const bool rb = L.rb != nullptr && p.n_mt == 1 && L.G >= 1 && L.G <= T;
+  p.rb = rb ? reinterpret_cast<int *>(static_cast<char *>(L.rb) + 256) : nullptr;
+  p.rb_gen = rb ? static_cast<unsigned long long *>(L.rb) : nullptr;
+  p.rb_ready = rb ? static_cast<unsigned long long *>(L.rb) + 1 : nullptr;
+  p.G = rb ? L.G : 0;
   cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel<T, PACKED, FP8, BN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<BN>());
   if (e != cudaSuccess) return e;
@@ -678,6 +846,7 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
 }  // namespace
 
 int lmhead_tile_rows(int R) { return R <= BM ? 128 : 256; }
+size_t lmhead_bound_bytes(int R, int T) { return R <= BM ? 256 + ((size_t)R * T * 4 + 255) / 256 * 256 : 0; }
 int lmhead_m_rows() { return BM; }
 int lmhead_k_chunk() { return BK; }
 

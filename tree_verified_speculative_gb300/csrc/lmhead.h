@@ -21,8 +21,15 @@ struct LmheadLaunch {
   const float *row_scale = nullptr;  // FP8: t_r per hidden row
   const float *w_amax = nullptr;     // FP8: the weight's largest magnitude (in the packed buffer's trailer)
   bool withhold = false;             // fault injection for tests of the bounded waits
+  // row bound (R <= 128): lmhead_bound_bytes(R, T) of scratch that no other
+  // launch touches while this one runs -- its generation and ready words,
+  // then the class maxima -- and G residue classes (the top-k, <= T); null:
+  // every range keeps its own top-T
+  void *rb = nullptr;
+  int G = 0;
 };
 
+size_t lmhead_bound_bytes(int R, int T);  // scratch of the row bound (0 when R > 128)
 int lmhead_tile_rows(int R);  // vocabulary rows per tile for R hidden rows (128 for one M tile, else 256)
 int lmhead_m_rows();     // hidden rows per M tile (128)
 int lmhead_k_chunk();    // K elements per pipeline stage (64)

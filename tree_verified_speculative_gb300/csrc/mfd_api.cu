@@ -106,6 +106,7 @@ struct TopkLayout {
   int P, T, chunk;
   size_t ms_bytes, cand_bytes, total;
   size_t stage_off = 0;  // LM head: room for the staged hidden rows (lmhead_hidden_stage)
+  size_t part_off = 0;   // LM head: the partials follow the row bound, which starts the scratch
 };
 
 // Fewest weight tiles for the busiest CTA when n_groups M tiles share
@@ -136,9 +137,12 @@ TopkLayout lmhead_layout(int R, int V, int topk, int n_sm) {
   if (n_mt > 1) best_ranges(tiles, n_mt, n_sm, &y.P);  // work items are (range, M tile)
   y.T = cand_width(topk);
   y.chunk = 0;
+  // the row bound's generation words sit at offset 0 for every shape, so a
+  // call of another shape finds them where the last one left them
+  y.part_off = mfd::lmhead_bound_bytes(R, y.T);
   y.ms_bytes = align256((size_t)R * y.P * 8);
   y.cand_bytes = align256((size_t)R * y.P * y.T * 8);
-  y.total = y.ms_bytes + y.cand_bytes;
+  y.total = y.part_off + y.ms_bytes + y.cand_bytes;
   // one M tile: room for the hidden rows staged when they span few bytes
   y.stage_off = y.total;
   if (R <= mfd::lmhead_m_rows()) y.total += align256(mfd::lmhead_stage_max_bytes());
@@ -346,10 +350,12 @@ int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int 
   L.T = y.T;
   L.P = y.P;
   L.n_sm = d.n_sm;
-  L.part_ms = base;
-  L.part_cand = base + y.ms_bytes;
+  L.part_ms = base + y.part_off;
+  L.part_cand = base + y.part_off + y.ms_bytes;
   L.status = status;
   L.withhold = withhold;
+  L.rb = y.part_off ? base : nullptr;
+  L.G = topk;
   if (fp8) {
     L.fp8 = true;
     L.row_scale = reinterpret_cast<const float *>(base + f8.sc_off);
