@@ -114,12 +114,6 @@ constexpr int RB_PASSES = 1 << 22;
 constexpr unsigned RB_SLEEP_NS = 256;
 constexpr int RB_BATCH = 8;  // 16-byte slot loads a lane has in flight at once
 
-// float -> int whose signed order is the float's order (-0.0 just below +0.0)
-__device__ __forceinline__ int ord_key(float f) {
-  const int b = __float_as_int(f);
-  return b >= 0 ? b : b ^ 0x7FFFFFFF;
-}
-__device__ __forceinline__ float ord_val(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7FFFFFFF); }
 // the largest float below g (-inf for -inf), so that x >= g is x > below(g)
 // for every non-NaN x; denormals are compared as they are (no flush to zero)
 __device__ __forceinline__ float below(float g) {
@@ -307,8 +301,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   static_assert(!FP8 || PACKED, "the FP8 weight is always packed");
   constexpr int KEL = FP8 ? BK8 : BK;  // K elements per stage
   const int nk = p.H / KEL;
-  // The prologue above may overlap the previous grid; global memory is
-  // touched only after it has finished.
+  if (PACKED && warp == 0 && lane == 0 && cta0 < p.n_items) {
+    // The weight is no product of the previous grid, so the first stages of
+    // this CTA's weight go to L2 while that grid finishes.  A prefetch moves
+    // nothing into the CTA: the loads below still read W after the wait.
+    int mt, t0, t1, range;
+    item_range(p, cta0, mt, t0, t1, range);
+    if (t0 < t1)
+      for (int kc = 0; kc < nk && kc < STAGES * KSUB; ++kc) bulk_prefetch_l2(packed_at<BN>(p.w_packed, t0, kc, nk), (uint32_t)B_SUB);
+  }
+  // The prologue above may overlap the previous grid; the CTA reads global
+  // memory only after it has finished.
   pdl_wait();
   pdl_launch_dependents();
 
@@ -819,8 +822,9 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
   p.row_scale = L.row_scale;
   p.w_amax = L.w_amax;
   p.withhold = L.withhold ? 1 : 0;
-  const bool rb = L.rb != nullptr && p.n_mt == 1 && L.G >= 1 && L.G <= T;
-  p.rb = rb ? reinterpret_cast<int *>(static_cast<char *>(L.rb) + 256) : nullptr;
+  const bool rb = L.rb != nullptr;
+  if (rb && !(p.n_mt == 1 && L.G >= 1 && L.G <= T)) return cudaErrorInvalidValue;
+  p.rb = rb ? reinterpret_cast<int *>(static_cast<char *>(L.rb) + LMHEAD_BOUND_HEADER) : nullptr;
   p.rb_gen = rb ? static_cast<unsigned long long *>(L.rb) : nullptr;
   p.rb_ready = rb ? static_cast<unsigned long long *>(L.rb) + 1 : nullptr;
   p.G = rb ? L.G : 0;
@@ -846,7 +850,9 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
 }  // namespace
 
 int lmhead_tile_rows(int R) { return R <= BM ? 128 : 256; }
-size_t lmhead_bound_bytes(int R, int T) { return R <= BM ? 256 + ((size_t)R * T * 4 + 255) / 256 * 256 : 0; }
+size_t lmhead_bound_bytes(int R, int T) {
+  return R <= BM ? LMHEAD_BOUND_HEADER + ((size_t)R * T * 4 + 255) / 256 * 256 : 0;
+}
 int lmhead_m_rows() { return BM; }
 int lmhead_k_chunk() { return BK; }
 

@@ -30,6 +30,7 @@ struct LmheadLaunch {
 };
 
 size_t lmhead_bound_bytes(int R, int T);  // scratch of the row bound (0 when R > 128)
+constexpr size_t LMHEAD_BOUND_HEADER = 256;  // generation and ready words; the class maxima follow
 int lmhead_tile_rows(int R);  // vocabulary rows per tile for R hidden rows (128 for one M tile, else 256)
 int lmhead_m_rows();     // hidden rows per M tile (128)
 int lmhead_k_chunk();    // K elements per pipeline stage (64)
@@ -74,6 +75,10 @@ struct MergeLaunch {
   // are written as vocab_ids[id] (ids in [0, V_full)); null: written as is
   const int32_t *vocab_ids;
   int V_sub, V_full;
+  // the LM head's row bound (int [R][T] class maxima as order keys, classes
+  // 0..G-1 used), or null: candidates below it cannot be in the top-k
+  const int *rb = nullptr;
+  int G = 0;
 };
 cudaError_t launch_merge_topk(const MergeLaunch &M, cudaStream_t stream);
 

@@ -376,6 +376,8 @@ int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int 
   M.vocab_ids = vocab_ids;
   M.V_sub = V;
   M.V_full = vocab_ids ? V_full : V;
+  M.rb = L.rb ? reinterpret_cast<const int *>(base + mfd::LMHEAD_BOUND_HEADER) : nullptr;
+  M.G = topk;
   return cuda_status(mfd::launch_merge_topk(M, s));
 }
 }  // namespace

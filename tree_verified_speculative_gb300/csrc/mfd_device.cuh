@@ -269,6 +269,14 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// float -> int whose signed order is the float's order (-0.0 just below
+// +0.0), and back
+__device__ __forceinline__ int ord_key(float f) {
+  const int b = __float_as_int(f);
+  return b >= 0 ? b : b ^ 0x7FFFFFFF;
+}
+__device__ __forceinline__ float ord_val(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7FFFFFFF); }
+
 // (value desc, index asc) "a before b"
 __device__ __forceinline__ bool vi_before(float av, int ai, float bv, int bi) {
   return av > bv || (av == bv && ai < bi);

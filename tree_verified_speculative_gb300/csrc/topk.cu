@@ -48,18 +48,23 @@ __device__ __forceinline__ Cand warp_best(Cand c) {
 //          two), and tau is the worst of the G group bests -- G distinct
 //          candidates, each at or before tau.  Nothing after tau can be in
 //          the top-k.
-//   top  = the survivors (each list's prefix at or before tau) ranked by
-//          counting how many survivors precede each one.
+//   top  = the survivors (each list's prefix at or before tau, and not below
+//          the LM head's row bound when there is one: the smallest of the
+//          k residue-class maxima its ranges published, the value of k
+//          distinct candidates or better) ranked by counting how many
+//          survivors precede each one.
 template <int T>
 __global__ void __launch_bounds__(MERGE_THREADS)
     merge_topk_kernel(const float2 *__restrict__ part_ms, const int2 *__restrict__ part_cand, int R, int P,
                       int topk, float *__restrict__ tk_logp, int32_t *__restrict__ tk_tok, float *__restrict__ lse_out,
-                      const int32_t *__restrict__ vocab_ids, int V_sub, int V_full, int32_t *status) {
+                      const int32_t *__restrict__ vocab_ids, int V_sub, int V_full, int32_t *status,
+                      const int *__restrict__ rb, int G_rb) {
   __shared__ Cand surv[SURV_CAP];
   __shared__ Cand top[32];
   __shared__ Cand gbest[MERGE_WARPS][32];
   __shared__ float red_m[MERGE_WARPS], red_s[MERGE_WARPS];
   __shared__ int n_surv_s;
+  __shared__ int bound_s;
   pdl_wait();
   pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -72,6 +77,16 @@ __global__ void __launch_bounds__(MERGE_THREADS)
     return cand_of(e.x, e.y);
   };
   if (tid == 0) n_surv_s = 0;
+  // the row bound's class maxima: T / 4 lanes of warp 0, one 16-byte word each
+  int bk = 0x7FFFFFFF;
+  if (rb && warp == 0 && lane < T / 4) {
+    const int4 q = __ldcg(reinterpret_cast<const int4 *>(rb + (size_t)row * T) + lane);
+    const int c4 = 4 * lane;
+    bk = c4 + 0 < G_rb ? min(bk, q.x) : bk;
+    bk = c4 + 1 < G_rb ? min(bk, q.y) : bk;
+    bk = c4 + 2 < G_rb ? min(bk, q.z) : bk;
+    bk = c4 + 3 < G_rb ? min(bk, q.w) : bk;
+  }
 
   // ---- (max, sum exp) and the first four candidates of each owned list, in
   // one round trip: a list rarely holds more than four of the row's top-k
@@ -117,6 +132,11 @@ __global__ void __launch_bounds__(MERGE_THREADS)
     red_s[warp] = ls;
   }
   if (lane < G) gbest[warp][lane] = g;
+  if (warp == 0) {
+#pragma unroll
+    for (int o = 1; o < T / 4; o <<= 1) bk = min(bk, __shfl_xor_sync(0xffffffffu, bk, o));
+    if (lane == 0) bound_s = bk;
+  }
   block_sync();
 
   float M = red_m[0];
@@ -139,6 +159,8 @@ __global__ void __launch_bounds__(MERGE_THREADS)
     if (before(t, d)) t = d;
   }
   const Cand tau = t;  // (-inf, max) when a group owns no list: everything survives
+  const float bnd = rb ? ord_val(bound_s) : -INFINITY;
+  auto survives = [&](const Cand &e) { return !before(tau, e) && e.v >= bnd; };
 
   // ---- survivors: per owned list, the prefix at or before tau
   int cnt[LISTS_PER_THREAD];
@@ -149,9 +171,9 @@ __global__ void __launch_bounds__(MERGE_THREADS)
     int k = 0;
     if (q < P) {
 #pragma unroll
-      for (int j = 0; j < HEAD; ++j) k += (k == j && !before(tau, hd[s][j])) ? 1 : 0;
+      for (int j = 0; j < HEAD; ++j) k += (k == j && survives(hd[s][j])) ? 1 : 0;
       if (k == HEAD)
-        while (k < T && !before(tau, list_at(q, k))) ++k;
+        while (k < T && survives(list_at(q, k))) ++k;
     }
     cnt[s] = k;
     c += k;
@@ -329,7 +351,7 @@ cudaError_t merge_t(const MergeLaunch &M, cudaStream_t s) {
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, merge_topk_kernel<T>, reinterpret_cast<const float2 *>(M.part_ms),
                          reinterpret_cast<const int2 *>(M.part_cand), M.R, M.P, M.topk, M.tk_logp, M.tk_tok, M.lse,
-                         M.vocab_ids, M.V_sub, M.V_full, M.status);
+                         M.vocab_ids, M.V_sub, M.V_full, M.status, M.rb, M.rb ? M.G : 0);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
