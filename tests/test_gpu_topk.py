@@ -279,15 +279,19 @@ def test_subset_head_rejects_ids_out_of_range():
     assert np.all(np_(a.tk_tok) == -1)
 
 
-TILE = 128  # vocabulary rows of one LM-head tile
-
-
-def _ranges(V: int) -> list[tuple[int, int]]:
-    """The LM head's vocabulary ranges at one M tile, as spans [t0, t1) of
-    128-row tiles: min(tiles, SMs) contiguous ranges (the split the library's
-    host code plans for R <= 128 rows)."""
+def _tile(V: int) -> int:
+    """Vocabulary rows of one LM-head tile at one M tile: 256, or 128 when
+    256-row tiles would leave SMs without one (the library's rule)."""
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
-    n_vt = -(-V // TILE)
+    return 256 if -(-V // 256) >= n_sm else 128
+
+
+def _ranges(V: int, tile: int) -> list[tuple[int, int]]:
+    """The LM head's vocabulary ranges at one M tile, as spans [t0, t1) of
+    tiles: min(tiles, SMs) contiguous ranges (the split the library's host
+    code plans for R <= 128 rows)."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    n_vt = -(-V // tile)
     P = min(n_vt, n_sm, 256)
     return [(r * n_vt // P, (r + 1) * n_vt // P) for r in range(P)]
 
@@ -299,14 +303,15 @@ def test_lmhead_ties_duplicate_rows(packed):
     Qwen3.5-4B", first paragraph: the B best prefixes, ties to the smaller
     ids; project page, How it works, step 3).  Groups of identical weight
     rows give exactly equal logits on both sides: (i) inside one range's
-    first 32 columns (the sorted first chunk), (ii) in different 128-row
-    tiles of one range, (iii) in different vocabulary ranges, and (iv) six
+    first 32 columns (the sorted first chunk), (ii) in different tiles of
+    one range, (iii) in different vocabulary ranges, and (iv) six
     copies across ranges with top-4, so the cut falls inside the tie.  Each
     hidden row points at one group, whose members are then its best
     logits."""
     V, H, topk = 51200, 128, 4
     rng = np.random.default_rng(31)
-    ranges = _ranges(V)
+    TILE = _tile(V)
+    ranges = _ranges(V, TILE)
     two = [rg for rg in ranges if rg[1] - rg[0] >= 2]
     assert two, "expected a range with two tiles"
     t2 = two[len(two) // 2]

@@ -9,17 +9,18 @@
 // whole cost, so the kernel reads W exactly once, with TMA, and keeps the
 // logits in tensor memory: they never reach global memory.
 //
-//   D[128 x 128] (TMEM, fp32) = h_tile[128 x H] . W_tile[128 x H]^T
+//   D[128 x BN] (TMEM, fp32) = h_tile[128 x H] . W_tile[BN x H]^T
 //
-// A = 128 hidden rows (one M tile, zero-filled past R), B = 128 vocabulary
-// rows, K streamed through a 6-stage shared-memory ring of one 64-element
-// (128-byte, swizzled) K atom each.  Each TMEM lane is one hidden row, so the
+// A = 128 hidden rows (one M tile, zero-filled past R), B = BN vocabulary
+// rows (256, or 128 when 256-row tiles would leave SMs idle), K streamed
+// through a shared-memory ring of one 64-element (128-byte, swizzled) K atom
+// per stage.  Each TMEM lane is one hidden row, so the
 // epilogue thread that owns lane r reads its row's logits column by column
 // and keeps the row's running max, running sum of exp and a sorted top-T in
 // registers -- no cross-thread reduction.
 //
 // Grid: persistent, one CTA per SM.  The vocabulary is split into P
-// contiguous ranges of 128-row tiles; work item = (range, M tile).  A CTA
+// contiguous ranges of BN-row tiles; work item = (range, M tile).  A CTA
 // writes, per row and range, (max, sum exp) and its T best (logit, id)
 // pairs; merge_topk (topk.cu) combines the P partials of a row.
 //
@@ -32,12 +33,9 @@
 // Roles (224 threads): warp 0 = TMA producer, warp 1 = MMA issuer (one
 // thread each), warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4)..),
 // warp 6 = the row bound's upkeep (one M tile; see the row bound below).
-// TMEM holds four 128-column fp32 accumulators, so that the MMAs can run up
-// to three tiles ahead of the epilogue: the epilogue of a range's first tile,
-// where the row's top-T fills and most columns enter it, takes longer than a
-// tile's stream, and with four accumulators the stream goes on meanwhile.
-// The exposed end, the last tile's epilogue after the last byte, is also
-// half of what a 256-row tile gave.
+// TMEM holds 512 / BN fp32 accumulators, so that the MMAs run ahead of the
+// epilogue while a range's first tile, where the row's top-T fills, is
+// worked through.
 //
 // FP8 form (project page, In a serving engine, Figure 5 caption: the
 // drafter's linear layers in FP8, quantized online): the weight is packed
@@ -66,11 +64,13 @@ constexpr int A_BYTES = KSUB * A_SUB;
 constexpr int THREADS = 224;
 constexpr int TMEM_COLS = 512;
 
-// Tile shape.  BN = 128 vocabulary rows (one M tile, the weight stream
-// bounds the head): four 128-column accumulators and a 6-stage ring of 32 KB
-// stages.  BN = 256 (several M tiles, tensor bound): two 256-column
-// accumulators, a 4-stage ring of 48 KB stages and half as many hidden-tile
-// loads per weight byte.
+// Tile shape.  BN = 256: two 256-column accumulators and a 4-stage ring of
+// 48 KB stages, two thirds of them weight.  A CTA streams about as many
+// bytes at once whatever the split, and at one M tile the weight's share of
+// them sets its rate.  Several M tiles also load the hidden tile half as
+// often per weight byte.  BN = 128: four 128-column accumulators and a
+// 6-stage ring of 32 KB stages, half of them weight, for vocabularies too
+// small to give every SM a 256-row tile.
 template <int BN_>
 struct Tile {
   static constexpr int BN = BN_;
@@ -849,7 +849,7 @@ cudaError_t launch_t(const LmheadLaunch &L, cudaStream_t stream) {
 
 }  // namespace
 
-int lmhead_tile_rows(int R) { return R <= BM ? 128 : 256; }
+int lmhead_tile_rows(int R, int V, int n_sm) { return R > BM || (V + 255) / 256 >= n_sm ? 256 : 128; }
 size_t lmhead_bound_bytes(int R, int T) {
   return R <= BM ? LMHEAD_BOUND_HEADER + ((size_t)R * T * 4 + 255) / 256 * 256 : 0;
 }
@@ -877,7 +877,8 @@ cudaError_t launch_bn(const LmheadLaunch &L, cudaStream_t stream) {
 }
 
 cudaError_t launch_lmhead_partials(const LmheadLaunch &L, cudaStream_t stream) {
-  return lmhead_tile_rows(L.R) == 128 ? launch_bn<128>(L, stream) : launch_bn<256>(L, stream);
+  if (L.tile_rows != lmhead_tile_rows(L.R, L.V, L.n_sm)) return cudaErrorInvalidValue;
+  return L.tile_rows == 128 ? launch_bn<128>(L, stream) : launch_bn<256>(L, stream);
 }
 
 size_t lmhead_packed_bytes(int V, int H) { return (size_t)((V + PK - 1) / PK) * PK * (size_t)H * 2; }

@@ -13,6 +13,7 @@ struct LmheadLaunch {
   int T;     // candidates kept per (row, range): 8, 16 or 32
   int P;     // vocabulary ranges (<= number of 256-row tiles)
   int n_sm;  // persistent grid size
+  int tile_rows;  // lmhead_tile_rows(R, V, n_sm)
   void *part_ms;    // float2 [R][P]
   void *part_cand;  // int2 [R][P][T]
   int32_t *status;
@@ -31,7 +32,10 @@ struct LmheadLaunch {
 
 size_t lmhead_bound_bytes(int R, int T);  // scratch of the row bound (0 when R > 128)
 constexpr size_t LMHEAD_BOUND_HEADER = 256;  // generation and ready words; the class maxima follow
-int lmhead_tile_rows(int R);  // vocabulary rows per tile for R hidden rows (128 for one M tile, else 256)
+// vocabulary rows per tile for R hidden rows, V vocabulary rows and n_sm
+// CTAs: 256, unless R fits one M tile and 256-row tiles would leave CTAs
+// without a tile (then 128)
+int lmhead_tile_rows(int R, int V, int n_sm);
 int lmhead_m_rows();     // hidden rows per M tile (128)
 int lmhead_k_chunk();    // K elements per pipeline stage (64)
 cudaError_t launch_lmhead_partials(const LmheadLaunch &L, cudaStream_t stream);

@@ -130,7 +130,8 @@ static long long best_ranges(int tiles, int n_groups, int workers, int *P_out) {
 
 TopkLayout lmhead_layout(int R, int V, int topk, int n_sm) {
   TopkLayout y;
-  const int tiles = (V + mfd::lmhead_tile_rows(R) - 1) / mfd::lmhead_tile_rows(R);
+  const int tile_rows = mfd::lmhead_tile_rows(R, V, n_sm);
+  const int tiles = (V + tile_rows - 1) / tile_rows;
   const int n_mt = (R + mfd::lmhead_m_rows() - 1) / mfd::lmhead_m_rows();
   y.P = tiles < n_sm ? tiles : n_sm;
   if (y.P > 256) y.P = 256;
@@ -339,7 +340,7 @@ int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int 
   } else if ((rc = tensor_map(h, R, H, mfd::lmhead_m_rows(), &mh)) != MFD_OK) {
     return rc;
   }
-  if (W && (rc = tensor_map(W, V, H, mfd::lmhead_tile_rows(R), &mw)) != MFD_OK) return rc;
+  if (W && (rc = tensor_map(W, V, H, mfd::lmhead_tile_rows(R, V, d.n_sm), &mw)) != MFD_OK) return rc;
   mfd::LmheadLaunch L;
   L.tmap_h = &mh;
   L.tmap_w = W ? &mw : nullptr;
@@ -350,6 +351,7 @@ int lmhead_call(const void *h, int R, int H, const void *W, const void *Wp, int 
   L.T = y.T;
   L.P = y.P;
   L.n_sm = d.n_sm;
+  L.tile_rows = mfd::lmhead_tile_rows(R, V, d.n_sm);
   L.part_ms = base + y.part_off;
   L.part_cand = base + y.part_off + y.ms_bytes;
   L.status = status;
