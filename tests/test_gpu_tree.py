@@ -161,6 +161,35 @@ def test_rejects_positive_or_unsorted_tables():
     assert st == mfd.MFD_ERR_INPUT
 
 
+@pytest.mark.parametrize("topk", [16, 5])
+@pytest.mark.parametrize("kind", ["dup", "nan", "unsorted", "positive"])
+@pytest.mark.parametrize("row", [0, 77, 119])
+def test_rejects_bad_entries_anywhere(topk, kind, row):
+    """The input checks cover every row of a full table, both rows a warp
+    checks at once, the last entry of a row and rows narrower than their
+    lane segment (top-5 in segments of 8): a repeated token, a NaN, an
+    unsorted pair or a positive log p anywhere is MFD_ERR_INPUT, and the
+    same tables without the fault build."""
+    rng = np.random.default_rng(40 + row)
+    lp, tk = _planted_tables(rng, 1, 8, 15, topk, 151936, 11)
+    _, st = gpu_tree(lp, tk, 64)
+    assert st == 0
+    k, i = divmod(row, 15)
+    j = topk - 1
+    lp2, tk2 = lp.copy(), tk.copy()
+    if kind == "dup":
+        tk2[0, k, i, j] = tk2[0, k, i, 0]
+    elif kind == "nan":
+        lp2[0, k, i, j] = np.nan
+    elif kind == "unsorted":
+        lp2[0, k, i, j] = lp2[0, k, i, j - 1] + 0.5
+        assert lp2[0, k, i, j] < 0
+    else:
+        lp2[0, k, i, j] = 0.25
+    _, st = gpu_tree(lp2, tk2, 64)
+    assert st == mfd.MFD_ERR_INPUT
+
+
 def test_rejects_out_of_limits():
     rd = mfd.Round(1, 17, 2, 4, 8, 64)
     with pytest.raises(mfd.MfdError) as e:
