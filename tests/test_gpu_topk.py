@@ -70,7 +70,11 @@ def test_logits_topk_ties():
 
 @pytest.mark.parametrize("R,H,V,topk", [
     (1, 64, 16, 1), (5, 64, 300, 8), (120, 128, 1000, 16), (128, 256, 4099, 32), (130, 64, 2305, 16),
-    (257, 192, 777, 8), (120, 2560, 20000, 16)])
+    (257, 192, 777, 8), (120, 2560, 20000, 16),
+    # vocabularies that give every SM a 256-row tile, with one residue class
+    # of the row bound (top-1), a top-k below its list width (5 of 8) and
+    # the widest list (32)
+    (64, 128, 40000, 1), (7, 256, 39000, 5), (128, 128, 50001, 32)])
 def test_lmhead_topk_small(R, H, V, topk):
     rng = np.random.default_rng(R + H + V)
     h = synth.bf16_round(rng.standard_normal((R, H)).astype(np.float32))
