@@ -431,3 +431,40 @@ def test_row_bound_every_logit_tied(packed, topk):
     np.testing.assert_allclose(lp, -np.log(V), atol=1e-4)
     o_lp, o_tok, _ = oracle.lmhead_topk(_bits(h), _bits(W), topk)
     assert (o_tok == np.arange(topk)[None, :]).all()
+
+
+def test_row_bound_under_graph_replay(head_2560):
+    """The LM head captured once in a CUDA graph and replayed with new hidden
+    rows each time: every replay clears the row bound behind a generation
+    that the replay itself advances on the device, so each gives the tables
+    of a direct call on those rows, bit for bit."""
+    W, Wd = head_2560
+    Wp = mfd.pack_lm_head(Wd)
+    hs = [synth.round_inputs(W, 8, 15, 11, seed=80 + i).h.cuda() for i in range(4)]
+    rd = mfd.Round(1, 8, 15, 16, 1, 151936)
+    h_static = torch.empty_like(hs[0])
+    h_static.copy_(hs[0])
+    rd.status.zero_()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        rd.lmhead_topk_packed(h_static, Wp)  # warm-up on a side stream, as before a capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        rd.lmhead_topk_packed(h_static, Wp)
+    ref = mfd.Round(1, 8, 15, 16, 1, 151936)
+    for i in (1, 2, 0, 3, 1):
+        h_static.copy_(hs[i])
+        rd.status.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert status_of(rd) == 0
+        ref.status.zero_()
+        ref.lmhead_topk_packed(hs[i], Wp)
+        torch.cuda.synchronize()
+        assert status_of(ref) == 0
+        np.testing.assert_array_equal(np_(rd.tk_tok), np_(ref.tk_tok))
+        np.testing.assert_array_equal(np_(rd.tk_logp).view(np.uint32), np_(ref.tk_logp).view(np.uint32))
+        np.testing.assert_array_equal(np_(rd.lse).view(np.uint32), np_(ref.lse).view(np.uint32))

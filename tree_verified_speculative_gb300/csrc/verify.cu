@@ -157,6 +157,12 @@ __global__ void __launch_bounds__(THREADS) verify_grid_kernel(const GridParams p
   // generation handshake (see the comment on the result words)
   // done by the last warp, so that warp 0's loads go out first; warp 0 takes
   // G from shared memory after the first block barrier
+  // The tree and the target rows may come from the grids just before; the
+  // next grid may start its prologue now (it waits for this one to end).
+  // No CTA waits on another before the grid before has ended and freed its
+  // SMs for the rest of this (cooperative) grid.
+  pdl_wait();
+  pdl_launch_dependents();
   bool acquired = false;  // this CTA has taken the ready words it reads
   unsigned long long rdy[POLL_SLOTS];  // ready words read early (warp 0)
 #pragma unroll
@@ -715,11 +721,13 @@ static cudaError_t launch_grid(const VerifyLaunch &V, cudaStream_t stream) {
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, verify_grid_kernel, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
