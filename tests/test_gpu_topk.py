@@ -292,11 +292,16 @@ def _tile(V: int) -> int:
 
 def _ranges(V: int, tile: int) -> list[tuple[int, int]]:
     """The LM head's vocabulary ranges at one M tile, as spans [t0, t1) of
-    tiles: min(tiles, SMs) contiguous ranges (the split the library's host
-    code plans for R <= 128 rows)."""
+    tiles: min(tiles, SMs) contiguous ranges, or, when at most three quarters
+    of those would hold the largest share, the fewest ranges with the same
+    largest share (the split the library's host code plans for R <= 128
+    rows)."""
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     n_vt = -(-V // tile)
     P = min(n_vt, n_sm, 256)
+    most = -(-n_vt // P)
+    if 4 * (n_vt - (most - 1) * P) <= 3 * P:
+        P = -(-n_vt // most)  # the fewest ranges with the same largest range
     return [(r * n_vt // P, (r + 1) * n_vt // P) for r in range(P)]
 
 
@@ -316,14 +321,15 @@ def test_lmhead_ties_duplicate_rows(packed):
     rng = np.random.default_rng(31)
     TILE = _tile(V)
     ranges = _ranges(V, TILE)
-    two = [rg for rg in ranges if rg[1] - rg[0] >= 2]
+    rg = lambda i: ranges[i * len(ranges) // 152]  # noqa: E731  (a range by its place among 152)
+    two = [r_ for r_ in ranges if r_[1] - r_[0] >= 2]
     assert two, "expected a range with two tiles"
     t2 = two[len(two) // 2]
     groups = [
-        [ranges[5][0] * TILE + 3, ranges[5][0] * TILE + 17, ranges[5][0] * TILE + 30],
+        [rg(5)[0] * TILE + 3, rg(5)[0] * TILE + 17, rg(5)[0] * TILE + 30],
         [t2[0] * TILE + 100, (t2[0] + 1) * TILE + 7],
-        [ranges[0][0] * TILE + 120, ranges[40][0] * TILE + 5, ranges[100][0] * TILE + 127, ranges[-1][0] * TILE + 1],
-        [ranges[i][0] * TILE + 11 * i % TILE for i in (2, 30, 31, 77, 120, 151 % len(ranges))],
+        [ranges[0][0] * TILE + 120, rg(40)[0] * TILE + 5, rg(100)[0] * TILE + 127, ranges[-1][0] * TILE + 1],
+        [rg(i)[0] * TILE + 11 * i % TILE for i in (2, 30, 31, 77, 120, 151)],
     ]
     members = [v for g in groups for v in g]
     assert len(set(members)) == len(members) and max(members) < V
