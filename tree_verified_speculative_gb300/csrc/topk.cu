@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(MERGE_THREADS)
                       const int *__restrict__ rb, int G_rb) {
   __shared__ Cand surv[SURV_CAP];
   __shared__ Cand top[32];
+  __shared__ int top_tok[32];  // a top entry's output token: its vocabulary id on a subset
   __shared__ Cand gbest[MERGE_WARPS][32];
   __shared__ float red_m[MERGE_WARPS], red_s[MERGE_WARPS];
   __shared__ int n_surv_s;
@@ -197,6 +198,8 @@ __global__ void __launch_bounds__(MERGE_THREADS)
     // ordered by slot)
     for (int a = tid; a < n_surv; a += MERGE_THREADS) {
       const Cand e = surv[a];
+      // a subset row's vocabulary id, loaded while the rank is counted
+      const int tok = vocab_ids ? ((e.i >= 0 && e.i < V_sub) ? __ldg(vocab_ids + e.i) : -1) : e.i;
       int r0 = 0, r1 = 0;
       int b = 0;
       for (; b + 1 < n_surv; b += 2) {
@@ -209,7 +212,10 @@ __global__ void __launch_bounds__(MERGE_THREADS)
         r0 += before(f, e) || (f.v == e.v && f.i == e.i && b < a);
       }
       const int r = r0 + r1;
-      if (r < topk) top[r] = e;
+      if (r < topk) {
+        top[r] = e;
+        top_tok[r] = tok;
+      }
     }
   } else if (warp == 0) {
     // many exact ties at the cut: topk rounds of "best remaining list head"
@@ -237,7 +243,10 @@ __global__ void __launch_bounds__(MERGE_THREADS)
         for (int s = 0; s < 8; ++s)
           if (s == bs) ++pos[s];
       }
-      if (lane == 0) top[r] = w;
+      if (lane == 0) {
+        top[r] = w;
+        top_tok[r] = vocab_ids ? ((w.i >= 0 && w.i < V_sub) ? __ldg(vocab_ids + w.i) : -1) : w.i;
+      }
     }
   }
   block_sync();
@@ -251,15 +260,12 @@ __global__ void __launch_bounds__(MERGE_THREADS)
       if (o == tid) continue;
       r2 += vi_before(top[o].v - lse, top[o].i, lp, e.i);
     }
-    int tok = e.i;
-    if (vocab_ids) {
-      // a subset row index back to its vocabulary id; the table is
-      // increasing, so (log p desc, subset index asc) is (log p desc, id asc)
-      tok = (tok >= 0 && tok < V_sub) ? __ldg(vocab_ids + tok) : -1;
-      if (tok < 0 || tok >= V_full) {
-        report(status, MFD_ERR_INPUT);
-        tok = -1;
-      }
+    // on a subset, the row index's vocabulary id; the table is increasing,
+    // so (log p desc, subset index asc) is (log p desc, id asc)
+    int tok = top_tok[tid];
+    if (vocab_ids && (tok < 0 || tok >= V_full)) {
+      report(status, MFD_ERR_INPUT);
+      tok = -1;
     }
     tk_logp[(size_t)row * topk + r2] = lp;
     tk_tok[(size_t)row * topk + r2] = tok;
